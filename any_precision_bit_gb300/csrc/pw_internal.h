@@ -1,0 +1,155 @@
+// pw_internal.h -- structures and index maps shared by the host runtime and the kernels.
+//
+// Kernel-private plane tiling (the ABI layout is restored by pw_unpack_indices):
+//   A block's rows are grouped in 16-row tiles.  For a gate_up block a tile holds 8 gate
+//   rows followed by the 8 up rows of the same 8 features, so that one warp's MMA tile
+//   yields gate and up of a feature in the same thread.  Columns are grouped in chunks of
+//   128 (the plane row is zero-padded to a multiple of 128 bits).  One (tile, chunk) pair
+//   of a plane is 64 uint32 words: word (lane * 2 + r) belongs to thread `lane` of the
+//   warp and row (g + 8r) of the tile, g = lane / 4; its bit (8e + s) holds column
+//   16 s + kofs(c, e) of the chunk, c = lane % 4, kofs = {2c, 2c+1, 2c+8, 2c+9}[e].
+//   These are exactly the elements of the m16n8k16 A fragment that thread holds for the
+//   eight 16-column steps s of the chunk.
+#pragma once
+#include <stdint.h>
+
+#ifdef __CUDACC__
+#define PW_HD __host__ __device__ __forceinline__
+#else
+#define PW_HD inline
+#endif
+
+namespace pw {
+
+constexpr int kMaxPlanes = 8;
+constexpr int kTileRows = 16;     // rows per warp tile
+constexpr int kChunkCols = 128;   // columns per plane chunk
+constexpr int kWarpsPerCta = 4;   // warp tiles per CTA tile in the decode kernels
+constexpr int kCtaRows = kTileRows * kWarpsPerCta;
+constexpr int kTokChunk = 64;     // tokens per work item in the decode kernels
+
+// One row of the device weight page table (PagedWeight Sec. 3.1).  The kernels read q and
+// the pointers of the block they run; commits rewrite the whole row between launches.
+struct BlockDev {
+  const uint32_t *plane[kMaxPlanes];  // tiled bit-planes (poison page when not resident)
+  const uint16_t *lut[9];             // LUT_b in device row order (poison page when absent)
+  int q;                              // committed bitwidth
+  int N, K, KC;                       // rows, columns, 128-column chunks
+};
+
+// A unit of work of the decode expert kernels.
+struct WorkItem {
+  int kind;    // 0 routed expert, 1 shared expert
+  int expert;  // routed expert id (kind 0)
+  int tile;    // CTA row tile (kCtaRows rows)
+  int tok0;    // first slot (routed: into the expert-sorted pair list; shared: token)
+  int ntok;    // tokens in this item (<= kTokChunk)
+};
+
+PW_HD int kpad_cols(int K) { return (K + kChunkCols - 1) / kChunkCols * kChunkCols; }
+
+// device row of an original row (u = 0 gate_up with I features, u = 1 identity)
+PW_HD int dev_row(int r, int u, int I) {
+  if (u != 0) return r;
+  int half = r >= I ? 1 : 0;
+  int f = half ? r - I : r;
+  return (f / 8) * 16 + half * 8 + (f % 8);
+}
+PW_HD int orig_row(int d, int u, int I) {
+  if (u != 0) return d;
+  int rt = d / 16, ri = d % 16;
+  int f = rt * 8 + (ri % 8);
+  return (ri >= 8) ? I + f : f;
+}
+
+// word index inside a tiled plane and bit inside that word for (device row d, column k)
+PW_HD void tile_pos(int d, int k, int KC, int *word, int *bit) {
+  int rt = d / 16, ri = d % 16;
+  int g = ri % 8, r = ri / 8;
+  int kc = k / 128, kk = k % 128;
+  int s = kk / 16, kin = kk % 16;
+  int c = (kin % 8) / 2;
+  int e = (kin & 1) + 2 * (kin / 8);
+  int lane = 4 * g + c;
+  *word = ((rt * KC + kc) * 32 + lane) * 2 + r;
+  *bit = 8 * e + s;
+}
+
+// Kernel-private layout of dense bf16 shared-expert weights (N x K, K % 16 == 0):
+// per 16-row tile and 16-column step, thread `lane` holds 4 words = its m16n8k16 A
+// fragment: (g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..2c+9), (g+8, 2c+8..).
+PW_HD long frag16_index(int d, int k, int K) {
+  int rt = d / 16, ri = d % 16;
+  int g = ri % 8, r = ri / 8;
+  int st = k / 16, kin = k % 16;
+  int c = (kin % 8) / 2;
+  int hi = kin / 8;
+  int lane = 4 * g + c;
+  int reg = r + 2 * hi;  // 0: (g,lo) 1: (g+8,lo) 2: (g,hi) 3: (g+8,hi)
+  long word = ((long)(rt * (K / 16) + st) * 32 + lane) * 4 + reg;
+  return word * 2 + (kin & 1);  // element index (bf16 units)
+}
+
+}  // namespace pw
+
+// ------------------------------------------------------------------ kernel launchers
+// Implemented in the .cu files; called by the host runtime.  Each returns a cudaError_t
+// value as int.
+namespace pw {
+
+struct Scratch {
+  float *logits;       // [Tm][E]
+  int *ids;            // [Tm][K]
+  float *w;            // [Tm][K]
+  int *counts;         // [E]
+  int *offsets;        // [E + 1]
+  int *slot_tok;       // [Tm*K] token of each expert-sorted slot
+  int *pair_slot;      // [Tm*K] slot of pair (t, k)
+  float *slot_w;       // [Tm*K] routing weight of each slot
+  WorkItem *items1;    // gate_up work
+  WorkItem *items2;    // down work
+  int *n_items;        // [2]
+  unsigned *ticket;    // [1] last-CTA counter of the router
+  uint16_t *h_routed;  // fp16 [Tm*K][I]
+  uint16_t *h_shared;  // bf16 [Tm][Is]
+  float *o_routed;     // [Tm*K][H]
+  float *o_shared;     // [Tm][H]
+  float *inv_rms;      // [Tm] per-token 1/rms of the layer input (PW_PRENORM)
+  double *stat_count;  // [L][E]
+  double *stat_wsum;   // [L][E]
+  int max_items1, max_items2;
+};
+
+struct LayerDev {
+  const float *Wr;         // [E][H]
+  const float *bias;       // [E] or null
+  const uint16_t *wgu;     // shared gate_up, frag16 layout (dev rows interleaved)
+  const uint16_t *wd;      // shared down, frag16 layout
+};
+
+struct FwdArgs {
+  int layer, T, E, H, I, K, Is, renorm, flags;
+  const BlockDev *table;  // device page table
+  LayerDev lay;
+  Scratch s;
+  const uint16_t *x;      // bf16 [T][H]
+  uint16_t *y;            // bf16 [T][H]
+  int *ids_out;           // optional
+  float *w_out;           // optional
+  int sm_count;
+};
+
+// ev: null, or five timing events recorded before, between and after the four kernels
+int launch_forward(const FwdArgs &a, void *stream, void *const *ev);
+int launch_commit(BlockDev *table, int block, const BlockDev &val, void *stream);
+int launch_pack(const uint8_t *idx, int N, int K, int KC, int u, int I, int bmax,
+                uint32_t *const *plane_out, void *stream);
+int launch_lut_permute(const uint16_t *lut_in, int N, int entries, int u, int I,
+                       uint16_t *lut_out, void *stream);
+int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_out,
+                  void *stream);
+int launch_unpack(const BlockDev *table, int block, int b, int u, int I, int N, int KC,
+                  uint8_t *idx_out, uint16_t *w_out, void *stream);
+int launch_fill_u32(uint32_t *p, uint32_t v, long n, void *stream);
+
+}  // namespace pw

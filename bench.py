@@ -1,0 +1,350 @@
+#!/usr/bin/env python3
+"""Throughput of the fused mixed-precision Any-Precision MoE layer stack on GB300.
+
+Workload (default): the Qwen1.5-MoE-A2.7B-shaped stack -- hidden 2048, 60 routed experts
+of intermediate 1408, top-4, a dense bf16 shared FFN of intermediate 5632, 24 layers,
+8 bit-planes per block with bitwidths 3..8 (experts in the top quarter of the Zipf(1.1)
+router prior at 5..8 bits, the rest at 3..4) -- decoding a batch of T tokens.  A step is
+one pass of the whole stack over one batch: in every layer the router, top-K, bucketing,
+gate_up (SiLU*up), down and combine kernels, x <- x + layer(x).  Inputs are synthetic and
+seeded; the step's weights (~6 GB) are far larger than L2.
+
+Prints one JSON line.  ``--impl reference`` times the float64 CPU oracle instead, on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as syn  # noqa: E402
+
+METRIC = "MoE-layer tokens/s (T*L / stack time); weight-read HBM GB/s vs GB300 peak at mixed per-block bits"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="qwen", choices=["qwen", "mixtral", "g128"])
+    ap.add_argument("--tokens", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=0, help="0 = the configuration's layer count")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def workload_config(shape, T, L):
+    return {
+        "workload": f"{shape.name}-shaped MoE stack decode: {L} layers, T={T} tokens",
+        "model_shape": {"H": shape.H, "E": shape.E, "I": shape.I, "K": shape.K, "Is": shape.Is,
+                        "bmax": shape.bmax, "bits": list(shape.bits), "q_rule": shape.q_rule},
+        "T": T, "layers": L,
+        "l2": "inputs larger than L2 (every step streams the whole stack's resident planes)",
+    }
+
+
+# ---------------------------------------------------------------- clocks
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- workload set-up
+def load_stack(pw, torch, shape, L, T, seed, device):
+    from synthetic.gen_torch import gen_block_torch, gen_shared_torch
+    d = pw.pw_desc(L=L, E=shape.E, H=shape.H, I=shape.I, K=shape.K, Is=shape.Is, bmax=shape.bmax,
+                   bits_mask=shape.bits_mask(), renorm=0, device=device, max_tokens=T, flags=0)
+    ctx = pw.pw_create(d)
+    qs = []
+    for l in range(L):
+        Wr, bias, ranks = syn.gen_router_np(shape, seed, l)
+        pw.pw_set_router(ctx, l, Wr, bias)
+        q = syn.gen_q_assignment(shape, seed, l, ranks)
+        qs.append(q)
+        if shape.Is:
+            wgu, wd = gen_shared_torch(shape, seed, l)
+            torch.cuda.synchronize()
+            pw.pw_set_shared(ctx, l, wgu, wd)
+            del wgu, wd
+        for e in range(shape.E):
+            for u in (0, 1):
+                idx, lut = gen_block_torch(shape, seed, l, e, u)
+                torch.cuda.synchronize()
+                pw.pw_pack(ctx, l, e, u, idx, lut, int(q[e, u]))
+                del idx, lut
+    return ctx, qs
+
+
+def layer_bytes(shape, q, counts, T):
+    """Algorithmic bytes of one layer: the active blocks' q planes + LUT_q, the shared FFN,
+    the router and the activations in and out."""
+    def read_bytes(N, K, b):  # b planes of N rows x ceil(K/128)*128 bits, plus LUT_b (2^b fp16 per row)
+        return b * N * ((K + 127) // 128 * 128) // 8 + N * (1 << b) * 2
+    gu = dn = 0
+    for e in np.nonzero(counts)[0]:
+        N, K = syn.block_shape(shape, 0)
+        gu += read_bytes(N, K, int(q[e, 0]))
+        N, K = syn.block_shape(shape, 1)
+        dn += read_bytes(N, K, int(q[e, 1]))
+    sh_gu = 2 * shape.Is * shape.H * 2
+    sh_dn = shape.H * shape.Is * 2
+    router = shape.E * shape.H * 4
+    act = 2 * T * shape.H * 2
+    return dict(gu=gu, dn=dn, sh_gu=sh_gu, sh_dn=sh_dn, router=router, act=act,
+                total=gu + dn + sh_gu + sh_dn + router + act, weights=gu + dn + sh_gu + sh_dn)
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_sample(shape, seed, T_sample, device_gen=True):
+    """Layer 0 of the workload on the host: router, shared weights and the routed experts of
+    the first T_sample tokens, drawn with the same generator keys as the GPU run."""
+    from oracle import moe as omoe
+    from synthetic.gen_torch import gen_block_torch, gen_shared_torch, split_luts
+    Wr, bias, ranks = syn.gen_router_np(shape, seed, 0)
+    q = syn.gen_q_assignment(shape, seed, 0, ranks)
+    x = syn.gen_tokens_np(shape, seed, 0, T_sample)
+    ids, _, _ = omoe.route(x, Wr, bias, shape.K)
+    experts = {}
+    for e in np.unique(ids):
+        blk = []
+        for u in (0, 1):
+            idx, lut = gen_block_torch(shape, seed, 0, int(e), u)
+            N, _ = syn.block_shape(shape, u)
+            blk += [idx.cpu().numpy(), split_luts(lut.cpu().numpy(), N, shape.bits)]
+        experts[int(e)] = tuple(blk)
+    shared = None
+    if shape.Is:
+        wgu, wd = gen_shared_torch(shape, seed, 0)
+        shared = (wgu.cpu().numpy().view(np.uint16), wd.cpu().numpy().view(np.uint16))
+    return x, Wr, bias, experts, q, shared
+
+
+def time_oracle(shape, sample, reps=1):
+    from oracle import moe as omoe
+    x, Wr, bias, experts, q, shared = sample
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        omoe.moe_layer(x, Wr, bias, experts, q, shape.K, shape.bmax, shared=shared)
+    return (time.perf_counter() - t0) / reps
+
+
+# ---------------------------------------------------------------- arms
+def run_reference(args, shape, L, T):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    T_sample = min(T, 4)
+    sample = oracle_sample(shape, args.seed, T_sample)
+    for _ in range(args.warmup):
+        time_oracle(shape, sample)
+    t = sum(time_oracle(shape, sample) for _ in range(args.steps)) / args.steps
+    value = T_sample * 1 / t
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(shape, T, L),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"layer 0 of {L}, first {T_sample} of {T} tokens per step (float64 numpy oracle)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, shape, L, T):
+    import torch
+    import any_precision_bit_gb300 as pw
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from any_precision_bit_gb300 import _build
+    _build.build()
+    t_setup = time.time()
+    ctx, qs = load_stack(pw, torch, shape, L, T, args.seed, local)
+    t_setup = time.time() - t_setup
+    stream = torch.cuda.Stream()
+    pw.pw_set_stream(ctx, stream)
+    x0 = torch.from_numpy(syn.gen_tokens_np(shape, args.seed, 0, T).view(np.int16)).cuda()
+    xw = torch.empty_like(x0)
+    torch.cuda.synchronize()
+    pw.pw_set_profiling(ctx, 1)
+
+    def step():
+        xw.copy_(x0)
+        pw.pw_stack_forward(ctx, xw, T, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.synchronize()
+    for l in range(L):
+        pw.pw_routing_stats(ctx, l, shape.E, reset=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clk = clocks.stop()
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    # kernel durations of the last timed step, per layer
+    kern = np.array([pw.pw_profile_read(ctx, l) for l in range(L)], dtype=np.float64)  # [L][4] ms
+    bytes_l = []
+    for l in range(L):
+        cnt, _ = pw.pw_routing_stats(ctx, l, shape.E)
+        bytes_l.append(layer_bytes(shape, qs[l], cnt, T))
+    tot = {k: sum(b[k] for b in bytes_l) for k in bytes_l[0]}
+    value = world * T * L / (ms * 1e-3)
+    peak, peak_kind = peaks()
+    # dominant kernel: the one with the largest share of the step
+    share = kern.sum(axis=0) / kern.sum()
+    names = ["route_kernel", "ffn_kernel<1> (gate_up + SiLU*up)", "ffn_kernel<2> (down)", "combine_kernel"]
+    dom = int(np.argmax(share))
+    dom_bytes = {1: tot["gu"] + tot["sh_gu"] + T * shape.H * 2 * L,
+                 2: tot["dn"] + tot["sh_dn"],
+                 0: tot["router"] + T * shape.H * 2 * L,
+                 3: T * shape.H * 2 * L}[dom]
+    dom_ms = kern[:, dom].sum()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                "algorithmic_bytes_per_launch": dom_bytes / L, "avg_launch_ms": dom_ms / L,
+                "kernel_share": {n: float(s) for n, s in zip(names, share)}}
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": workload_config(shape, T, L),
+        "stack_tokens_per_s": world * T / (ms * 1e-3),
+        "gbs": tot["total"] / (ms * 1e-3) / 1e9, "weight_gbs": tot["weights"] / (ms * 1e-3) / 1e9,
+        "routed_gbs": (tot["gu"] + tot["dn"]) / (ms * 1e-3) / 1e9,
+        "hbm_frac": tot["total"] / (ms * 1e-3) / 1e9 / peak,
+        "bytes_per_step": tot["total"], "roofline": roofline, "clocks": clk,
+        "gpu_launches": 4 * L * args.steps, "setup_s": round(t_setup, 1),
+    }
+    # end to end through the C ABI with pinned host buffers
+    if not args.no_e2e:
+        xh = torch.from_numpy(syn.gen_tokens_np(shape, args.seed, 0, T).view(np.int16)).pin_memory()
+        yh = torch.empty_like(xh).pin_memory()
+        pw.pw_stack_forward_host(ctx, xh, T, yh)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pw.pw_stack_forward_host(ctx, xh, T, yh)
+        te = (time.perf_counter() - t0) / args.steps
+        line["e2e"] = {"value": world * T * L / te, "unit": "tokens/s", "ms_per_step": te * 1e3,
+                       "h2d_bytes_per_step": T * shape.H * 2, "d2h_bytes_per_step": T * shape.H * 2}
+    if rank == 0 and not args.no_cpu_baseline:
+        sample = oracle_sample(shape, args.seed, T)
+        t = time_oracle(shape, sample)
+        line["cpu_baseline"] = {"value": T / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"layer 0 of {L}, all {T} tokens, one pass of the float64 numpy "
+                                          f"oracle ({t:.1f} s); BLAS may use every core, the rest runs on one"}
+    pw.pw_destroy(ctx)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    shape = syn.SHAPES[args.config]
+    L = args.layers or shape.L
+    T = args.tokens
+    if args.impl == "reference":
+        run_reference(args, shape, L, T)
+    else:
+        run_ours(args, shape, L, T)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,310 @@
+/*
+ * pw.h -- C ABI of libpw.so: a GB300-native (sm_103a) fused mixed-precision MoE layer
+ * that reads Any-Precision bit-planes and per-row centroid LUTs directly, with a
+ * device-resident weight page table, asynchronous page offload/reload and a greedy
+ * quality-aware planner.
+ *
+ * Source of every operation: "PagedWeight: Efficient MoE LLM Serving with Dynamic
+ * Quality-Aware Weight Quantization" (arXiv 2607.16184).
+ *
+ * Conventions shared by every call
+ *   - Every call returns pw_status; nothing throws across the ABI.  pw_last_error()
+ *     gives a message for the last failing call on a context (or, with ctx == NULL,
+ *     on the calling thread).
+ *   - A CUDA error met asynchronously (a failed kernel or copy) is sticky: the next call
+ *     on the same context returns PW_ERR_CUDA.
+ *   - Host inputs are copied; the caller keeps ownership.  Device pointers handed to a
+ *     call (x, y, ids, w) are borrowed and must stay valid until the stream reaches the
+ *     work.  The context owns planes, LUTs, the page table, pinned host pages and scratch.
+ *   - A context is used by one host thread at a time.
+ *   - Linear block i = (layer, expert, u), u = 0 gate_up, 1 down, is addressed by the
+ *     block id (layer * E + expert) * 2 + u.
+ *   - A gate_up block has N = 2*I rows (gate rows 0..I-1, then up rows I..2I-1) and K = H
+ *     columns; a down block has N = H rows and K = I columns.
+ *   - Bitwidths: a block stores bmax <= 8 bit-planes, plane 0 the most significant bit,
+ *     so a b-bit code is the top b planes.  Supported bitwidths are the set bits of
+ *     bits_mask (each between 1 and bmax).  A LUT for bitwidth b holds 2^b fp16
+ *     centroids per output row.
+ *   - Page p of a block is bit-plane p together with LUT_{p+1} when p+1 is supported.
+ *     At committed bitwidth q the GPU holds planes 0..q-1 and LUT_c for supported c <= q;
+ *     M^b (Eq. 3 of the paper) counts exactly those bytes.
+ */
+#ifndef PW_H
+#define PW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PW_OK = 0,
+    PW_ERR_INVALID = 1, /* bad argument: nothing was changed */
+    PW_ERR_CUDA = 2,    /* a CUDA call failed (message in pw_last_error) */
+    PW_ERR_OOM = 3,     /* device or pinned-host memory exhausted: nothing was changed */
+    PW_ERR_STATE = 4,   /* the page state forbids the request (e.g. a page in transfer) */
+    PW_ERR_TIMEOUT = 5, /* a bounded device wait gave up */
+    PW_ERR_BUSY = 6     /* an earlier transfer of the same block has not landed yet */
+} pw_status;
+
+typedef struct pw_ctx pw_ctx;
+typedef void *pw_stream; /* a cudaStream_t; NULL means the legacy default stream */
+
+enum {
+    PW_FLAG_POISON = 1 /* fill retired device pages with 0xFF before reuse (testing) */
+};
+
+enum {
+    PW_ACCUMULATE = 1, /* pw_moe_forward: y <- bf16(y + layer(x)); y may alias x */
+    PW_PRENORM = 2     /* the layer reads RMSNorm(x) = x / sqrt(mean_h x^2 + 1e-6) (unit gain), the
+                          way the pre-norm models of the paper's Table 1 feed their MoE blocks */
+};
+
+typedef struct {
+    int L, E, H, I, K; /* layers, routed experts, hidden, expert intermediate, top-K */
+    int Is;            /* shared-expert intermediate; 0 = no shared expert */
+    int bmax;          /* bit-planes per block, 1..8 */
+    uint32_t bits_mask;/* bit b set <=> bitwidth b supported */
+    int renorm;        /* 1: routing weights renormalised over the chosen K */
+    int device;        /* CUDA device ordinal */
+    int max_tokens;    /* largest T accepted by the forward calls */
+    int flags;         /* PW_FLAG_* */
+} pw_desc;
+
+/* ---------------------------------------------------------------- lifetime */
+
+/* Create a context on desc->device.  Requires H % 16 == 0, I % 8 == 0, Is % 8 == 0,
+ * K <= E <= 256, K <= 8.  Allocates the page table, scratch for max_tokens tokens and
+ * the two streams (compute stream = a new non-blocking stream, side stream for page
+ * copies).  Errors: PW_ERR_INVALID on bad shapes, PW_ERR_CUDA / PW_ERR_OOM otherwise. */
+pw_status pw_create(const pw_desc *desc, pw_ctx **out);
+void pw_destroy(pw_ctx *ctx);
+const char *pw_last_error(const pw_ctx *ctx);
+const char *pw_version(void);
+
+/* Stream on which commits (pw_set_bits, pw_offload's lowering, pw_commit's raising) and
+ * the context's own copies are enqueued; by default a non-blocking stream the context
+ * created.  Forward calls should run on the same stream so that a commit lands between
+ * launches (PagedWeight Sec. 3.3: commit only at safe boundaries).  Switching waits for
+ * the previous stream.  The caller keeps ownership of a stream it sets. */
+pw_status pw_set_stream(pw_ctx *ctx, pw_stream stream);
+pw_status pw_get_stream(pw_ctx *ctx, pw_stream *stream);
+
+/* ---------------------------------------------------------------- weights */
+
+/* Pack one linear block (PagedWeight Sec. 3.1 paged weight representation; APL overlaid
+ * bit-planes, Sec. 2.2).
+ *   idx: uint8 [N][K] codes < 2^bmax, row-major.
+ *   lut: fp16 bits, the LUTs of every supported b in ascending b, concatenated:
+ *        [N][2^b] for the smallest b, then the next, ...; entries in any order.
+ *   q_init: initial committed bitwidth (supported).
+ * idx and lut may both be host memory or both be device memory (detected).  Pages
+ * 0..q_init-1 become GPU-resident, the rest CPU-resident in pinned host memory.
+ * Re-packing a block replaces it (its pages must not be in transfer: PW_ERR_BUSY).
+ * The device copy uses a kernel-private tiling of each plane; pw_unpack_indices
+ * reproduces the plain codes. */
+pw_status pw_pack(pw_ctx *ctx, int layer, int expert, int u, const uint8_t *idx,
+                  const uint16_t *lut, int q_init);
+
+/* Router of a layer (Sec. 2.1): Wr fp32 [E][H]; bias fp32 [E] or NULL.
+ * Host or device pointers (detected). */
+pw_status pw_set_router(pw_ctx *ctx, int layer, const float *Wr, const float *bias);
+
+/* Shared expert of a layer (Table 1 counts shared experts): wgu bf16 bits [2*Is][H]
+ * (gate rows, then up rows), wd bf16 bits [H][Is].  Host or device pointers. */
+pw_status pw_set_shared(pw_ctx *ctx, int layer, const uint16_t *wgu, const uint16_t *wd);
+
+/* ---------------------------------------------------------------- forward */
+
+/* One fused MoE layer (Sec. 3.3 "fused mixed-precision MoE kernel"): router logits in
+ * fp32, softmax over E, top-K (ties to the lower expert id, listed by descending
+ * probability), token-to-expert bucketing, gate_up with SiLU(gate)*up, down projection
+ * and the routing-weighted combine y_t = sum_k r_tk o_tk (k order), plus the shared
+ * expert.  Each block is read at the committed bitwidth q_i held in the device page
+ * table when the launch runs.
+ *   x: device bf16 [T][H]; y: device bf16 [T][H] (with PW_ACCUMULATE, y += layer(x);
+ *   y may equal x).  ids (int32 [T][K]) and w (fp32 [T][K]) are optional device
+ *   outputs (NULL to skip).  1 <= T <= max_tokens.  Asynchronous on `stream`; no host
+ *   synchronisation and no allocation, so it can be captured in a CUDA graph.
+ * Activations are handled in fp16 inside the expert kernels: |x| and |h| must stay
+ * below 65504. */
+pw_status pw_moe_forward(pw_ctx *ctx, int layer, const void *x, int T, void *y,
+                         int32_t *ids, float *w, int flags, pw_stream stream);
+
+/* The whole stack in place: for l = 0..L-1, x <- bf16(x + layer_l(RMSNorm(x))), i.e.
+ * pw_moe_forward with PW_ACCUMULATE | PW_PRENORM and y = x.  x: device bf16 [T][H].  Asynchronous; launched as a CUDA graph replay after the first call
+ * for a given (x, T, stream). */
+pw_status pw_stack_forward(pw_ctx *ctx, void *x, int T, pw_stream stream);
+
+/* End-to-end variant with host buffers: copies x_host (bf16 [T][H]) to the device,
+ * runs pw_stack_forward, copies the result to y_host and waits for it.  Pinned host
+ * buffers give full copy bandwidth; pageable ones work too. */
+pw_status pw_stack_forward_host(pw_ctx *ctx, const void *x_host, int T, void *y_host);
+
+/* Online routing statistics (Sec. 3.2 "Routing statistics"): per expert of `layer`, the
+ * number of (token, k) selections and the sum of their routing weights since the last
+ * reset, accumulated by every forward call.  Outputs are host double [E].  Waits for
+ * the compute stream. */
+pw_status pw_routing_stats(pw_ctx *ctx, int layer, double *count, double *weight_sum,
+                           int reset);
+
+/* Tracing: while on, every forward records five CUDA timing events per layer, before,
+ * between and after its four kernels (router, gate_up, down, combine), on the launch
+ * stream; stack graphs captured while on contain the event records.  The events are
+ * owned by the context.  pw_profile_read waits for the latest recording of `layer` and
+ * writes the four kernel durations in milliseconds to ms[0..3]. */
+pw_status pw_set_profiling(pw_ctx *ctx, int on);
+pw_status pw_profile_read(pw_ctx *ctx, int layer, float *ms);
+
+/* ---------------------------------------------------------------- page table */
+
+enum { PW_PAGE_GPU = 0, PW_PAGE_CPU = 1, PW_PAGE_TO_CPU = 2, PW_PAGE_TO_GPU = 3 };
+
+typedef struct {
+    int layer, expert, u;
+    int N, K;
+    int q;          /* committed bitwidth (read by the kernels) */
+    int d;          /* desired bitwidth (set by the planner and by offload/reload) */
+    int pending_q;  /* reload target waiting for its pages, or 0 */
+    int state[8];   /* PW_PAGE_* per page 0..bmax-1 */
+    int64_t M[9];   /* M^b bytes for b = 0..8 (-1 when b is not supported) */
+} pw_block_info;
+
+/* Commit bitwidth q for a block now (stream-ordered write of the device table entry on
+ * the ctx stream).  Every page below q must be GPU-resident and no transfer pending,
+ * else PW_ERR_STATE. */
+pw_status pw_set_bits(pw_ctx *ctx, int block, int q);
+
+/* Offload (Sec. 3.1, Sec. 3.3): lower the committed bitwidth of `block` to q_new first
+ * (enqueued on the ctx stream), then copy pages q_new..q-1 to pinned host memory on the
+ * side stream after the compute stream has passed the lowering.  The device pages are
+ * released by the pw_commit call that sees the copy landed.  PW_ERR_STATE if q_new is
+ * not a supported bitwidth below q or a page of the range is not GPU-resident;
+ * PW_ERR_BUSY if a transfer of the block is in flight. */
+pw_status pw_offload(pw_ctx *ctx, int block, int q_new);
+
+/* Reload: allocate device pages q..q_new-1 and copy them in from pinned host memory on
+ * the side stream; q stays unchanged until pw_commit sees the copy landed and then
+ * raises q (Sec. 3.1: raise only once GPU-resident).  PW_ERR_OOM if device memory is
+ * exhausted (nothing changed); PW_ERR_STATE / PW_ERR_BUSY as for pw_offload. */
+pw_status pw_reload(pw_ctx *ctx, int block, int q_new);
+
+/* Apply every transfer that has landed: retire offloaded device pages and commit the
+ * raises of landed reloads on the ctx stream.  *n_applied (may be NULL) receives the
+ * number of raises committed.  Never blocks.  A failed copy rolls its block back
+ * (pages stay or become CPU-resident, q is not raised) and returns PW_ERR_CUDA. */
+pw_status pw_commit(pw_ctx *ctx, int *n_applied);
+
+/* Wait for every transfer in flight (then pw_commit applies them). */
+pw_status pw_sync_io(pw_ctx *ctx);
+
+pw_status pw_query(pw_ctx *ctx, int block, pw_block_info *info);
+
+typedef struct {
+    int64_t resident_bytes;   /* sum over blocks of M_i^{q_i} (routed planes + LUTs) */
+    int64_t device_pool_bytes;/* bytes reserved from cudaMalloc for pages */
+    int64_t device_pool_free; /* of which free for reuse */
+    int64_t pinned_bytes;     /* pinned host bytes reserved for CPU-resident pages */
+    int64_t scratch_bytes;    /* forward scratch */
+} pw_mem_info;
+pw_status pw_memory(pw_ctx *ctx, pw_mem_info *info);
+
+/* Host-side fault injection for testing the page I/O error paths (no GPU fault is ever
+ * made): kind 1 = the n-th next page copy is reported failed instead of issued;
+ * kind 2 = the n-th next device page allocation fails.  n = 0 clears. */
+pw_status pw_set_fault(pw_ctx *ctx, int kind, int n);
+
+/* ---------------------------------------------------------------- planner */
+
+typedef struct {
+    int T_blk;          /* free-block threshold (Eq. 7) */
+    int F_blk;          /* current number of free KV blocks (Eq. 7) */
+    double B_KV;        /* bytes of one KV block (Eq. 7) */
+    int R;              /* reload margin in blocks (reload when F_blk >= T_blk + R) */
+    const double *mass; /* [L][E] routing mass (Eq. 1), or NULL: use the context's
+                           online routing statistics (pw_plan_step only) */
+    const double *phi;  /* [n_blocks][3] routed-input features (Eq. 5) */
+} pw_obs;
+
+typedef struct {
+    int n_bits;             /* number of supported bitwidths */
+    const double *s;        /* [n_blocks][n_bits] offline sensitivity s_i^b (Eq. 2), b ascending */
+    const double *head_w;   /* [2][n_bits-1][3] residual heads w_u^{b->b'} (Eq. 5); transition j: bits[j+1] -> bits[j] */
+    const double *head_a;   /* [2][n_bits-1] */
+    const double *head_c;   /* [2][n_bits-1] confidence c_u^{b->b'} (Eq. 6) */
+    double alpha, rho_min, rho_max, eps; /* Eq. 6, Eq. 8 */
+    int n_buckets;
+    const double *mu;       /* [n_buckets] damage multipliers, bucket 0 hottest (Eq. 8) */
+    const int *floors;      /* [n_buckets] bitwidth floors */
+    int n_stages;           /* bitwidth-floor stages: stage s allows s+1 levels below q_i */
+} pw_offline;
+
+typedef struct {
+    int block, from_bits, to_bits;
+    double delta;           /* bytes released (offload) or restored (reload) */
+} pw_plan_entry;
+
+typedef struct {
+    pw_plan_entry *entries; /* caller storage */
+    int capacity;           /* entries available; PW_ERR_INVALID if too small */
+    int n;                  /* entries written */
+    int kind;               /* 0 no plan, 1 offload plan, 2 reload plan */
+    int stage;              /* stage of the chosen offload plan, -1 otherwise */
+    double D;               /* Eq. 7 byte target */
+    double total;           /* bytes of the chosen plan */
+} pw_plan;
+
+/* A planner problem over explicit arrays (no context, no GPU). */
+typedef struct {
+    int n_blocks, n_bits, L, E;
+    const int *bits;        /* [n_bits] ascending supported bitwidths */
+    const int *q;           /* [n_blocks] committed bitwidths */
+    const int *q_init;      /* [n_blocks] bitwidths reloads may restore up to */
+    const int *utype;       /* [n_blocks] 0 gate_up, 1 down */
+    const int *layer;       /* [n_blocks] */
+    const int *expert;      /* [n_blocks] */
+    const double *M;        /* [n_blocks][n_bits] M^b bytes (Eq. 3) */
+} pw_plan_problem;
+
+/* PlanStep (Algorithm 1 of Sec. 3.2) on an explicit problem: D from Eq. 7; for every
+ * stage: score the legal single-level steps with Eqs. 4-6, 8, greedily take the lowest
+ * d_hat / Delta until D is met (ties: larger Delta, then lower block); keep each stage's
+ * plan; when D > 0 return the lowest stage meeting D, else the largest reduction.  When
+ * D == 0 and F_blk >= T_blk + R, returns a reload plan instead (most damaging reduction
+ * restored first while the bytes fit in (F_blk - T_blk - R) * B_KV).  Host only. */
+pw_status pw_plan_host(const pw_plan_problem *prob, const pw_obs *obs,
+                       const pw_offline *off, pw_plan *out);
+
+/* PlanStep on the context's page table (q_i, M_i^b) and, when obs->mass is NULL, its
+ * online routing statistics (Eq. 1).  Writes the desired bitwidth d_i of every planned
+ * block.  Applying the plan is the caller's pw_offload / pw_reload. */
+pw_status pw_plan_step(pw_ctx *ctx, const pw_obs *obs, const pw_offline *off, pw_plan *out);
+
+/* ---------------------------------------------------------------- inspection */
+
+/* b-bit codes of a block as the GPU kernels read them (the same device extraction code
+ * as the forward): host uint8 [N][K].  Pages 0..b-1 must be GPU-resident.  Waits. */
+pw_status pw_unpack_indices(pw_ctx *ctx, int block, int b, uint8_t *host_out);
+
+/* Dequantised weights W^(b)[n][k] = LUT_b[n][code] as the GPU kernels produce them:
+ * host fp16 bits [N][K].  Pages 0..b-1 and LUT_b must be GPU-resident.  Waits. */
+pw_status pw_dequant(pw_ctx *ctx, int block, int b, uint16_t *host_out);
+
+/* Pure host helpers (no context, no GPU) for checking the packer.
+ * pw_pack_planes_host: the plain plane layout -- planes [bmax][N][W] uint32,
+ *   W = ceil(K/128)*4 words per row, bit j of word w is column 32w+j, plane 0 = MSB.
+ * pw_tile_planes_host / pw_untile_planes_host: the kernel-private device tiling of
+ *   those planes for a block of type u (gate_up rows are interleaved per 16-row tile)
+ *   and its inverse.  Sizes: bmax * N * W words each. */
+pw_status pw_pack_planes_host(const uint8_t *idx, int N, int K, int bmax, uint32_t *planes);
+pw_status pw_tile_planes_host(const uint32_t *planes, int N, int K, int nplanes, int u,
+                              uint32_t *tiled);
+pw_status pw_untile_planes_host(const uint32_t *tiled, int N, int K, int nplanes, int u,
+                                uint32_t *planes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PW_H */

@@ -11,7 +11,10 @@ Readings where the pages are silent:
 * top-K keeps the K largest p, ties to the lower expert id, listed by descending p;
 * expert activation is SiLU(gate) * up with gate rows [0, I) and up rows [I, 2I) of the
   gate_up block; silu(g) = g / (1 + exp(-g));
-* the shared expert is a dense FFN of the same form added to every token, ungated.
+* the shared expert is a dense FFN of the same form added to every token, ungated;
+* with ``prenorm`` the layer reads RMSNorm(x) = x / sqrt(mean(x^2) + 1e-6) with unit
+  gain, as the pre-norm transformers of the pages' model table (Table 1) feed their MoE
+  blocks; the caller adds the output to the un-normalised x.
 """
 from __future__ import annotations
 
@@ -27,8 +30,15 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
-def router_logits(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray]) -> np.ndarray:
+def rmsnorm(x: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    """Unit-gain RMSNorm over the hidden dimension."""
+    return x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + eps)
+
+
+def router_logits(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray], prenorm: bool = False) -> np.ndarray:
     x = bf16_to_f64(x_bits)
+    if prenorm:
+        x = rmsnorm(x)
     l = x @ np.asarray(Wr, dtype=np.float64).T
     if bias is not None:
         l = l + np.asarray(bias, dtype=np.float64)[None, :]
@@ -51,8 +61,8 @@ def topk(p: np.ndarray, K: int) -> Tuple[np.ndarray, np.ndarray]:
     return ids, w
 
 
-def route(x_bits, Wr, bias, K: int, renorm: bool = False):
-    p = softmax(router_logits(x_bits, Wr, bias))
+def route(x_bits, Wr, bias, K: int, renorm: bool = False, prenorm: bool = False):
+    p = softmax(router_logits(x_bits, Wr, bias, prenorm))
     ids, w = topk(p, K)
     if renorm:
         w = w / w.sum(axis=1, keepdims=True)
@@ -81,7 +91,7 @@ def expert_ffn(xe: np.ndarray, Wgu: np.ndarray, Wd: np.ndarray) -> np.ndarray:
 
 
 def moe_layer(x_bits: np.ndarray, Wr, bias, experts, q: np.ndarray, K: int, bmax: int,
-              shared=None, renorm: bool = False, tokens=None):
+              shared=None, renorm: bool = False, tokens=None, prenorm: bool = False):
     """Forward of one MoE layer in float64.
 
     experts: dict e -> (gu_idx, gu_luts, d_idx, d_luts); only routed experts are needed.
@@ -93,8 +103,10 @@ def moe_layer(x_bits: np.ndarray, Wr, bias, experts, q: np.ndarray, K: int, bmax
     xb = np.asarray(x_bits)
     if tokens is not None:
         xb = xb[np.asarray(tokens)]
-    ids, w, _ = route(xb, Wr, bias, K, renorm)
+    ids, w, _ = route(xb, Wr, bias, K, renorm, prenorm)
     x = bf16_to_f64(xb)
+    if prenorm:
+        x = rmsnorm(x)
     T, H = x.shape
     y = np.zeros((T, H), dtype=np.float64)
     o = np.zeros((T, K, H), dtype=np.float64)

@@ -153,3 +153,21 @@ def test_layer_uses_committed_bits():
     for t in range(x.shape[0]):
         changed = not np.allclose(y[t], y2[t])
         assert changed == (e0 in ids[t])
+
+
+def test_rmsnorm_and_prenorm_layer():
+    x = np.array([[3.0, 4.0], [1.0, -1.0]])
+    n = moe.rmsnorm(x, eps=0.0)
+    assert np.allclose(n, [[3 / np.sqrt(12.5), 4 / np.sqrt(12.5)], [1.0, -1.0]])
+    # a pre-normalised layer is invariant to scaling its input (up to eps)
+    shape = syn.SHAPES["tiny"]
+    Wr, bias, _ = syn.gen_router_np(shape, 3, 0)
+    xb = syn.gen_tokens_np(shape, 3, 0, 4)
+    experts = {e: syn.gen_block_np(shape, 3, 0, e, 0) + syn.gen_block_np(shape, 3, 0, e, 1) for e in range(shape.E)}
+    q = syn.gen_q_assignment(shape, 3, 0)
+    y1, ids1, _ = moe.moe_layer(xb, Wr, bias, experts, q, shape.K, shape.bmax, prenorm=True)
+    x2 = syn.bf16_bits_from_f32((moe.bf16_to_f64(xb) * 4.0).astype(np.float32))  # exact power of two
+    y2, ids2, _ = moe.moe_layer(x2, Wr, bias, experts, q, shape.K, shape.bmax, prenorm=True)
+    assert np.array_equal(ids1, ids2)
+    # eps = 1e-6 against mean(x^2) ~ 1 perturbs the scale by ~eps/2
+    assert np.allclose(y1, y2, rtol=1e-5, atol=1e-9)
