@@ -142,6 +142,7 @@ struct pw_ctx {
   std::string err;
   int sticky = 0;
   int fault_copy = 0, fault_alloc = 0;
+  int hold = 0;  // testing: transfers are not observed as landed while set
 };
 
 namespace {
@@ -564,14 +565,19 @@ pw_status pw_set_shared(pw_ctx *c, int layer, const uint16_t *wgu, const uint16_
   CU(c, cudaStreamSynchronize(c->compute));
   if (!l.wgu) CU(c, cudaMalloc((void **)&l.wgu, ngu));
   if (!l.wd) CU(c, cudaMalloc((void **)&l.wd, nd));
-  if (pw_status st = ensure_stage(c, std::max(ngu, nd))) return st;
+  if (pw_status st = ensure_stage(c, std::max(ngu, nd) + 256)) return st;
+  int *d_bad = reinterpret_cast<int *>(static_cast<char *>(c->stage) + std::max(ngu, nd));
+  CU(c, cudaMemsetAsync(d_bad, 0, sizeof(int), c->compute));
   CU(c, cudaMemcpyAsync(c->stage, wgu, ngu, cudaMemcpyDefault, c->compute));
-  if (int e = launch_frag16(static_cast<uint16_t *>(c->stage), 2 * Is, H, 0, Is, const_cast<uint16_t *>(l.wgu), c->compute))
+  if (int e = launch_frag16(static_cast<uint16_t *>(c->stage), 2 * Is, H, 0, Is, const_cast<uint16_t *>(l.wgu), d_bad, c->compute))
     return fail(c, PW_ERR_CUDA, "frag16 kernel: %s", cudaGetErrorString((cudaError_t)e));
   CU(c, cudaMemcpyAsync(c->stage, wd, nd, cudaMemcpyDefault, c->compute));
-  if (int e = launch_frag16(static_cast<uint16_t *>(c->stage), H, Is, 1, Is, const_cast<uint16_t *>(l.wd), c->compute))
+  if (int e = launch_frag16(static_cast<uint16_t *>(c->stage), H, Is, 1, Is, const_cast<uint16_t *>(l.wd), d_bad, c->compute))
     return fail(c, PW_ERR_CUDA, "frag16 kernel: %s", cudaGetErrorString((cudaError_t)e));
+  int bad = 0;
+  CU(c, cudaMemcpyAsync(&bad, d_bad, sizeof(int), cudaMemcpyDeviceToHost, c->compute));
   CU(c, cudaStreamSynchronize(c->compute));
+  if (bad) return fail(c, PW_ERR_INVALID, "%d shared-expert weights exceed the fp16 range (|w| > 65504)", bad);
   c->shared_set[layer] = 1;
   return PW_OK;
 }
@@ -843,7 +849,7 @@ pw_status pw_reload(pw_ctx *c, int block, int q_new) {
 namespace {
 pw_status observe(pw_ctx *c, int id) {
   HostBlock &b = c->blocks[id];
-  if (!b.pend.kind || b.landed) return PW_OK;
+  if (!b.pend.kind || b.landed || c->hold) return PW_OK;
   cudaError_t e = cudaEventQuery(b.ev);
   if (e == cudaErrorNotReady) return PW_OK;
   if (e != cudaSuccess) {
@@ -975,6 +981,8 @@ pw_status pw_set_fault(pw_ctx *c, int kind, int n) {
     c->fault_copy = n;
   else if (kind == 2)
     c->fault_alloc = n;
+  else if (kind == 3)
+    c->hold = n ? 1 : 0;
   else
     return fail(c, PW_ERR_INVALID, "unknown fault kind %d", kind);
   return PW_OK;

@@ -111,7 +111,7 @@ struct Scratch {
   int *n_items;        // [2]
   unsigned *ticket;    // [1] last-CTA counter of the router
   uint16_t *h_routed;  // fp16 [Tm*K][I]
-  uint16_t *h_shared;  // bf16 [Tm][Is]
+  uint16_t *h_shared;  // fp16 [Tm][Is]
   float *o_routed;     // [Tm*K][H]
   float *o_shared;     // [Tm][H]
   float *inv_rms;      // [Tm] per-token 1/rms of the layer input (PW_PRENORM)
@@ -123,8 +123,8 @@ struct Scratch {
 struct LayerDev {
   const float *Wr;         // [E][H]
   const float *bias;       // [E] or null
-  const uint16_t *wgu;     // shared gate_up, frag16 layout (dev rows interleaved)
-  const uint16_t *wd;      // shared down, frag16 layout
+  const uint16_t *wgu;     // shared gate_up, fp16, frag16 layout (dev rows interleaved)
+  const uint16_t *wd;      // shared down, fp16, frag16 layout
 };
 
 struct FwdArgs {
@@ -146,7 +146,7 @@ int launch_pack(const uint8_t *idx, int N, int K, int KC, int u, int I, int bmax
                 uint32_t *const *plane_out, void *stream);
 int launch_lut_permute(const uint16_t *lut_in, int N, int entries, int u, int I,
                        uint16_t *lut_out, void *stream);
-int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_out,
+int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_out, int *bad,
                   void *stream);
 int launch_unpack(const BlockDev *table, int block, int b, int u, int I, int N, int KC,
                   uint8_t *idx_out, uint16_t *w_out, void *stream);

@@ -353,9 +353,10 @@ struct FfnSmem {
   uint16_t *xs;   // [xt][kXStride]
 };
 
-// Stage activation columns [c0, c0 + kXCols) of the item's tokens into xs (zero padded).
-// PHASE 1 routed: gathered x rows converted bf16 -> fp16; PHASE 2 routed: h rows (fp16);
-// shared: x / h_shared rows kept as bf16.
+// Stage activation columns [c0, c0 + kXCols) of the item's tokens into xs (zero padded),
+// as fp16: PHASE 1 converts the bf16 layer input (times 1/rms under PW_PRENORM) -- routed
+// items gather their tokens, shared items take them in order; PHASE 2 copies the fp16 h
+// rows.
 template <int PHASE, bool SHARED>
 __device__ __forceinline__ void stage_x(const FwdArgs &a, const WorkItem &w, int slot0, int Kc,
                                         int c0, int xt, uint16_t *xs) {
@@ -364,20 +365,10 @@ __device__ __forceinline__ void stage_x(const FwdArgs &a, const WorkItem &w, int
     const int j = v / vecs, c = c0 + (v % vecs) * 8;
     uint4 val = make_uint4(0, 0, 0, 0);
     if (j < w.ntok && c < Kc) {
-      if (SHARED) {
-        const int t = w.tok0 + j;
-        const uint16_t *src = (PHASE == 1) ? a.x + (size_t)t * a.H : a.s.h_shared + (size_t)t * a.Is;
-        val = *reinterpret_cast<const uint4 *>(src + c);
-        if (PHASE == 1 && (a.flags & 2)) {  // normalised input, rounded back to bf16
-          const float inv = a.s.inv_rms[t];
-          uint32_t r[4] = {val.x, val.y, val.z, val.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            r[i] = pack2(f2bf(bf16f(r[i] & 0xFFFF) * inv), f2bf(bf16f(r[i] >> 16) * inv));
-          val = make_uint4(r[0], r[1], r[2], r[3]);
-        }
+      if (PHASE == 2 && SHARED) {
+        val = *reinterpret_cast<const uint4 *>(a.s.h_shared + (size_t)(w.tok0 + j) * a.Is + c);
       } else if (PHASE == 1) {
-        const int t = a.s.slot_tok[slot0 + j];
+        const int t = SHARED ? w.tok0 + j : a.s.slot_tok[slot0 + j];
         const float inv = (a.flags & 2) ? a.s.inv_rms[t] : 1.0f;
         uint4 raw = *reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + c);
         uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -410,7 +401,7 @@ __device__ __forceinline__ void epilogue(const FwdArgs &a, const WorkItem &w, in
         const int f = rt * 8 + g;
         const float hv = silu(acc[j][h]) * acc[j][2 + h];
         if (SHARED)
-          a.s.h_shared[(size_t)(w.tok0 + tj) * a.Is + f] = f2bf(hv);
+          a.s.h_shared[(size_t)(w.tok0 + tj) * a.Is + f] = f2h(hv);
         else
           a.s.h_routed[(size_t)(slot0 + tj) * a.I + f] = f2h(hv);
       } else {
@@ -490,7 +481,7 @@ __device__ void routed_item(const FwdArgs &a, const WorkItem &w, const BlockDev 
   if (active) epilogue<PHASE, false>(a, w, slot0, rt, ngroups, acc);
 }
 
-// Shared-expert item: dense bf16 weights in the frag16 layout.
+// Shared-expert item: dense weights (bf16 converted to fp16 when set) in the frag16 layout.
 template <int PHASE>
 __device__ void shared_item(const FwdArgs &a, const WorkItem &w, uint8_t *smem) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -529,7 +520,7 @@ __device__ void shared_item(const FwdArgs &a, const WorkItem &w, uint8_t *smem) 
         const uint16_t *xb = xrow + j * 8 * kXStride + (st * 16 - c0);
         const uint32_t b0 = *reinterpret_cast<const uint32_t *>(xb);
         const uint32_t b1 = *reinterpret_cast<const uint32_t *>(xb + 8);
-        mma_bf16(acc[j], af.x, af.y, af.z, af.w, b0, b1);
+        mma_f16(acc[j], af.x, af.y, af.z, af.w, b0, b1);
       }
     }
   }
@@ -559,6 +550,7 @@ __global__ void __launch_bounds__(kFfnThreads) ffn_kernel(FwdArgs a) {
         default: routed_item<PHASE, 8>(a, w, bd, smem_raw); break;
       }
     }
+    __syncthreads();  // the next item restages the LUT and activations in shared memory
   }
 }
 
@@ -609,6 +601,17 @@ static size_t ffn_smem_bytes(int xt) {
   return (size_t)kCtaRows * 256 * 2 + (size_t)xt * kXStride * 2;
 }
 
+// Timing events: under stream capture an ordinary record only orders graph nodes, so the
+// record is made an external event node that fires on every replay.
+static void record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
+
 int launch_forward(const FwdArgs &a, void *stream_, void *const *ev_) {
   cudaEvent_t const *ev = reinterpret_cast<cudaEvent_t const *>(ev_);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
@@ -623,9 +626,9 @@ int launch_forward(const FwdArgs &a, void *stream_, void *const *ev_) {
     g_smem_attr_done = dev;
   }
   dim3 rg((a.T + kRtTok - 1) / kRtTok, (a.E + kRtExp - 1) / kRtExp);
-  if (ev) cudaEventRecord(ev[0], st);
+  if (ev) record(ev[0], st);
   route_kernel<<<rg, kRtThreads, kRtTok * a.H * 2, st>>>(a);
-  if (ev) cudaEventRecord(ev[1], st);
+  if (ev) record(ev[1], st);
   const size_t smem = ffn_smem_bytes(xt);
   int per_sm = 1;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_kernel<1>, kFfnThreads, smem);
@@ -633,11 +636,11 @@ int launch_forward(const FwdArgs &a, void *stream_, void *const *ev_) {
   const int grid1 = min(a.s.max_items1, a.sm_count * per_sm);
   const int grid2 = min(a.s.max_items2, a.sm_count * per_sm);
   ffn_kernel<1><<<grid1, kFfnThreads, smem, st>>>(a);
-  if (ev) cudaEventRecord(ev[2], st);
+  if (ev) record(ev[2], st);
   ffn_kernel<2><<<grid2, kFfnThreads, smem, st>>>(a);
-  if (ev) cudaEventRecord(ev[3], st);
+  if (ev) record(ev[3], st);
   combine_kernel<<<a.T, 256, 0, st>>>(a);
-  if (ev) cudaEventRecord(ev[4], st);
+  if (ev) record(ev[4], st);
   return (int)cudaGetLastError();
 }
 
@@ -701,17 +704,20 @@ int launch_lut_permute(const uint16_t *lut_in, int N, int entries, int u, int I,
   return (int)cudaGetLastError();
 }
 
-__global__ void frag16_kernel(const uint16_t *in, int N, int K, int u, int I, uint16_t *out) {
+// bf16 -> fp16 in the frag16 layout; counts values that overflow fp16 into *bad.
+__global__ void frag16_kernel(const uint16_t *in, int N, int K, int u, int I, uint16_t *out, int *bad) {
   long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long)N * K) return;
   const int d = (int)(i / K), k = (int)(i % K);
-  out[frag16_index(d, k, K)] = in[(size_t)orig_row(d, u, I) * K + k];
+  const float v = bf16f(in[(size_t)orig_row(d, u, I) * K + k]);
+  if (!(fabsf(v) <= 65504.0f)) atomicAdd(bad, 1);
+  out[frag16_index(d, k, K)] = f2h(v);
 }
 
-int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_out, void *stream) {
+int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_out, int *bad, void *stream) {
   const long n = (long)N * K;
   frag16_kernel<<<(unsigned)((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      w_in, N, K, u, I, w_out);
+      w_in, N, K, u, I, w_out, bad);
   return (int)cudaGetLastError();
 }
 

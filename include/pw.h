@@ -113,7 +113,9 @@ pw_status pw_pack(pw_ctx *ctx, int layer, int expert, int u, const uint8_t *idx,
 pw_status pw_set_router(pw_ctx *ctx, int layer, const float *Wr, const float *bias);
 
 /* Shared expert of a layer (Table 1 counts shared experts): wgu bf16 bits [2*Is][H]
- * (gate rows, then up rows), wd bf16 bits [H][Is].  Host or device pointers. */
+ * (gate rows, then up rows), wd bf16 bits [H][Is].  Host or device pointers.  The device
+ * copy is fp16 (exact for bf16 values in [2^-14, 65504]; smaller ones keep an absolute
+ * error below 2^-25); PW_ERR_INVALID if a weight exceeds 65504 in magnitude. */
 pw_status pw_set_shared(pw_ctx *ctx, int layer, const uint16_t *wgu, const uint16_t *wd);
 
 /* ---------------------------------------------------------------- forward */
@@ -211,9 +213,11 @@ typedef struct {
 } pw_mem_info;
 pw_status pw_memory(pw_ctx *ctx, pw_mem_info *info);
 
-/* Host-side fault injection for testing the page I/O error paths (no GPU fault is ever
- * made): kind 1 = the n-th next page copy is reported failed instead of issued;
- * kind 2 = the n-th next device page allocation fails.  n = 0 clears. */
+/* Host-side fault injection for testing the page I/O paths (no GPU fault is ever made):
+ * kind 1 = the n-th next page copy is reported failed instead of issued;
+ * kind 2 = the n-th next device page allocation fails;
+ * kind 3 = while n != 0, no transfer is observed as landed (the copies still run), so a
+ * test can act while pages are in transfer.  n = 0 clears. */
 pw_status pw_set_fault(pw_ctx *ctx, int kind, int n);
 
 /* ---------------------------------------------------------------- planner */

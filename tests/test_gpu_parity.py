@@ -206,7 +206,7 @@ def test_stack_graph_replay_equals_layer_by_layer():
         s = torch.cuda.Stream()
         with torch.cuda.stream(s):
             for layer in range(3):
-                pw.pw_moe_forward(ctx, layer, xa, T, xa, None, None, pw.PW_ACCUMULATE, s)
+                pw.pw_moe_forward(ctx, layer, xa, T, xa, None, None, pw.PW_ACCUMULATE | pw.PW_PRENORM, s)
             pw.pw_stack_forward(ctx, xb, T, s)  # first call captures and replays
         s.synchronize()
         assert torch.equal(xa, xb)
