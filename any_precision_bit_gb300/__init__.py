@@ -100,6 +100,7 @@ _SIGS = {
     "pw_set_fault": [_P, _I, _I],
     "pw_plan_host": [C.POINTER(pw_plan_problem), C.POINTER(pw_obs), C.POINTER(pw_offline), C.POINTER(pw_plan)],
     "pw_plan_step": [_P, C.POINTER(pw_obs), C.POINTER(pw_offline), C.POINTER(pw_plan)],
+    "pw_route_noalloc": [_P, _I, _P, _I, _P, _P, _I, _P],
     "pw_set_profiling": [_P, _I],
     "pw_profile_read": [_P, _I, _P],
     "pw_unpack_indices": [_P, _I, _I, _P],
@@ -257,6 +258,10 @@ def pw_memory(ctx) -> pw_mem_info:
 
 def pw_set_fault(ctx, kind, n):
     _check(lib().pw_set_fault(ctx, kind, n), ctx)
+
+
+def pw_route_noalloc(ctx, layer, x, T, ids, w, flags=0, stream=None):
+    _check(lib().pw_route_noalloc(ctx, layer, _ptr(x), T, _ptr(ids), _ptr(w), flags, _stream(stream)), ctx)
 
 
 def pw_set_profiling(ctx, on):

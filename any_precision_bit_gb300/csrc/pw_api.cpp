@@ -1090,3 +1090,19 @@ pw_status pw_profile_read(pw_ctx *c, int layer, float *ms) {
 }
 
 }  // extern "C"
+
+// ================================================================== helpers for pw_static.cu
+namespace pw {
+
+pw_status route_args(pw_ctx *c, int layer, const void *x, int T, int32_t *ids, float *w, int flags,
+                     FwdArgs *a) {
+  if (!c) return fail(nullptr, PW_ERR_INVALID, "null context");
+  if (pw_status st = check_sticky(c)) return st;
+  return forward_args(c, layer, x, T, const_cast<void *>(x), ids, w, flags, a);
+}
+
+pw_status report(pw_ctx *c, pw_status st, const char *msg) { return fail(c, st, "%s", msg); }
+
+int ctx_device(const pw_ctx *c) { return c->d.device; }
+
+}  // namespace pw

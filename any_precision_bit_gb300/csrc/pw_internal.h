@@ -153,3 +153,13 @@ int launch_unpack(const BlockDev *table, int block, int b, int u, int I, int N, 
 int launch_fill_u32(uint32_t *p, uint32_t v, long n, void *stream);
 
 }  // namespace pw
+
+// ------------------------------------------------------------------ routing-only launches
+#include "../../include/pw.h"
+namespace pw {
+int launch_route(const FwdArgs &a, void *stream);
+pw_status route_args(pw_ctx *c, int layer, const void *x, int T, int32_t *ids, float *w, int flags,
+                     FwdArgs *a);
+pw_status report(pw_ctx *c, pw_status st, const char *msg);
+int ctx_device(const pw_ctx *c);
+}  // namespace pw

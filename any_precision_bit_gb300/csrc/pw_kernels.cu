@@ -784,3 +784,14 @@ int launch_fill_u32(uint32_t *p, uint32_t v, long n, void *stream) {
 }
 
 }  // namespace pw
+
+namespace pw {
+// The router kernel alone (logits, softmax, top-K, bucketing) on scratch the caller chose.
+int launch_route(const FwdArgs &a, void *stream_) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
+  cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtTok * 8192 * 2);
+  dim3 rg((a.T + kRtTok - 1) / kRtTok, (a.E + kRtExp - 1) / kRtExp);
+  route_kernel<<<rg, kRtThreads, kRtTok * a.H * 2, st>>>(a);
+  return (int)cudaGetLastError();
+}
+}  // namespace pw

@@ -1,0 +1,130 @@
+// pw_static.cu -- pw_route_noalloc: the routing kernel run on scratch that lives in a static
+// device array of this library, so that the call allocates no memory.
+//
+// Who needs it: code that must not call cudaMalloc (or any allocating routine) at the point
+// where it routes tokens -- for example a caller that runs under an external memory
+// budget or allocator it does not control, or a host thread that may not touch the CUDA
+// allocator while other work is in flight.  pw_moe_forward's own scratch is allocated by
+// pw_create; this entry point uses none of it.
+//
+// The array below is part of the module: every GPU that loads libpw.so holds it until the
+// process exits.  All calls share it and it keeps the last call's contents.
+#include <cuda_runtime.h>
+
+#include <cstdio>
+
+#include "pw_internal.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
+
+// Host-side stand-in of g_route_scratch is not a device address: the real address is looked
+// up once per device, with that device current.
+void *g_scratch_addr[kMaxDevices] = {};
+
+size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int T, int32_t *ids,
+                                      float *w, int flags, pw_stream stream) {
+  using namespace pw;
+  if (!ctx || !ids || !w) return report(ctx, PW_ERR_INVALID, "pw_route_noalloc: null context, ids or w");
+  const int dev = ctx_device(ctx);
+  if (dev < 0 || dev >= kMaxDevices) return report(ctx, PW_ERR_INVALID, "pw_route_noalloc: device ordinal too large");
+  FwdArgs a;
+  if (pw_status st = route_args(ctx, layer, x, T, ids, w, flags & PW_PRENORM, &a)) return st;
+
+  // scratch the router kernel touches, carved from the static array (256-byte aligned)
+  const long TK = (long)T * a.K;
+  const int tiles1 = (2 * a.I + kCtaRows - 1) / kCtaRows;
+  const int tiles2 = (a.H + kCtaRows - 1) / kCtaRows;
+  const long tch = (T + kTokChunk - 1) / kTokChunk;
+  const long chunks = (a.E < TK ? a.E : TK) + TK / kTokChunk + 1;
+  const long n1 = tiles1 * chunks + (a.Is ? ((2L * a.Is + kCtaRows - 1) / kCtaRows) * tch : 0);
+  const long n2 = tiles2 * chunks + (a.Is ? tiles2 * tch : 0);
+  const size_t sizes[] = {
+      sizeof(float) * T * a.E,      // logits
+      sizeof(int) * TK,             // ids
+      sizeof(float) * TK,           // w
+      sizeof(int) * a.E,            // counts
+      sizeof(int) * (a.E + 1),      // offsets
+      sizeof(int) * TK,             // slot_tok
+      sizeof(int) * TK,             // pair_slot
+      sizeof(float) * TK,           // slot_w
+      sizeof(WorkItem) * n1,        // items1
+      sizeof(WorkItem) * n2,        // items2
+      sizeof(int) * 2,              // n_items
+      sizeof(unsigned),             // ticket
+      sizeof(float) * T,            // inv_rms
+      sizeof(double) * a.E,         // stat_count (discarded)
+      sizeof(double) * a.E,         // stat_wsum (discarded)
+  };
+  size_t need = 0;
+  for (size_t s : sizes) need += align256(s);
+  if (need > kStaticScratchBytes) {
+    char msg[200];
+    snprintf(msg, sizeof msg, "pw_route_noalloc: T=%d needs %zu bytes of scratch, the static array holds %zu",
+             T, need, kStaticScratchBytes);
+    return report(ctx, PW_ERR_INVALID, msg);
+  }
+
+  // one-time set-up per device, with that device current
+  if (!g_scratch_addr[dev]) {
+    int prev = 0;
+    cudaGetDevice(&prev);
+    cudaSetDevice(dev);
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+    cudaSetDevice(prev);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();
+      return report(ctx, PW_ERR_CUDA, "pw_route_noalloc: cudaGetSymbolAddress failed");
+    }
+    g_scratch_addr[dev] = p;
+  }
+  char *base = static_cast<char *>(g_scratch_addr[dev]);
+  char *cur = base;
+  auto take = [&](size_t n) {
+    char *p = cur;
+    cur += align256(n);
+    return p;
+  };
+  Scratch s{};
+  s.logits = reinterpret_cast<float *>(take(sizes[0]));
+  s.ids = reinterpret_cast<int *>(take(sizes[1]));
+  s.w = reinterpret_cast<float *>(take(sizes[2]));
+  s.counts = reinterpret_cast<int *>(take(sizes[3]));
+  s.offsets = reinterpret_cast<int *>(take(sizes[4]));
+  s.slot_tok = reinterpret_cast<int *>(take(sizes[5]));
+  s.pair_slot = reinterpret_cast<int *>(take(sizes[6]));
+  s.slot_w = reinterpret_cast<float *>(take(sizes[7]));
+  s.items1 = reinterpret_cast<WorkItem *>(take(sizes[8]));
+  s.items2 = reinterpret_cast<WorkItem *>(take(sizes[9]));
+  s.n_items = reinterpret_cast<int *>(take(sizes[10]));
+  s.ticket = reinterpret_cast<unsigned *>(take(sizes[11]));
+  s.inv_rms = reinterpret_cast<float *>(take(sizes[12]));
+  s.stat_count = reinterpret_cast<double *>(take(sizes[13]));
+  s.stat_wsum = reinterpret_cast<double *>(take(sizes[14]));
+  s.max_items1 = (int)n1;
+  s.max_items2 = (int)n2;
+  a.s = s;
+  a.layer = 0;  // the kernel indexes its statistics by layer; these go to the discarded slots
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the last-CTA ticket must start at zero; the array keeps whatever the last call left
+  if (cudaMemsetAsync(s.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
+    cudaGetLastError();
+    return report(ctx, PW_ERR_CUDA, "pw_route_noalloc: clearing the ticket failed");
+  }
+  if (int e = launch_route(a, stream)) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "pw_route_noalloc: launch failed: %s", cudaGetErrorString((cudaError_t)e));
+    return report(ctx, PW_ERR_CUDA, msg);
+  }
+  return PW_OK;
+}

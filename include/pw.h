@@ -160,6 +160,21 @@ pw_status pw_routing_stats(pw_ctx *ctx, int layer, double *count, double *weight
 pw_status pw_set_profiling(pw_ctx *ctx, int on);
 pw_status pw_profile_read(pw_ctx *ctx, int layer, float *ms);
 
+/* Routing without allocation.  The paper has no counterpart: this entry point exists for
+ * callers that cannot call cudaMalloc (or anything that allocates) where they route, e.g.
+ * code running under a memory budget or allocator it does not own.  It runs the same
+ * router kernel as pw_moe_forward -- fp32 logits, softmax, top-K, bucketing -- for layer
+ * `layer` on device x (bf16 [T][H], 16-byte aligned), writing ids (int32 [T][K]) and w
+ * (fp32 [T][K]) to the caller's device buffers.  flags: PW_PRENORM or 0.
+ * Its scratch is a static device array of 8 MiB inside libpw.so (held by every GPU that
+ * loads the library until the process exits); T is limited by it, and a T whose scratch
+ * does not fit returns PW_ERR_INVALID.  The first call on a device looks up the array's
+ * device address, so make it before any stream capture.  Calls share the array: calls
+ * that overlap on the GPU (e.g. on two streams) race.  Online routing statistics are not
+ * updated.  No cudaMalloc, cudaFree or other allocation happens in the call. */
+pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int T, int32_t *ids, float *w,
+                           int flags, pw_stream stream);
+
 /* ---------------------------------------------------------------- page table */
 
 enum { PW_PAGE_GPU = 0, PW_PAGE_CPU = 1, PW_PAGE_TO_CPU = 2, PW_PAGE_TO_GPU = 3 };
