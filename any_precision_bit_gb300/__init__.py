@@ -87,6 +87,7 @@ _SIGS = {
     "pw_set_router": [_P, _I, _P, _P],
     "pw_set_shared": [_P, _I, _P, _P],
     "pw_moe_forward": [_P, _I, _P, _I, _P, _P, _P, _I, _P],
+    "pw_check": [_P],
     "pw_stack_forward": [_P, _P, _I, _P],
     "pw_stack_forward_host": [_P, _P, _I, _P],
     "pw_routing_stats": [_P, _I, _P, _P, _I],
@@ -205,6 +206,10 @@ def pw_set_shared(ctx, layer, wgu, wd):
 
 def pw_moe_forward(ctx, layer, x, T, y, ids=None, w=None, flags=0, stream=None):
     _check(lib().pw_moe_forward(ctx, layer, _ptr(x), T, _ptr(y), _ptr(ids), _ptr(w), flags, _stream(stream)), ctx)
+
+
+def pw_check(ctx):
+    _check(lib().pw_check(ctx), ctx)
 
 
 def pw_stack_forward(ctx, x, T, stream=None):

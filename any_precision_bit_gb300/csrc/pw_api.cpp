@@ -342,7 +342,8 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
   const long tch = (Tm + kTokChunk - 1) / kTokChunk;
   const long chunks_routed = std::min<long>(d.E, TK) + TK / kTokChunk + 1;
   c->s.max_items1 = (int)(tiles1 * chunks_routed + (d.Is ? ((2 * d.Is + kCtaRows - 1) / kCtaRows) * tch : 0));
-  c->s.max_items2 = (int)(tiles2 * chunks_routed + (d.Is ? tiles2 * tch : 0));
+  const int nsplit = shared_down_splits(d.I, d.Is);
+  c->s.max_items2 = (int)(tiles2 * chunks_routed + (d.Is ? tiles2 * tch * nsplit : 0));
   auto salloc = [&](void **p, size_t n) -> bool {
     n = std::max<size_t>(n, 16);
     if (cudaMalloc(p, n) != cudaSuccess) {
@@ -366,8 +367,10 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.h_routed, sizeof(uint16_t) * TK * d.I) &&
             salloc((void **)&c->s.h_shared, sizeof(uint16_t) * Tm * std::max(d.Is, 1)) &&
             salloc((void **)&c->s.o_routed, sizeof(float) * TK * d.H) &&
-            salloc((void **)&c->s.o_shared, sizeof(float) * Tm * d.H) &&
+            salloc((void **)&c->s.o_shared, sizeof(float) * nsplit * Tm * d.H) &&
             salloc((void **)&c->s.inv_rms, sizeof(float) * Tm) &&
+            salloc((void **)&c->s.xh, sizeof(uint16_t) * Tm * d.H) &&
+            salloc((void **)&c->s.err, sizeof(int)) &&
             salloc((void **)&c->s.stat_count, sizeof(double) * d.L * d.E) &&
             salloc((void **)&c->s.stat_wsum, sizeof(double) * d.L * d.E) &&
             salloc(&c->xdev, sizeof(uint16_t) * Tm * d.H);
@@ -376,6 +379,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
     return bail(PW_ERR_OOM);
   }
   cudaMemset(c->s.ticket, 0, sizeof(unsigned));
+  cudaMemset(c->s.err, 0, sizeof(int));
   cudaMemset(c->s.stat_count, 0, sizeof(double) * d.L * d.E);
   cudaMemset(c->s.stat_wsum, 0, sizeof(double) * d.L * d.E);
   if (cudaDeviceSynchronize() != cudaSuccess) {
@@ -1090,6 +1094,19 @@ pw_status pw_profile_read(pw_ctx *c, int layer, float *ms) {
 }
 
 }  // extern "C"
+
+// ================================================================== device-side timeouts
+extern "C" pw_status pw_check(pw_ctx *c) {
+  if (!c) return fail(nullptr, PW_ERR_INVALID, "null context");
+  CU(c, cudaStreamSynchronize(c->compute));
+  int err = 0;
+  CU(c, cudaMemcpy(&err, c->s.err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (err) {
+    CU(c, cudaMemset(c->s.err, 0, sizeof(int)));
+    return fail(c, PW_ERR_TIMEOUT, "a bounded wait in an expert kernel expired; that launch's outputs are invalid");
+  }
+  return check_sticky(c);
+}
 
 // ================================================================== helpers for pw_static.cu
 namespace pw {

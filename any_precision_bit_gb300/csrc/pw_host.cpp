@@ -44,8 +44,9 @@ pw_status pw_tile_planes_host(const uint32_t *planes, int N, int K, int nplanes,
       const int r = orig_row(d, u, I);
       for (int k = 0; k < Kp; ++k) {
         const uint32_t bit = (planes[p * per + (size_t)r * W + k / 32] >> (k % 32)) & 1u;
-        int word, pos;
-        tile_pos(d, k, KC, &word, &pos);
+        long word;
+        int pos;
+        tile_pos(d, k, N, KC, &word, &pos);
         tiled[p * per + word] |= bit << pos;
       }
     }
@@ -61,8 +62,9 @@ pw_status pw_untile_planes_host(const uint32_t *tiled, int N, int K, int nplanes
     for (int d = 0; d < N; ++d) {
       const int r = orig_row(d, u, I);
       for (int k = 0; k < Kp; ++k) {
-        int word, pos;
-        tile_pos(d, k, KC, &word, &pos);
+        long word;
+        int pos;
+        tile_pos(d, k, N, KC, &word, &pos);
         const uint32_t bit = (tiled[p * per + word] >> pos) & 1u;
         planes[p * per + (size_t)r * W + k / 32] |= bit << (k % 32);
       }

@@ -1,15 +1,17 @@
 // pw_internal.h -- structures and index maps shared by the host runtime and the kernels.
 //
 // Kernel-private plane tiling (the ABI layout is restored by pw_unpack_indices):
-//   A block's rows are grouped in 16-row tiles.  For a gate_up block a tile holds 8 gate
-//   rows followed by the 8 up rows of the same 8 features, so that one warp's MMA tile
-//   yields gate and up of a feature in the same thread.  Columns are grouped in chunks of
-//   128 (the plane row is zero-padded to a multiple of 128 bits).  One (tile, chunk) pair
-//   of a plane is 64 uint32 words: word (lane * 2 + r) belongs to thread `lane` of the
-//   warp and row (g + 8r) of the tile, g = lane / 4; its bit (8e + s) holds column
-//   16 s + kofs(c, e) of the chunk, c = lane % 4, kofs = {2c, 2c+1, 2c+8, 2c+9}[e].
-//   These are exactly the elements of the m16n8k16 A fragment that thread holds for the
-//   eight 16-column steps s of the chunk.
+//   A block's rows are grouped in 16-row warp tiles.  For a gate_up block a warp tile holds
+//   8 gate rows followed by the 8 up rows of the same 8 features, so that one warp's MMA
+//   tile yields gate and up of a feature in the same thread.  Columns are grouped in chunks
+//   of 128 (the plane row is zero-padded to a multiple of 128 bits).  Warp tiles are grouped
+//   by 8 into CTA tiles of 128 rows (the last CTA tile may hold fewer).  Within a CTA tile
+//   the data of one plane is ordered [chunk][warp tile][64 words], so one 128-column stage
+//   of a CTA tile is a single contiguous run of (warp tiles x 256) bytes per plane.
+//   Word (lane * 2 + r) of a (chunk, warp tile) belongs to thread `lane` of the warp and row
+//   (g + 8r) of the warp tile, g = lane / 4; its bit (8e + s) holds column 16 s + kofs(c, e)
+//   of the chunk, c = lane % 4, kofs = {2c, 2c+1, 2c+8, 2c+9}[e]: exactly the elements of
+//   the m16n8k16 A fragment that thread holds for the chunk's eight 16-column steps.
 #pragma once
 #include <stdint.h>
 
@@ -23,8 +25,8 @@ namespace pw {
 
 constexpr int kMaxPlanes = 8;
 constexpr int kTileRows = 16;     // rows per warp tile
-constexpr int kChunkCols = 128;   // columns per plane chunk
-constexpr int kWarpsPerCta = 4;   // warp tiles per CTA tile in the decode kernels
+constexpr int kChunkCols = 128;   // columns per plane chunk (one pipeline stage)
+constexpr int kWarpsPerCta = 8;   // consumer warps (warp tiles) per CTA tile
 constexpr int kCtaRows = kTileRows * kWarpsPerCta;
 constexpr int kTokChunk = 64;     // tokens per work item in the decode kernels
 
@@ -44,9 +46,22 @@ struct WorkItem {
   int tile;    // CTA row tile (kCtaRows rows)
   int tok0;    // first slot (routed: into the expert-sorted pair list; shared: token)
   int ntok;    // tokens in this item (<= kTokChunk)
+  int kc0, kc1;  // 128-column stages [kc0, kc1) of the item along K
+  int part;    // shared down projection: the partial-sum buffer this item writes
 };
 
 PW_HD int kpad_cols(int K) { return (K + kChunkCols - 1) / kChunkCols * kChunkCols; }
+
+// The shared expert's down projection (K = Is) is split along K into this many items per
+// row tile, so that each is about as long as a routed down item (K = I); the parts are
+// summed, in order, by the combine kernel.
+PW_HD int shared_down_splits(int I, int Is) {
+  if (Is <= 0) return 1;
+  const int sh = (Is / 16 + 7) / 8;           // 128-column stages of the shared down
+  const int rt = kpad_cols(I) / kChunkCols;   // stages of a routed down
+  const int n = (sh + rt - 1) / rt;
+  return n < 1 ? 1 : (n > 8 ? 8 : n);
+}
 
 // device row of an original row (u = 0 gate_up with I features, u = 1 identity)
 PW_HD int dev_row(int r, int u, int I) {
@@ -62,8 +77,19 @@ PW_HD int orig_row(int d, int u, int I) {
   return (ri >= 8) ? I + f : f;
 }
 
+// warp tiles in CTA tile ct of a block with NT warp tiles
+PW_HD int cta_warps(int ct, int NT) {
+  return NT - ct * kWarpsPerCta < kWarpsPerCta ? NT - ct * kWarpsPerCta : kWarpsPerCta;
+}
+
+// first word of (warp tile rt, chunk kc) inside a tiled plane; its 64 words follow
+PW_HD long plane_pair_word(int rt, int kc, int NT, int KC) {
+  const int ct = rt / kWarpsPerCta, w = rt % kWarpsPerCta;
+  return ((long)ct * kWarpsPerCta * KC + (long)kc * cta_warps(ct, NT) + w) * 64;
+}
+
 // word index inside a tiled plane and bit inside that word for (device row d, column k)
-PW_HD void tile_pos(int d, int k, int KC, int *word, int *bit) {
+PW_HD void tile_pos(int d, int k, int N, int KC, long *word, int *bit) {
   int rt = d / 16, ri = d % 16;
   int g = ri % 8, r = ri / 8;
   int kc = k / 128, kk = k % 128;
@@ -71,14 +97,20 @@ PW_HD void tile_pos(int d, int k, int KC, int *word, int *bit) {
   int c = (kin % 8) / 2;
   int e = (kin & 1) + 2 * (kin / 8);
   int lane = 4 * g + c;
-  *word = ((rt * KC + kc) * 32 + lane) * 2 + r;
+  *word = plane_pair_word(rt, kc, N / 16, KC) + lane * 2 + r;
   *bit = 8 * e + s;
 }
 
-// Kernel-private layout of dense bf16 shared-expert weights (N x K, K % 16 == 0):
-// per 16-row tile and 16-column step, thread `lane` holds 4 words = its m16n8k16 A
-// fragment: (g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..2c+9), (g+8, 2c+8..).
-PW_HD long frag16_index(int d, int k, int K) {
+// Kernel-private layout of dense fp16 shared-expert weights (N x K, N % 16 == 0,
+// K % 16 == 0): per (16-row warp tile, 16-column step) 128 words in which thread `lane`
+// holds 4 words = its m16n8k16 A fragment: (g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..2c+9),
+// (g+8, 2c+8..).  Warp tiles are grouped by 8 like the planes and ordered [step][warp tile]
+// inside a CTA tile, so consecutive steps of a CTA tile are one contiguous run.
+PW_HD long frag_pair_word(int rt, int ks, int NT, int KS) {
+  const int ct = rt / kWarpsPerCta, w = rt % kWarpsPerCta;
+  return ((long)ct * kWarpsPerCta * KS + (long)ks * cta_warps(ct, NT) + w) * 128;
+}
+PW_HD long frag16_index(int d, int k, int N, int K) {
   int rt = d / 16, ri = d % 16;
   int g = ri % 8, r = ri / 8;
   int st = k / 16, kin = k % 16;
@@ -86,8 +118,8 @@ PW_HD long frag16_index(int d, int k, int K) {
   int hi = kin / 8;
   int lane = 4 * g + c;
   int reg = r + 2 * hi;  // 0: (g,lo) 1: (g+8,lo) 2: (g,hi) 3: (g+8,hi)
-  long word = ((long)(rt * (K / 16) + st) * 32 + lane) * 4 + reg;
-  return word * 2 + (kin & 1);  // element index (bf16 units)
+  long word = frag_pair_word(rt, st, N / 16, K / 16) + lane * 4 + reg;
+  return word * 2 + (kin & 1);  // element index (16-bit units)
 }
 
 }  // namespace pw
@@ -110,13 +142,15 @@ struct Scratch {
   WorkItem *items2;    // down work
   int *n_items;        // [2]
   unsigned *ticket;    // [1] last-CTA counter of the router
+  uint16_t *xh;        // fp16 [Tm][H]: the layer input as the experts read it (normalised under PW_PRENORM)
   uint16_t *h_routed;  // fp16 [Tm*K][I]
   uint16_t *h_shared;  // fp16 [Tm][Is]
   float *o_routed;     // [Tm*K][H]
-  float *o_shared;     // [Tm][H]
+  float *o_shared;     // [splits][T][H] partial sums of the shared down projection
   float *inv_rms;      // [Tm] per-token 1/rms of the layer input (PW_PRENORM)
   double *stat_count;  // [L][E]
   double *stat_wsum;   // [L][E]
+  int *err;            // [1] bounded-wait timeouts in the expert kernels (0 = none)
   int max_items1, max_items2;
 };
 
@@ -141,6 +175,7 @@ struct FwdArgs {
 
 // ev: null, or five timing events recorded before, between and after the four kernels
 int launch_forward(const FwdArgs &a, void *stream, void *const *ev);
+int launch_ffn(const FwdArgs &a, int phase, void *stream);
 int launch_commit(BlockDev *table, int block, const BlockDev &val, void *stream);
 int launch_pack(const uint8_t *idx, int N, int K, int KC, int u, int I, int bmax,
                 uint32_t *const *plane_out, void *stream);
@@ -150,7 +185,6 @@ int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_
                   void *stream);
 int launch_unpack(const BlockDev *table, int block, int b, int u, int I, int N, int KC,
                   uint8_t *idx_out, uint16_t *w_out, void *stream);
-int launch_fill_u32(uint32_t *p, uint32_t v, long n, void *stream);
 
 }  // namespace pw
 

@@ -46,7 +46,7 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   const long tch = (T + kTokChunk - 1) / kTokChunk;
   const long chunks = (a.E < TK ? a.E : TK) + TK / kTokChunk + 1;
   const long n1 = tiles1 * chunks + (a.Is ? ((2L * a.Is + kCtaRows - 1) / kCtaRows) * tch : 0);
-  const long n2 = tiles2 * chunks + (a.Is ? tiles2 * tch : 0);
+  const long n2 = tiles2 * chunks + (a.Is ? tiles2 * tch * shared_down_splits(a.I, a.Is) : 0);
   const size_t sizes[] = {
       sizeof(float) * T * a.E,      // logits
       sizeof(int) * TK,             // ids
@@ -63,6 +63,7 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
       sizeof(float) * T,            // inv_rms
       sizeof(double) * a.E,         // stat_count (discarded)
       sizeof(double) * a.E,         // stat_wsum (discarded)
+      sizeof(uint16_t) * T * a.H,   // xh: the fp16 expert input the router also writes
   };
   size_t need = 0;
   for (size_t s : sizes) need += align256(s);
@@ -110,6 +111,7 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   s.inv_rms = reinterpret_cast<float *>(take(sizes[12]));
   s.stat_count = reinterpret_cast<double *>(take(sizes[13]));
   s.stat_wsum = reinterpret_cast<double *>(take(sizes[14]));
+  s.xh = reinterpret_cast<uint16_t *>(take(sizes[15]));
   s.max_items1 = (int)n1;
   s.max_items2 = (int)n2;
   a.s = s;

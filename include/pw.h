@@ -135,6 +135,11 @@ pw_status pw_set_shared(pw_ctx *ctx, int layer, const uint16_t *wgu, const uint1
 pw_status pw_moe_forward(pw_ctx *ctx, int layer, const void *x, int T, void *y,
                          int32_t *ids, float *w, int flags, pw_stream stream);
 
+/* Wait for the compute stream and report whether a bounded wait inside an expert kernel
+ * expired since the last check (PW_ERR_TIMEOUT; the outputs of that launch are invalid).
+ * Also reports sticky CUDA errors. */
+pw_status pw_check(pw_ctx *ctx);
+
 /* The whole stack in place: for l = 0..L-1, x <- bf16(x + layer_l(RMSNorm(x))), i.e.
  * pw_moe_forward with PW_ACCUMULATE | PW_PRENORM and y = x.  x: device bf16 [T][H].  Asynchronous; launched as a CUDA graph replay after the first call
  * for a given (x, T, stream). */
