@@ -566,9 +566,15 @@ pw_status pw_set_shared(pw_ctx *c, int layer, const uint16_t *wgu, const uint16_
   LayerDev &l = c->layers[layer];
   const int H = c->d.H, Is = c->d.Is;
   const size_t ngu = sizeof(uint16_t) * 2 * (size_t)Is * H, nd = sizeof(uint16_t) * (size_t)H * Is;
+  // device copies: rows and columns padded to multiples of 128 (operand tiles), zero-filled
+  auto pad128 = [](size_t n) { return (n + 127) / 128 * 128; };
+  const size_t dgu = sizeof(uint16_t) * pad128(2 * (size_t)Is) * pad128(H);
+  const size_t dd = sizeof(uint16_t) * pad128(H) * pad128(Is);
   CU(c, cudaStreamSynchronize(c->compute));
-  if (!l.wgu) CU(c, cudaMalloc((void **)&l.wgu, ngu));
-  if (!l.wd) CU(c, cudaMalloc((void **)&l.wd, nd));
+  if (!l.wgu) CU(c, cudaMalloc((void **)&l.wgu, dgu));
+  if (!l.wd) CU(c, cudaMalloc((void **)&l.wd, dd));
+  CU(c, cudaMemsetAsync(const_cast<uint16_t *>(l.wgu), 0, dgu, c->compute));
+  CU(c, cudaMemsetAsync(const_cast<uint16_t *>(l.wd), 0, dd, c->compute));
   if (pw_status st = ensure_stage(c, std::max(ngu, nd) + 256)) return st;
   int *d_bad = reinterpret_cast<int *>(static_cast<char *>(c->stage) + std::max(ngu, nd));
   CU(c, cudaMemsetAsync(d_bad, 0, sizeof(int), c->compute));

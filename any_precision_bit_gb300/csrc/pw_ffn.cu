@@ -1,59 +1,75 @@
-// pw_ffn.cu -- the expert kernels of the fused mixed-precision MoE layer (sm_103a).
+// pw_ffn.cu -- the expert kernels of the fused mixed-precision MoE layer on the 5th-generation
+// tensor cores (sm_103a).
 //
 // PagedWeight Sec. 3.3: every active expert's linear block is read directly from its
 // bit-planes and LUT at its committed bitwidth q_i (Sec. 3.1 weight page table), the gate_up
 // output goes through SiLU(gate)*up ("expert activation"), and the down projection follows.
 // The shared expert of the layer (Table 1) rides in the same launches.
 //
-// One persistent CTA per SM, warp-specialised:
-//   * warp 8 (producer) walks the CTA's work items and fills a ring of shared-memory stages.
-//     Each stage is one 128-column chunk of a 128-row CTA tile: the q bit-planes (or the
-//     fp16 shared weights) arrive by TMA bulk copies (cp.async.bulk, one per plane, each a
-//     contiguous run thanks to the kernel-private tiling), the tokens' fp16 activation rows
-//     by 16-byte cp.async gathers.  Both complete on the stage's "full" mbarrier.  The
-//     tile's LUT_q rows arrive by one bulk copy per item on a separate barrier pair.
-//   * warps 0..7 (consumers) each own a 16-row warp tile.  Per chunk a thread reads its one
-//     word per plane per row, an 8x8 bit transpose yields the MSB-aligned codes of its
-//     m16n8k16 A fragment, the codes index LUT_q in shared memory, and the fp16 centroids
-//     go straight into the A registers; tokens are the N side (8 per MMA, up to 64 per
-//     item).  A consumer releases the stage on its "empty" mbarrier.
+// A work item is a 128-row tile of one block times up to 64 tokens: D[128][N] = W x X^T,
+// N = tokens padded to 16.  One persistent CTA per SM, warp-specialised:
+//   * plane producer (1 warp): LUT_q rows of the tile (one TMA bulk copy per item) and, per
+//     128-column chunk, the q bit-planes (one bulk copy per plane) into a 4-deep ring;
+//   * A/B producer (1 warp): the tokens' fp16 activation rows (16-byte cp.async gathers) into
+//     the B operand tile and, for the dense shared expert, its fp16 weight tile (one bulk
+//     copy) into the A operand tile, in a 2-deep ring;
+//   * dequantising warps (16): an 8x8 bit transpose turns a row's plane words into codes of
+//     32 consecutive columns, the codes index LUT_q in shared memory, and the fp16 centroids
+//     are stored into the A operand tile (core-matrix layout, 128-bit stores);
+//   * MMA warp (1 thread): eight tcgen05.mma (M=128, N, K=16) per chunk, accumulator in
+//     tensor memory (two buffers), completion signalled to mbarriers by tcgen05.commit;
+//   * the first 8 dequantising warps read the accumulator (tcgen05.ld) and write h = silu(g)*u
+//     or the down output.
 // Every mbarrier wait is bounded: on expiry the kernel records an error (PW_ERR_TIMEOUT on
-// the host), lets the producer wait for the copies it issued, and returns.
+// the host), every role stops, the producers and the MMA thread wait (bounded) for what they
+// issued, and tensor memory is freed before the kernel returns.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "pw_device.cuh"
 #include "pw_internal.h"
+#include "pw_tc.cuh"
 
 namespace pw {
 
-constexpr int kConsumers = kWarpsPerCta;              // 8 consumer warps
-constexpr int kFfnThreads = (kConsumers + 1) * 32;    // + 1 producer warp
-constexpr int kXRowBytes = (kChunkCols + 8) * 2;      // padded activation row: conflict-free B reads
-constexpr int kPlaneStride = kWarpsPerCta * 256;      // bytes of one plane in a stage
-constexpr int kFragStageBytes = 8 * kWarpsPerCta * 512;  // 8 steps of fp16 shared weights
+constexpr int kDq = 16;                     // dequantising warps
+constexpr int kWarpP = kDq;                 // plane producer
+constexpr int kWarpAB = kDq + 1;            // activation / dense-weight producer
+constexpr int kWarpMma = kDq + 2;           // MMA issuer, tensor-memory owner
+constexpr int kTcThreads = (kDq + 3) * 32;
+constexpr int kEpiWarps = 8;                // warps that read the accumulator
+constexpr int kPStages = 4;                 // plane ring depth
+constexpr int kPStageBytes = kMaxPlanes * kWarpsPerCta * 256;  // 16 KB
+constexpr int kPlaneBytes = kWarpsPerCta * 256;                // one plane of a stage
+constexpr int kATileBytes = kCtaRows * kChunkCols * 2;         // 32 KB
+constexpr int kLutBytes = kCtaRows * 256 * 2;                  // LUT_8 of 128 rows
+constexpr int kAccCols = 64;                // tensor-memory columns per accumulator buffer
+constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr long kSpinLimit = 1L << 22;
-constexpr int kSmemLimit = 227 * 1024 - 1024;          // dynamic shared memory per CTA
+constexpr int kSmemLimit = 227 * 1024 - 1024;
 
-struct FfnLayout {
-  int stages;       // ring depth
-  int stage_bytes;  // bytes per stage
-  int x_off;        // activation rows inside a stage
-  int xt;           // activation rows per stage (multiple of 8)
-  int lut_off;      // LUT buffer
-  int bar_off;      // mbarriers: full[S], empty[S], lut_full, lut_empty
-  int smem;         // total dynamic shared memory
+struct TcLayout {
+  int npad_max;    // B tile rows (tokens padded to 16)
+  int ab_bytes;    // one A/B stage: A tile then B tile
+  int ab_off;      // offset of the A/B ring
+  int lut_off;     // LUT region (+512 bytes for alignment)
+  int bar_off;     // mbarriers
+  int smem;        // total dynamic shared memory
 };
+
+// mbarrier indices
+enum { kPF = 0, kPE = kPF + kPStages, kABF = kPE + kPStages, kABE = kABF + 2, kLF = kABE + 2, kLE = kLF + 1,
+       kAF = kLE + 1, kAE = kAF + 2, kDrain = kAE + 2, kNumBars = kDrain + 1 };
 
 struct ItemView {
   bool routed;
   int q;         // routed: committed bitwidth
-  int nchunks;   // 128-column stages
   int nwt;       // warp tiles in this CTA tile
   int NT;        // warp tiles of the block
-  int KC;        // routed: 128-column chunks; shared: 16-column steps (KS)
+  int KC;        // routed: 128-column chunks of the planes
   int Kc;        // activation columns
-  int ntok;
+  int N;         // rows of the block
+  int ntok, npad;
   int row0;      // first activation row: routed slot (expert-sorted), shared token
   const BlockDev *bd;
   const uint16_t *W;  // shared weights
@@ -63,13 +79,13 @@ template <int PHASE>
 __device__ __forceinline__ ItemView view_item(const FwdArgs &a, const WorkItem &w) {
   ItemView v;
   v.ntok = w.ntok;
+  v.npad = max(16, (w.ntok + 15) / 16 * 16);
   if (w.kind == 0) {
     v.routed = true;
     v.bd = &a.table[(a.layer * a.E + w.expert) * 2 + (PHASE - 1)];
     v.q = v.bd->q;
-    v.NT = v.bd->N / 16;
+    v.N = v.bd->N;
     v.KC = v.bd->KC;
-    v.nchunks = v.KC;
     v.Kc = v.bd->K;
     v.row0 = a.s.offsets[w.expert] + w.tok0;
     v.W = nullptr;
@@ -77,14 +93,13 @@ __device__ __forceinline__ ItemView view_item(const FwdArgs &a, const WorkItem &
     v.routed = false;
     v.bd = nullptr;
     v.q = 0;
-    const int N = (PHASE == 1) ? 2 * a.Is : a.H;
+    v.N = (PHASE == 1) ? 2 * a.Is : a.H;
     v.Kc = (PHASE == 1) ? a.H : a.Is;
-    v.NT = N / 16;
-    v.KC = v.Kc / 16;
-    v.nchunks = (v.KC + 7) / 8;
+    v.KC = kpad_cols(v.Kc) / kChunkCols;
     v.row0 = w.tok0;
     v.W = (PHASE == 1) ? a.lay.wgu : a.lay.wd;
   }
+  v.NT = v.N / 16;
   v.nwt = cta_warps(w.tile, v.NT);
   return v;
 }
@@ -99,8 +114,7 @@ __device__ __forceinline__ const uint16_t *act_row(const FwdArgs &a, const ItemV
   return v.routed ? a.s.h_routed + (size_t)(v.row0 + j) * a.I : a.s.h_shared + (size_t)(v.row0 + j) * a.Is;
 }
 
-// LUT buffer: 512-byte aligned inside the dynamic shared memory (same for producer and consumers)
-__device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const FfnLayout &L) {
+__device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const TcLayout &L) {
   return (smem_u32(sm) + L.lut_off + 511u) & ~511u;
 }
 
@@ -114,141 +128,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   atomicExch(err, 1);
   return false;
 }
-
-// ------------------------------------------------------------------ producer warp
-template <int PHASE>
-__device__ void producer(const FwdArgs &a, const FfnLayout &L, uint8_t *sm, uint32_t bars,
-                         volatile int *abort_flag) {
-  const int lane = threadIdx.x & 31;
-  const int S = L.stages;
-  const uint32_t full0 = bars, empty0 = bars + 8 * S, lut_full = bars + 16 * S, lut_empty = lut_full + 8;
-  const int n_items = a.s.n_items[PHASE - 1];
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  uint32_t stage_seq = 0, lut_seq = 0;
-  bool ok = true;
-  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
-    const int rt0 = w.tile * kWarpsPerCta;
-    if (v.routed) {
-      if (lane == 0) {
-        ok = wait_bar(lut_empty, (lut_seq & 1) ^ 1, abort_flag, a.s.err);
-        if (ok) {
-          const uint32_t bytes = (uint32_t)(v.nwt * 16) << v.q << 1;
-          mbar_arrive_expect_tx(lut_full, bytes);
-          bulk_g2s(lut_base(sm, L), v.bd->lut[v.q] + ((size_t)rt0 * 16 << v.q), bytes, lut_full);
-        }
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      ++lut_seq;
-    }
-    // this lane's activation rows (lane, lane + 32): base addresses once per item
-    const uint16_t *rb0 = lane < v.ntok ? act_row<PHASE>(a, v, lane) : nullptr;
-    const uint16_t *rb1 = lane + 32 < v.ntok ? act_row<PHASE>(a, v, lane + 32) : nullptr;
-    for (int kc = w.kc0; kc < w.kc1 && ok; ++kc, ++stage_seq) {
-      const int s = stage_seq % S;
-      const uint32_t ph = (stage_seq / S) & 1;
-      uint8_t *st = sm + (size_t)s * L.stage_bytes;
-      if (lane == 0) ok = wait_bar(empty0 + 8 * s, ph ^ 1, abort_flag, a.s.err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const uint32_t full = full0 + 8 * s;
-      if (lane == 0) {
-        if (v.routed) {
-          const uint32_t bytes = (uint32_t)v.nwt * 256;
-          mbar_arrive_expect_tx(full, bytes * v.q);
-          const long off = plane_pair_word(rt0, kc, v.NT, v.KC);
-          for (int p = 0; p < v.q; ++p)
-            bulk_g2s(smem_u32(st + p * kPlaneStride), v.bd->plane[p] + off, bytes, full);
-        } else {
-          const int nks = min(8, v.KC - kc * 8);
-          const uint32_t bytes = (uint32_t)(nks * v.nwt) * 512;
-          mbar_arrive_expect_tx(full, bytes);
-          bulk_g2s(smem_u32(st), v.W + 2 * frag_pair_word(rt0, kc * 8, v.NT, v.KC), bytes, full);
-        }
-      }
-      const uint32_t xdst = smem_u32(st + L.x_off);
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int j = lane + 32 * r;
-        if (j >= L.xt) break;
-        const uint16_t *rb = r ? rb1 : rb0;
-#pragma unroll 4
-        for (int c16 = 0; c16 < 16; ++c16) {
-          const int col = kc * kChunkCols + c16 * 8;
-          const bool valid = rb != nullptr && col < v.Kc;
-          cp_async16(xdst + j * kXRowBytes + c16 * 16, valid ? rb + col : a.s.xh, valid ? 16u : 0u);
-        }
-      }
-      cp_async_arrive(full);
-    }
-  }
-  // every copy this warp issued must land before the CTA may exit
-  if (lane == 0) {
-    for (uint32_t k = 0; k < (uint32_t)S && k < stage_seq; ++k) {
-      const uint32_t q = stage_seq - 1 - k;
-      for (long i = 0; i < kSpinLimit && !mbar_try_wait(full0 + 8 * (q % S), (q / S) & 1); ++i) {
-      }
-    }
-    if (lut_seq > 0)
-      for (long i = 0; i < kSpinLimit && !mbar_try_wait(lut_full, (lut_seq - 1) & 1); ++i) {
-      }
+// Wait that ignores the abort flag (used to drain what this thread issued); bounded.
+__device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
+  for (long i = 0; i < kSpinLimit && !mbar_try_wait(bar, parity); ++i) {
   }
 }
 
-// ------------------------------------------------------------------ consumer warps
-template <int PHASE, bool SHARED>
-__device__ __forceinline__ void epilogue(const FwdArgs &a, const ItemView &v, int rt, int ngroups,
-                                         float (&acc)[8][4], int part) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j >= ngroups) break;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int tj = 8 * j + 2 * c + h;
-      if (tj >= v.ntok) continue;
-      if (PHASE == 1) {
-        const int f = rt * 8 + g;
-        const float hv = silu(acc[j][h]) * acc[j][2 + h];
-        if (SHARED)
-          a.s.h_shared[(size_t)(v.row0 + tj) * a.Is + f] = f2h(hv);
-        else
-          a.s.h_routed[(size_t)(v.row0 + tj) * a.I + f] = f2h(hv);
-      } else {
-        const int r0 = rt * 16 + g;
-        float *dst = SHARED ? a.s.o_shared + ((size_t)part * a.T + v.row0 + tj) * a.H
-                            : a.s.o_routed + (size_t)(v.row0 + tj) * a.H;
-        dst[r0] = acc[j][h];
-        dst[r0 + 8] = acc[j][2 + h];
-      }
-    }
-  }
-}
-
-// ldmatrix row address of this thread for B fragments: matrices (group j, k 0-7), (j, k 8-15),
-// (j+1, k 0-7), (j+1, k 8-15) of a 16-column step; rows are tokens.
-__device__ __forceinline__ uint32_t b_lane_offset() {
-  const int lane = threadIdx.x & 31;
-  return (uint32_t)(((((lane >> 4) & 1) * 8 + (lane & 7)) * kXRowBytes) + ((lane >> 3) & 1) * 16);
-}
-
-// B fragments of all token groups of one 16-column step, two groups per ldmatrix.
-template <int NG>
-__device__ __forceinline__ void load_b_step(uint32_t xs_lane, int s, uint32_t (&b)[8][2]) {
-#pragma unroll
-  for (int j = 0; j < NG; j += 2) {
-    const uint32_t addr = xs_lane + j * 8 * kXRowBytes + s * 32;
-    if (j + 1 < NG)
-      ldm_x4(addr, b[j][0], b[j][1], b[j + 1][0], b[j + 1][1]);
-    else
-      ldm_x2(addr, b[j][0], b[j][1]);
-  }
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
 // Shared-memory address of LUT entry `code` of a row whose table starts at a base aligned to
-// 2^(Q+1) bytes: the code, shifted to bytes, is OR-ed into the base.  Y holds MSB-aligned
-// codes in its bytes; E selects the byte.
+// 2^(Q+1) bytes; Y holds MSB-aligned codes in its bytes and E selects the byte.
 template <int Q, int E>
 __device__ __forceinline__ uint32_t lut_addr(uint32_t Y, uint32_t base) {
   constexpr int sh = 8 * E + 7 - Q;
@@ -256,216 +147,352 @@ __device__ __forceinline__ uint32_t lut_addr(uint32_t Y, uint32_t base) {
   const uint32_t v = sh >= 0 ? (Y >> (sh >= 0 ? sh : 0)) : (Y << (sh < 0 ? -sh : 0));
   return (v & m) | base;
 }
-
-// The A-fragment register of elements (E, E+1) of row base `base` from code word Y.
+// fp16 centroids of the codes in bytes E and E+1 of Y, packed low-first.
 template <int Q, int E>
 __device__ __forceinline__ uint32_t lut_pair(uint32_t Y, uint32_t base) {
   return lds_pair(lut_addr<Q, E>(Y, base), lut_addr<Q, E + 1>(Y, base));
 }
 
-// One stage of a routed item at compile-time group count NG.
-template <int Q, int NG>
-__device__ __forceinline__ void routed_stage(const uint8_t *st, uint32_t xs_lane, uint32_t lg, uint32_t l8,
-                                             float (&acc)[8][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint2 pw_[Q];
+// Dequantise 32 consecutive columns of one row (the thread's plane words) into the A tile.
+template <int Q>
+__device__ __forceinline__ void dq_chunk(const uint8_t *pslot, uint32_t a_tile, uint32_t lut0, int tw, int half,
+                                         int lane) {
+  uint32_t Y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) Y[i] = 0u;
 #pragma unroll
   for (int p = 0; p < Q; ++p)
-    pw_[p] = *reinterpret_cast<const uint2 *>(st + p * kPlaneStride + warp * 256 + lane * 8);
-  uint32_t Yg[8], Y8[8];
-  codes_from_planes<Q>(pw_, Yg, Y8);
+    Y[7 - p] = *reinterpret_cast<const uint32_t *>(pslot + p * kPlaneBytes + tw * 256 + (lane * 2 + half) * 4);
+  transpose8(Y);
+  const int row = tw * 16 + half * 8 + (lane & 7);
+  const uint32_t lb = lut0 + ((uint32_t)row << (Q + 1));
+  const uint32_t dst = a_tile + (uint32_t)core_offset128(row, (lane >> 3) * 32);
 #pragma unroll
-  for (int s8 = 0; s8 < 8; ++s8) {
-    const uint32_t a0 = lut_pair<Q, 0>(Yg[s8], lg);
-    const uint32_t a1 = lut_pair<Q, 0>(Y8[s8], l8);
-    const uint32_t a2 = lut_pair<Q, 2>(Yg[s8], lg);
-    const uint32_t a3 = lut_pair<Q, 2>(Y8[s8], l8);
-    uint32_t b[8][2];
-    load_b_step<NG>(xs_lane, s8, b);
-#pragma unroll
-    for (int j = 0; j < NG; ++j) mma_f16(acc[j], a0, a1, a2, a3, b[j][0], b[j][1]);
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t r0 = lut_pair<Q, 0>(Y[2 * m], lb);
+    const uint32_t r1 = lut_pair<Q, 2>(Y[2 * m], lb);
+    const uint32_t r2 = lut_pair<Q, 0>(Y[2 * m + 1], lb);
+    const uint32_t r3 = lut_pair<Q, 2>(Y[2 * m + 1], lb);
+    sts128(dst + m * 128, r0, r1, r2, r3);
   }
 }
 
-// Returns false when a wait gave up.
-template <int PHASE, int Q>
-__device__ bool routed_item(const FwdArgs &a, const FfnLayout &L, uint8_t *sm, uint32_t bars,
-                            volatile int *abort_flag, const ItemView &v, const WorkItem &w,
-                            uint32_t &stage_seq, uint32_t &lut_seq) {
-  const int tile = w.tile;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2;
-  const int S = L.stages;
-  const uint32_t full0 = bars, empty0 = bars + 8 * S, lut_full = bars + 16 * S, lut_empty = lut_full + 8;
-  const bool active = warp < v.nwt;
-  const int rt = tile * kWarpsPerCta + warp;
-  const int ngroups = (v.ntok + 7) / 8;
-  const uint32_t lg = lut_base(sm, L) + ((uint32_t)(warp * 16 + g) << (Q + 1));
-  const uint32_t l8 = lg + (8u << (Q + 1));
-  const uint32_t xoff = (uint32_t)L.x_off + b_lane_offset();
-  float acc[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
-  if (!wait_bar(lut_full, lut_seq & 1, abort_flag, a.s.err)) return false;
-  for (int kc = w.kc0; kc < w.kc1; ++kc, ++stage_seq) {
-    const int s = stage_seq % S;
-    if (!wait_bar(full0 + 8 * s, (stage_seq / S) & 1, abort_flag, a.s.err)) return false;
-    const uint8_t *st = sm + (size_t)s * L.stage_bytes;
-    if (active) {
-      const uint32_t xs_lane = smem_u32(st) + xoff;
-      switch (ngroups) {
-        case 1: routed_stage<Q, 1>(st, xs_lane, lg, l8, acc); break;
-        case 2: routed_stage<Q, 2>(st, xs_lane, lg, l8, acc); break;
-        case 3: case 4: routed_stage<Q, 4>(st, xs_lane, lg, l8, acc); break;
-        default: routed_stage<Q, 8>(st, xs_lane, lg, l8, acc); break;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
-  }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(lut_empty);
-  ++lut_seq;
-  if (active) epilogue<PHASE, false>(a, v, rt, ngroups, acc, 0);
-  return true;
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
 }
 
-template <int NG>
-__device__ __forceinline__ void shared_stage(const uint8_t *st, uint32_t xs_lane, int nks, int nwt,
-                                             float (&acc)[8][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int ks = 0; ks < nks; ++ks) {
-    const uint4 af = *reinterpret_cast<const uint4 *>(st + (ks * nwt + warp) * 512 + lane * 16);
-    uint32_t b[8][2];
-    load_b_step<NG>(xs_lane, ks, b);
-#pragma unroll
-    for (int j = 0; j < NG; ++j) mma_f16(acc[j], af.x, af.y, af.z, af.w, b[j][0], b[j][1]);
-  }
-}
-
+// ------------------------------------------------------------------ roles
 template <int PHASE>
-__device__ bool shared_item(const FwdArgs &a, const FfnLayout &L, uint8_t *sm, uint32_t bars,
-                            volatile int *abort_flag, const ItemView &v, const WorkItem &w,
-                            uint32_t &stage_seq) {
-  const int tile = w.tile;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int S = L.stages;
-  const uint32_t full0 = bars, empty0 = bars + 8 * S;
-  const bool active = warp < v.nwt;
-  const int rt = tile * kWarpsPerCta + warp;
-  const int ngroups = (v.ntok + 7) / 8;
-  const uint32_t xoff = (uint32_t)L.x_off + b_lane_offset();
-  float acc[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
-  for (int kc = w.kc0; kc < w.kc1; ++kc, ++stage_seq) {
-    const int s = stage_seq % S;
-    if (!wait_bar(full0 + 8 * s, (stage_seq / S) & 1, abort_flag, a.s.err)) return false;
-    const uint8_t *st = sm + (size_t)s * L.stage_bytes;
-    if (active) {
-      const int nks = min(8, v.KC - kc * 8);
-      const uint32_t xs_lane = smem_u32(st) + xoff;
-      switch (ngroups) {
-        case 1: shared_stage<1>(st, xs_lane, nks, v.nwt, acc); break;
-        case 2: shared_stage<2>(st, xs_lane, nks, v.nwt, acc); break;
-        case 3: case 4: shared_stage<4>(st, xs_lane, nks, v.nwt, acc); break;
-        default: shared_stage<8>(st, xs_lane, nks, v.nwt, acc); break;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
-  }
-  if (active) epilogue<PHASE, true>(a, v, rt, ngroups, acc, w.part);
-  return true;
-}
-
-template <int PHASE>
-__device__ void consumer(const FwdArgs &a, const FfnLayout &L, uint8_t *sm, uint32_t bars,
-                         volatile int *abort_flag) {
+__device__ void plane_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                               volatile int *abort_flag) {
+  if ((threadIdx.x & 31) != 0) return;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  uint32_t stage_seq = 0, lut_seq = 0;
+  uint32_t p_seq = 0, lut_seq = 0;
+  bool ok = true;
+  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    const WorkItem w = items[it];
+    const ItemView v = view_item<PHASE>(a, w);
+    if (!v.routed) continue;
+    const int rt0 = w.tile * kWarpsPerCta;
+    ok = wait_bar(bars + 8 * kLE, (lut_seq & 1) ^ 1, abort_flag, a.s.err);
+    if (!ok) break;
+    const uint32_t lbytes = (uint32_t)(v.nwt * 16) << v.q << 1;
+    mbar_arrive_expect_tx(bars + 8 * kLF, lbytes);
+    bulk_g2s(lut_base(sm, L), v.bd->lut[v.q] + ((size_t)rt0 * 16 << v.q), lbytes, bars + 8 * kLF);
+    ++lut_seq;
+    for (int kc = w.kc0; kc < w.kc1; ++kc) {
+      const int ps = p_seq % kPStages;
+      ok = wait_bar(bars + 8 * (kPE + ps), ((p_seq / kPStages) & 1) ^ 1, abort_flag, a.s.err);
+      if (!ok) break;
+      const uint32_t bytes = (uint32_t)v.nwt * 256;
+      const uint32_t full = bars + 8 * (kPF + ps);
+      mbar_arrive_expect_tx(full, bytes * v.q);
+      const long off = plane_pair_word(rt0, kc, v.NT, v.KC);
+      const uint32_t dst = smem_u32(sm) + ps * kPStageBytes;
+      for (int p = 0; p < v.q; ++p) bulk_g2s(dst + p * kPlaneBytes, v.bd->plane[p] + off, bytes, full);
+      ++p_seq;
+    }
+  }
+  // every copy issued must land before the CTA may exit
+  for (uint32_t k = 0; k < (uint32_t)kPStages && k < p_seq; ++k) {
+    const uint32_t q = p_seq - 1 - k;
+    drain_bar(bars + 8 * (kPF + q % kPStages), (q / kPStages) & 1);
+  }
+  if (lut_seq > 0) drain_bar(bars + 8 * kLF, (lut_seq - 1) & 1);
+}
+
+template <int PHASE>
+__device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                            volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int n_items = a.s.n_items[PHASE - 1];
+  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  uint32_t ab_seq = 0;
+  bool ok = true;
+  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    const WorkItem w = items[it];
+    const ItemView v = view_item<PHASE>(a, w);
+    const uint16_t *rb0 = lane < v.ntok ? act_row<PHASE>(a, v, lane) : nullptr;
+    const uint16_t *rb1 = lane + 32 < v.ntok ? act_row<PHASE>(a, v, lane + 32) : nullptr;
+    for (int kc = w.kc0; kc < w.kc1; ++kc) {
+      const int as = ab_seq % 2;
+      if (lane == 0) ok = wait_bar(bars + 8 * (kABE + as), ((ab_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const uint32_t full = bars + 8 * (kABF + as);
+      const uint32_t a_tile = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
+      const uint32_t b_tile = a_tile + kATileBytes;
+      if (lane == 0) {
+        if (v.routed) {
+          mbar_arrive(full);
+        } else {
+          mbar_arrive_expect_tx(full, kATileBytes);
+          const long tile_elem = ((long)w.tile * v.KC + kc) * (kCtaRows * kChunkCols);
+          bulk_g2s(a_tile, v.W + tile_elem, kATileBytes, full);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int j = lane + 32 * r;
+        if (j >= v.npad) break;
+        const uint16_t *rb = r ? rb1 : rb0;
+#pragma unroll 4
+        for (int c16 = 0; c16 < 16; ++c16) {
+          const int col = kc * kChunkCols + c16 * 8;
+          const bool valid = rb != nullptr && col < v.Kc;
+          cp_async16(b_tile + core_offset128(j, c16 * 8), valid ? rb + col : a.s.xh, valid ? 16u : 0u);
+        }
+      }
+      cp_async_arrive(full);
+      ++ab_seq;
+    }
+  }
+  if (lane == 0)
+    for (uint32_t k = 0; k < 2 && k < ab_seq; ++k) {
+      const uint32_t q = ab_seq - 1 - k;
+      drain_bar(bars + 8 * (kABF + q % 2), (q / 2) & 1);
+    }
+}
+
+template <int PHASE>
+__device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
+                           volatile int *abort_flag) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int n_items = a.s.n_items[PHASE - 1];
+  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  uint32_t ab_seq = 0, item_seq = 0;
+  bool ok = true;
+  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    const WorkItem w = items[it];
+    const ItemView v = view_item<PHASE>(a, w);
+    const uint32_t idesc = idesc_f16_f32(128, v.npad);
+    const int acs = item_seq % 2;
+    ok = wait_bar(bars + 8 * (kAE + acs), ((item_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
+    if (!ok) break;
+    tc_fence_after();
+    const uint32_t d = tmem + acs * kAccCols;
+    bool first = true;
+    for (int kc = w.kc0; kc < w.kc1; ++kc) {
+      const int as = ab_seq % 2;
+      ok = wait_bar(bars + 8 * (kABF + as), (ab_seq / 2) & 1, abort_flag, a.s.err);
+      if (!ok) break;
+      // the B rows (and routed A) were written through the generic proxy; the MMAs read
+      // them through the async proxy
+      fence_async_smem();
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
+      const uint32_t b0 = a0 + kATileBytes;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const uint64_t ad = smem_desc(a0 + 256 * t, 128, 16 * 128);
+        const uint64_t bd = smem_desc(b0 + 256 * t, 128, 16 * 128);
+        tc_mma_f16(d, ad, bd, idesc, (first && t == 0) ? 0u : 1u);
+      }
+      first = false;
+      tc_commit(bars + 8 * (kABE + as));
+      ++ab_seq;
+    }
+    if (!ok) break;
+    tc_commit(bars + 8 * (kAF + acs));
+    ++item_seq;
+  }
+  // every MMA issued must complete before tensor memory is freed
+  tc_commit(bars + 8 * kDrain);
+  drain_bar(bars + 8 * kDrain, 0);
+}
+
+template <int PHASE>
+__device__ void dequant_and_epilogue(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
+                                     volatile int *abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tw = warp % kWarpsPerCta, half = warp / kWarpsPerCta;
+  const int n_items = a.s.n_items[PHASE - 1];
+  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  const uint32_t lut0 = lut_base(sm, L);
+  uint32_t p_seq = 0, ab_seq = 0, lut_seq = 0, item_seq = 0;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
-    bool ok;
-    if (!v.routed) {
-      ok = shared_item<PHASE>(a, L, sm, bars, abort_flag, v, w, stage_seq);
-    } else {
-      switch (v.q) {
-        case 1: ok = routed_item<PHASE, 1>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        case 2: ok = routed_item<PHASE, 2>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        case 3: ok = routed_item<PHASE, 3>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        case 4: ok = routed_item<PHASE, 4>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        case 5: ok = routed_item<PHASE, 5>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        case 6: ok = routed_item<PHASE, 6>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        case 7: ok = routed_item<PHASE, 7>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
-        default: ok = routed_item<PHASE, 8>(a, L, sm, bars, abort_flag, v, w, stage_seq, lut_seq); break;
+    const bool active = tw < v.nwt;
+    if (v.routed && !wait_bar(bars + 8 * kLF, lut_seq & 1, abort_flag, a.s.err)) return;
+    for (int kc = w.kc0; kc < w.kc1; ++kc) {
+      const int as = ab_seq % 2;
+      if (!wait_bar(bars + 8 * (kABE + as), ((ab_seq / 2) & 1) ^ 1, abort_flag, a.s.err)) return;
+      if (v.routed) {
+        const int ps = p_seq % kPStages;
+        if (!wait_bar(bars + 8 * (kPF + ps), (p_seq / kPStages) & 1, abort_flag, a.s.err)) return;
+        if (active) {
+          const uint8_t *pslot = sm + ps * kPStageBytes;
+          const uint32_t a_tile = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
+          switch (v.q) {
+            case 1: dq_chunk<1>(pslot, a_tile, lut0, tw, half, lane); break;
+            case 2: dq_chunk<2>(pslot, a_tile, lut0, tw, half, lane); break;
+            case 3: dq_chunk<3>(pslot, a_tile, lut0, tw, half, lane); break;
+            case 4: dq_chunk<4>(pslot, a_tile, lut0, tw, half, lane); break;
+            case 5: dq_chunk<5>(pslot, a_tile, lut0, tw, half, lane); break;
+            case 6: dq_chunk<6>(pslot, a_tile, lut0, tw, half, lane); break;
+            case 7: dq_chunk<7>(pslot, a_tile, lut0, tw, half, lane); break;
+            default: dq_chunk<8>(pslot, a_tile, lut0, tw, half, lane); break;
+          }
+          fence_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (kPE + ps));
+        ++p_seq;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (kABF + as));
+      ++ab_seq;
     }
-    if (!ok) return;
+    if (v.routed) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * kLE);
+      ++lut_seq;
+    }
+    // epilogue: the accumulator of this item (tensor-memory lanes = tile rows, columns = tokens)
+    if (warp < kEpiWarps) {
+      const int acs = item_seq % 2;
+      if (!wait_bar(bars + 8 * (kAF + acs), (item_seq / 2) & 1, abort_flag, a.s.err)) return;
+      tc_fence_after();
+      const int quarter = warp % 4, colhalf = warp / 4;
+      const int ncols = v.npad / 2, col0 = colhalf * ncols;
+      const int row = 32 * quarter + lane;  // tile row
+      const int R = w.tile * kCtaRows + row;
+      const bool empty = w.kc1 <= w.kc0;     // nothing accumulated (an empty split part)
+      const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * kAccCols;
+      for (int c = 0; c < ncols; c += 8) {
+        uint32_t r[8];
+        tmem_ld8(taddr + col0 + c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float acc = empty ? 0.f : __uint_as_float(r[i]);
+          const int j = col0 + c + i;
+          if (PHASE == 1) {
+            const float up = __shfl_down_sync(0xffffffffu, acc, 8);
+            if ((row & 15) < 8 && R < v.N && j < v.ntok) {
+              const int f = R / 16 * 8 + (R & 7);
+              const uint16_t hv = f2h(silu(acc) * up);
+              if (v.routed)
+                a.s.h_routed[(size_t)(v.row0 + j) * a.I + f] = hv;
+              else
+                a.s.h_shared[(size_t)(v.row0 + j) * a.Is + f] = hv;
+            }
+          } else if (R < v.N && j < v.ntok) {
+            if (v.routed)
+              a.s.o_routed[(size_t)(v.row0 + j) * a.H + R] = acc;
+            else
+              a.s.o_shared[((size_t)w.part * a.T + v.row0 + j) * a.H + R] = acc;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (kAE + acs));
+    }
+    ++item_seq;
   }
 }
 
 template <int PHASE>
-__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(FwdArgs a, FfnLayout L) {
-  extern __shared__ __align__(128) uint8_t sm[];
+__global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayout L) {
+  extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ int abort_flag;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5;
   const uint32_t bars = smem_u32(sm + L.bar_off);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L.stages; ++s) {
-      mbar_init(bars + 8 * s, 33);                             // full: 1 expect_tx + 32 cp.async lanes
-      mbar_init(bars + 8 * (L.stages + s), kConsumers);        // empty: one arrival per consumer warp
+    for (int i = 0; i < kPStages; ++i) {
+      mbar_init(bars + 8 * (kPF + i), 1);
+      mbar_init(bars + 8 * (kPE + i), kDq);
     }
-    mbar_init(bars + 16 * L.stages, 1);                        // lut_full
-    mbar_init(bars + 16 * L.stages + 8, kConsumers);           // lut_empty
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars + 8 * (kABF + i), 32 + 1 + kDq);  // cp.async lanes, producer lane 0, dequantisers
+      mbar_init(bars + 8 * (kABE + i), 1);
+      mbar_init(bars + 8 * (kAF + i), 1);
+      mbar_init(bars + 8 * (kAE + i), kEpiWarps);
+    }
+    mbar_init(bars + 8 * kLF, 1);
+    mbar_init(bars + 8 * kLE, kDq);
+    mbar_init(bars + 8 * kDrain, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
-  if ((threadIdx.x >> 5) == kConsumers)
-    producer<PHASE>(a, L, sm, bars, &abort_flag);
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  if (warp < kDq)
+    dequant_and_epilogue<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+  else if (warp == kWarpP)
+    plane_producer<PHASE>(a, L, sm, bars, &abort_flag);
+  else if (warp == kWarpAB)
+    ab_producer<PHASE>(a, L, sm, bars, &abort_flag);
   else
-    consumer<PHASE>(a, L, sm, bars, &abort_flag);
+    mma_issuer<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
 }
 
-static FfnLayout ffn_layout(const FwdArgs &a, int bmax_lut_entries) {
-  FfnLayout L{};
-  const int wbytes = a.Is > 0 ? kFragStageBytes : kMaxPlanes * kPlaneStride;
-  // activation rows per stage: the token groups rounded the way the consumers round them
-  // (1, 2, 4 or 8 groups of 8), so that every row an ldmatrix reads lies in the stage
-  const int groups = (min(a.T, kTokChunk) + 7) / 8;
-  L.xt = 8 * (groups <= 2 ? groups : (groups <= 4 ? 4 : 8));
-  L.x_off = wbytes;
-  L.stage_bytes = (wbytes + L.xt * kXRowBytes + 127) / 128 * 128;
-  const int lut_bytes = kCtaRows * bmax_lut_entries * 2 + 512;  // + alignment slack
-  const int budget = kSmemLimit - lut_bytes - 256;
-  L.stages = min(6, budget / L.stage_bytes);
-  L.lut_off = L.stages * L.stage_bytes;
-  L.bar_off = L.lut_off + lut_bytes;
-  L.smem = L.bar_off + (2 * L.stages + 2) * 8;
+static TcLayout tc_layout(const FwdArgs &a) {
+  TcLayout L{};
+  L.npad_max = max(16, (min(a.T, kTokChunk) + 15) / 16 * 16);
+  L.ab_bytes = kATileBytes + L.npad_max * kChunkCols * 2;
+  L.ab_off = kPStages * kPStageBytes;
+  L.lut_off = L.ab_off + 2 * L.ab_bytes;
+  L.bar_off = L.lut_off + kLutBytes + 512;
+  L.smem = L.bar_off + kNumBars * 8;
   return L;
 }
 
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
-  const FfnLayout L = ffn_layout(a, 256);
-  if (L.stages < 2) return (int)cudaErrorInvalidConfiguration;
+  const TcLayout L = tc_layout(a);
+  if (L.smem > kSmemLimit) return (int)cudaErrorInvalidConfiguration;
   static int attr_done = 0;
   if (!attr_done) {
-    cudaFuncSetAttribute(ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    cudaFuncSetAttribute(ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     attr_done = 1;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
   const int grid = min(max_items, a.sm_count);
   if (phase == 1)
-    ffn_kernel<1><<<grid, kFfnThreads, L.smem, st>>>(a, L);
+    tc_ffn_kernel<1><<<grid, kTcThreads, L.smem, st>>>(a, L);
   else
-    ffn_kernel<2><<<grid, kFfnThreads, L.smem, st>>>(a, L);
+    tc_ffn_kernel<2><<<grid, kTcThreads, L.smem, st>>>(a, L);
   return (int)cudaGetLastError();
 }
 

@@ -8,10 +8,11 @@
 //   by 8 into CTA tiles of 128 rows (the last CTA tile may hold fewer).  Within a CTA tile
 //   the data of one plane is ordered [chunk][warp tile][64 words], so one 128-column stage
 //   of a CTA tile is a single contiguous run of (warp tiles x 256) bytes per plane.
-//   Word (lane * 2 + r) of a (chunk, warp tile) belongs to thread `lane` of the warp and row
-//   (g + 8r) of the warp tile, g = lane / 4; its bit (8e + s) holds column 16 s + kofs(c, e)
-//   of the chunk, c = lane % 4, kofs = {2c, 2c+1, 2c+8, 2c+9}[e]: exactly the elements of
-//   the m16n8k16 A fragment that thread holds for the chunk's eight 16-column steps.
+//   Word (lane * 2 + r) of a (chunk, warp tile) holds row (8r + lane % 8) of the warp tile
+//   and the 32 columns [32 (lane / 8), 32 (lane / 8) + 32) of the chunk: bit (8e + s) is
+//   column 32 (lane / 8) + 4 s + e.  After an 8x8 bit transpose of a row's plane words, byte
+//   e of word s is the code of column 4 s + e, so one thread turns a word per plane into 32
+//   consecutive dequantised columns of one row.
 #pragma once
 #include <stdint.h>
 
@@ -90,36 +91,30 @@ PW_HD long plane_pair_word(int rt, int kc, int NT, int KC) {
 
 // word index inside a tiled plane and bit inside that word for (device row d, column k)
 PW_HD void tile_pos(int d, int k, int N, int KC, long *word, int *bit) {
-  int rt = d / 16, ri = d % 16;
-  int g = ri % 8, r = ri / 8;
-  int kc = k / 128, kk = k % 128;
-  int s = kk / 16, kin = kk % 16;
-  int c = (kin % 8) / 2;
-  int e = (kin & 1) + 2 * (kin / 8);
-  int lane = 4 * g + c;
+  const int rt = d / 16, ri = d % 16;
+  const int r = ri / 8, g8 = ri % 8;
+  const int kc = k / 128, kk = k % 128;
+  const int seg = kk / 32, kin = kk % 32;
+  const int s = kin / 4, e = kin % 4;
+  const int lane = seg * 8 + g8;
   *word = plane_pair_word(rt, kc, N / 16, KC) + lane * 2 + r;
   *bit = 8 * e + s;
 }
 
-// Kernel-private layout of dense fp16 shared-expert weights (N x K, N % 16 == 0,
-// K % 16 == 0): per (16-row warp tile, 16-column step) 128 words in which thread `lane`
-// holds 4 words = its m16n8k16 A fragment: (g, 2c..2c+1), (g+8, 2c..), (g, 2c+8..2c+9),
-// (g+8, 2c+8..).  Warp tiles are grouped by 8 like the planes and ordered [step][warp tile]
-// inside a CTA tile, so consecutive steps of a CTA tile are one contiguous run.
-PW_HD long frag_pair_word(int rt, int ks, int NT, int KS) {
-  const int ct = rt / kWarpsPerCta, w = rt % kWarpsPerCta;
-  return ((long)ct * kWarpsPerCta * KS + (long)ks * cta_warps(ct, NT) + w) * 128;
+// Operand tiles of the tensor-core MMAs are stored as 8x8 "core matrices" of fp16 (128
+// contiguous bytes, row i at byte 16 i); in a tile of R rows by 128 columns, core matrix
+// (row group rg, column group kc) sits at byte (rg * 16 + kc) * 128.
+PW_HD int core_offset128(int row, int col) {
+  return ((row >> 3) * 16 + (col >> 3)) * 128 + (row & 7) * 16 + (col & 7) * 2;
 }
-PW_HD long frag16_index(int d, int k, int N, int K) {
-  int rt = d / 16, ri = d % 16;
-  int g = ri % 8, r = ri / 8;
-  int st = k / 16, kin = k % 16;
-  int c = (kin % 8) / 2;
-  int hi = kin / 8;
-  int lane = 4 * g + c;
-  int reg = r + 2 * hi;  // 0: (g,lo) 1: (g+8,lo) 2: (g,hi) 3: (g+8,hi)
-  long word = frag_pair_word(rt, st, N / 16, K / 16) + lane * 4 + reg;
-  return word * 2 + (kin & 1);  // element index (16-bit units)
+
+// Kernel-private layout of dense fp16 shared-expert weights (N x K): rows padded to a
+// multiple of 128, columns to a multiple of 128; each (128-row tile, 128-column chunk) is a
+// contiguous 32 KB operand tile in the core-matrix order above, tiles ordered [tile][chunk].
+PW_HD long shared_tile_index(int d, int k, int K) {
+  const int KCh = kpad_cols(K) / kChunkCols;
+  return ((long)(d / kCtaRows) * KCh + k / kChunkCols) * (kCtaRows * kChunkCols) +
+         core_offset128(d % kCtaRows, k % kChunkCols) / 2;
 }
 
 }  // namespace pw

@@ -407,14 +407,12 @@ __global__ void pack_kernel(const uint8_t *idx, int N, int K, int KC, int u, int
   const long tk = li >> 6;
   const int kc = (int)(tk % KC);
   const int rt = (int)(tk / KC);
-  const int g = lane >> 2, c = lane & 3;
-  const int d = rt * 16 + g + 8 * r;
+  const int d = rt * 16 + 8 * r + (lane & 7);
   const int row = orig_row(d, u, I);
   uint32_t words[kMaxPlanes] = {0, 0, 0, 0, 0, 0, 0, 0};
   for (int e = 0; e < 4; ++e) {
-    const int kofs = 2 * c + (e & 1) + 8 * (e >> 1);
     for (int s = 0; s < 8; ++s) {
-      const int col = kc * 128 + 16 * s + kofs;
+      const int col = kc * 128 + 32 * (lane >> 3) + 4 * s + e;
       const uint32_t code = (col < K) ? idx[(size_t)row * K + col] : 0u;
       for (int p = 0; p < bmax; ++p) words[p] |= ((code >> (bmax - 1 - p)) & 1u) << (8 * e + s);
     }
@@ -448,14 +446,15 @@ int launch_lut_permute(const uint16_t *lut_in, int N, int entries, int u, int I,
   return (int)cudaGetLastError();
 }
 
-// bf16 -> fp16 in the frag16 layout; counts values that overflow fp16 into *bad.
+// bf16 -> fp16 in the shared-weight operand-tile layout (the output is pre-zeroed, so the
+// padding rows and columns stay zero); counts values that overflow fp16 into *bad.
 __global__ void frag16_kernel(const uint16_t *in, int N, int K, int u, int I, uint16_t *out, int *bad) {
   long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long)N * K) return;
   const int d = (int)(i / K), k = (int)(i % K);
   const float v = bf16f(in[(size_t)orig_row(d, u, I) * K + k]);
   if (!(fabsf(v) <= 65504.0f)) atomicAdd(bad, 1);
-  out[frag16_index(d, k, N, K)] = f2h(v);
+  out[shared_tile_index(d, k, K)] = f2h(v);
 }
 
 int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_out, int *bad, void *stream) {
@@ -469,7 +468,7 @@ int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_
 template <int Q>
 __device__ void unpack_chunk(const BlockDev &bd, int rt, int kc, int u, int I, uint8_t *idx_out,
                              uint16_t *w_out) {
-  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+  const int lane = threadIdx.x & 31;
   const long base = plane_pair_word(rt, kc, bd.N / 16, bd.KC) / 2 + lane;
   uint2 pw_[Q];
 #pragma unroll
@@ -478,13 +477,13 @@ __device__ void unpack_chunk(const BlockDev &bd, int rt, int kc, int u, int I, u
   codes_from_planes<Q>(pw_, Yg, Y8);
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
-    const int d = rt * 16 + g + 8 * r;
+    const int d = rt * 16 + 8 * r + (lane & 7);
     const int row = orig_row(d, u, I);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int col = kc * 128 + 16 * s + 2 * c + (e & 1) + 8 * (e >> 1);
+        const int col = kc * 128 + 32 * (lane >> 3) + 4 * s + e;
         if (col >= bd.K) continue;
         const uint32_t code = code_at<Q>(r ? Y8[s] : Yg[s], e);
         if (idx_out) idx_out[(size_t)row * bd.K + col] = (uint8_t)code;

@@ -316,6 +316,13 @@ pw_status pw_unpack_indices(pw_ctx *ctx, int block, int b, uint8_t *host_out);
  * host fp16 bits [N][K].  Pages 0..b-1 and LUT_b must be GPU-resident.  Waits. */
 pw_status pw_dequant(pw_ctx *ctx, int block, int b, uint16_t *host_out);
 
+/* Self-check of the 5th-generation tensor-core path (tcgen05) on one CTA: D[128][N] =
+ * A[128][K] * B[N][K]^T with fp16 A, B (row-major, device) and fp32 D (row-major, device),
+ * 16 <= N <= 256 and 16 <= K <= 128, both multiples of 16.  *err (device int) is set to 1
+ * if the bounded wait for the MMAs expired.  Asynchronous on `stream`. */
+pw_status pw_tc_selftest(const uint16_t *A, const uint16_t *B, int N, int K, float *D, int *err,
+                         pw_stream stream);
+
 /* Pure host helpers (no context, no GPU) for checking the packer.
  * pw_pack_planes_host: the plain plane layout -- planes [bmax][N][W] uint32,
  *   W = ceil(K/128)*4 words per row, bit j of word w is column 32w+j, plane 0 = MSB.
