@@ -363,7 +363,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.slot_w, sizeof(float) * TK) &&
             salloc((void **)&c->s.items1, sizeof(WorkItem) * c->s.max_items1) &&
             salloc((void **)&c->s.items2, sizeof(WorkItem) * c->s.max_items2) &&
-            salloc((void **)&c->s.n_items, sizeof(int) * 2) && salloc((void **)&c->s.ticket, sizeof(unsigned)) &&
+            salloc((void **)&c->s.n_items, sizeof(int) * 2) && salloc((void **)&c->s.ticket, sizeof(unsigned) * (1 + (Tm + 7) / 8)) &&
             salloc((void **)&c->s.h_routed, sizeof(uint16_t) * TK * d.I) &&
             salloc((void **)&c->s.h_shared, sizeof(uint16_t) * Tm * std::max(d.Is, 1)) &&
             salloc((void **)&c->s.o_routed, sizeof(float) * TK * d.H) &&
@@ -378,7 +378,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
     fail(nullptr, PW_ERR_OOM, "scratch allocation failed (max_tokens=%d)", d.max_tokens);
     return bail(PW_ERR_OOM);
   }
-  cudaMemset(c->s.ticket, 0, sizeof(unsigned));
+  cudaMemset(c->s.ticket, 0, sizeof(unsigned) * (1 + (Tm + 7) / 8));
   cudaMemset(c->s.err, 0, sizeof(int));
   cudaMemset(c->s.stat_count, 0, sizeof(double) * d.L * d.E);
   cudaMemset(c->s.stat_wsum, 0, sizeof(double) * d.L * d.E);

@@ -136,7 +136,7 @@ struct Scratch {
   WorkItem *items1;    // gate_up work
   WorkItem *items2;    // down work
   int *n_items;        // [2]
-  unsigned *ticket;    // [1] last-CTA counter of the router
+  unsigned *ticket;    // [1 + ceil(Tm/8)] router last-CTA counters: all token groups, then per group
   uint16_t *xh;        // fp16 [Tm][H]: the layer input as the experts read it (normalised under PW_PRENORM)
   uint16_t *h_routed;  // fp16 [Tm*K][I]
   uint16_t *h_shared;  // fp16 [Tm][Is]

@@ -59,7 +59,7 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
       sizeof(WorkItem) * n1,        // items1
       sizeof(WorkItem) * n2,        // items2
       sizeof(int) * 2,              // n_items
-      sizeof(unsigned),             // ticket
+      sizeof(unsigned) * (1 + (T + 7) / 8),  // tickets: all token groups, then one per group
       sizeof(float) * T,            // inv_rms
       sizeof(double) * a.E,         // stat_count (discarded)
       sizeof(double) * a.E,         // stat_wsum (discarded)
@@ -118,8 +118,8 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   a.layer = 0;  // the kernel indexes its statistics by layer; these go to the discarded slots
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // the last-CTA ticket must start at zero; the array keeps whatever the last call left
-  if (cudaMemsetAsync(s.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
+  // the last-CTA tickets must start at zero; the array keeps whatever the last call left
+  if (cudaMemsetAsync(s.ticket, 0, sizes[11], st) != cudaSuccess) {
     cudaGetLastError();
     return report(ctx, PW_ERR_CUDA, "pw_route_noalloc: clearing the ticket failed");
   }
