@@ -104,7 +104,7 @@ _SIGS = {
     "pw_route_noalloc": [_P, _I, _P, _I, _P, _P, _I, _P],
     "pw_set_profiling": [_P, _I],
     "pw_profile_read": [_P, _I, _P],
-    "pw_tc_selftest": [_P, _P, _I, _I, _P, _P, _P],
+    "pw_tc_selftest": [_P, _P, _I, _I, _I, _P, _P, _P],
     "pw_unpack_indices": [_P, _I, _I, _P],
     "pw_dequant": [_P, _I, _I, _P],
     "pw_pack_planes_host": [_P, _I, _I, _I, _P],
@@ -280,8 +280,8 @@ def pw_profile_read(ctx, layer):
     return ms
 
 
-def pw_tc_selftest(A, B, N, K, D, err, stream=None):
-    _check(lib().pw_tc_selftest(_ptr(A), _ptr(B), N, K, _ptr(D), _ptr(err), _stream(stream)))
+def pw_tc_selftest(A, B, N, K, D, err, stream=None, a_in_tmem=False):
+    _check(lib().pw_tc_selftest(_ptr(A), _ptr(B), N, K, 1 if a_in_tmem else 0, _ptr(D), _ptr(err), _stream(stream)))
 
 
 def pw_unpack_indices(ctx, block, b, N, K):

@@ -1,0 +1,150 @@
+// pw_dq.cuh -- from a row's bit-plane words to fp16 centroids (PagedWeight Sec. 3.1 weight
+// pages: Any-Precision bit-planes, plane 0 the most significant, with a per-row LUT for each
+// supported bitwidth).  Used by the expert kernels and by the read-back kernels, so that the
+// read-back checks the very code the forward runs.
+//
+// Input: the Q words W[p] (plane p) of one row and one 32-column group, in the nibble-major
+// bit order of the plane tiling (bit 4 i + j holds column 8 j + i).  Output: 16 registers
+// v[t], t = 0..15, each the fp16 centroids of columns 2t (low half) and 2t + 1 (high half).
+//   Q <= 4: a 4x4 bit transpose across the planes gives word j = the 4-bit codes of columns
+//           8j..8j+7 (column 8j + i in nibble i).  The row's LUT sits in registers as the
+//           low bytes and the high bytes of its centroids; byte permutes (prmt) look up four
+//           codes at a time and interleave the bytes into fp16 pairs.
+//   Q >= 5: an 8x8 bit transpose gives word s, byte e = the code (MSB-aligned) of column
+//           8 (s & 3) + 2e + (s >> 2).  One byte permute turns a code into the shared-memory
+//           address of its centroid in the row's LUT, and a 16-bit shared load fetches it.
+#pragma once
+#include <stdint.h>
+
+#include "pw_device.cuh"
+
+namespace pw {
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// 4x4 bit transpose inside every nibble column of four words:
+// out word s, bit (4i + p) = in word p, bit (4i + s).
+__device__ __forceinline__ void transpose4(uint32_t (&X)[4]) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t t = ((X[j] >> 2) ^ X[j + 2]) & 0x33333333u;
+    X[j + 2] ^= t;
+    X[j] ^= t << 2;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; j += 2) {
+    const uint32_t t = ((X[j] >> 1) ^ X[j + 1]) & 0x55555555u;
+    X[j + 1] ^= t;
+    X[j] ^= t << 1;
+  }
+}
+
+// A LUT of up to 16 centroids as byte planes: lo[m] byte b = low byte of entry 4m + b,
+// hi[m] likewise for the high bytes.
+struct LutRegs {
+  uint32_t lo[4], hi[4];
+};
+// From the entries as fp16 pairs P[i] = entry 2i | entry 2i+1 << 16 (unused entries zero).
+__device__ __forceinline__ void lut_regs(const uint32_t (&P)[8], LutRegs &L) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    L.lo[m] = prmt(P[2 * m], P[2 * m + 1], 0x6420);
+    L.hi[m] = prmt(P[2 * m], P[2 * m + 1], 0x7531);
+  }
+}
+
+// Q <= 4: codes of the 32 columns, word j = columns 8j..8j+7 (nibble i = column 8j + i).
+template <int Q>
+__device__ __forceinline__ void codes_nib(const uint32_t (&W)[8], uint32_t (&S)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) S[i] = 0u;
+#pragma unroll
+  for (int p = 0; p < Q; ++p) S[Q - 1 - p] = W[p];
+  transpose4(S);
+}
+
+// Q <= 4: centroids of four codes (the low 16 bits of s hold them, one per nibble), as the
+// low bytes and the high bytes of the four results.
+template <int Q>
+__device__ __forceinline__ void lut4(uint32_t s, const LutRegs &L, uint32_t &lo, uint32_t &hi) {
+  if constexpr (Q <= 3) {
+    lo = prmt(L.lo[0], L.lo[1], s);
+    hi = prmt(L.hi[0], L.hi[1], s);
+  } else {
+    // prmt reads nibble bit 3 as a sign-replicate flag: look up with bits 0..2 in both
+    // halves of the table, then pick per byte by bit 3
+    const uint32_t s7 = s & 0x7777u;
+    const uint32_t sel = ((s >> 1) & 0x4444u) | 0x3210u;
+    lo = prmt(prmt(L.lo[0], L.lo[1], s7), prmt(L.lo[2], L.lo[3], s7), sel);
+    hi = prmt(prmt(L.hi[0], L.hi[1], s7), prmt(L.hi[2], L.hi[3], s7), sel);
+  }
+}
+
+template <int Q>
+__device__ __forceinline__ void dq_nib(const uint32_t (&S)[4], const LutRegs &L, uint32_t (&v)[16]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t lo, hi;
+      lut4<Q>(h ? (S[j] >> 16) : S[j], L, lo, hi);
+      v[4 * j + 2 * h] = prmt(lo, hi, 0x5140);
+      v[4 * j + 2 * h + 1] = prmt(lo, hi, 0x7362);
+    }
+  }
+}
+
+// Q >= 5 (any Q works): codes of the 32 columns, word s byte e = code of column
+// 8 (s & 3) + 2e + (s >> 2), plane 0 in bit 7.
+template <int Q>
+__device__ __forceinline__ void codes_byte(const uint32_t (&W)[8], uint32_t (&Y)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) Y[i] = 0u;
+#pragma unroll
+  for (int p = 0; p < Q; ++p) Y[7 - p] = W[p];
+  transpose8(Y);
+}
+
+// Q >= 5: centroids from the row's LUT in shared memory at row_addr (aligned to 2^(Q+1)
+// bytes; the table region is aligned to 512 bytes).
+template <int Q>
+__device__ __forceinline__ void dq_byte(const uint32_t (&Y)[8], uint32_t row_addr, uint32_t (&v)[16]) {
+  if constexpr (Q <= 7) {
+    // byte e of Z = (code << 1) | the row's low address byte; its permute with the row
+    // address's upper bytes is the entry's address
+    const uint32_t rlo = (row_addr & 0xFFu) * 0x01010101u;
+    uint32_t Z[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) Z[s] = (Y[s] >> (7 - Q)) | rlo;
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[4 * s + e] = lds_pair(prmt(Z[s], row_addr, 0x7650u | e), prmt(Z[s + 4], row_addr, 0x7650u | e));
+  } else {
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        v[4 * s + e] = lds_pair(row_addr + (prmt(Y[s], 0u, 0x4440u + e) << 1),
+                                row_addr + (prmt(Y[s + 4], 0u, 0x4440u + e) << 1));
+  }
+}
+
+// code of column c (0..31) of the group, from the outputs of codes_nib / codes_byte
+template <int Q>
+__device__ __forceinline__ uint32_t code_nib(const uint32_t (&S)[4], int c) {
+  return (S[c >> 3] >> (4 * (c & 7))) & 0xFu;
+}
+template <int Q>
+__device__ __forceinline__ uint32_t code_byte(const uint32_t (&Y)[8], int c) {
+  const int j = c >> 3, i = c & 7;  // column 8j + i = 8 (s & 3) + 2e + (s >> 2)
+  const int s = j + 4 * (i & 1), e = i >> 1;
+  return ((Y[s] >> (8 * e)) & 0xFFu) >> (8 - Q);
+}
+
+}  // namespace pw

@@ -7,19 +7,24 @@
 // The shared expert of the layer (Table 1) rides in the same launches.
 //
 // A work item is a 128-row tile of one block times up to 64 tokens: D[128][N] = W x X^T,
-// N = tokens padded to 16.  One persistent CTA per SM, warp-specialised:
-//   * plane producer (1 warp): LUT_q rows of the tile (one TMA bulk copy per item) and, per
-//     128-column chunk, the q bit-planes (one bulk copy per plane) into a 4-deep ring;
-//   * A/B producer (1 warp): the tokens' fp16 activation rows (16-byte cp.async gathers) into
-//     the B operand tile and, for the dense shared expert, its fp16 weight tile (one bulk
-//     copy) into the A operand tile, in a 2-deep ring;
-//   * dequantising warps (16): an 8x8 bit transpose turns a row's plane words into codes of
-//     32 consecutive columns, the codes index LUT_q in shared memory, and the fp16 centroids
-//     are stored into the A operand tile (core-matrix layout, 128-bit stores);
-//   * MMA warp (1 thread): eight tcgen05.mma (M=128, N, K=16) per chunk, accumulator in
-//     tensor memory (two buffers), completion signalled to mbarriers by tcgen05.commit;
-//   * the first 8 dequantising warps read the accumulator (tcgen05.ld) and write h = silu(g)*u
-//     or the down output.
+// N = tokens padded to 16, accumulated in tensor memory.  One persistent CTA per SM, warp-
+// specialised:
+//   * plane producer (1 warp): the tile's LUT_q rows (one TMA bulk copy per item, into one
+//     of two LUT slots so that the next item's table loads while this one runs; a q = 8
+//     table takes both) and, per 128-column chunk, the q bit-plane slabs (one bulk copy per
+//     plane) into a 4-deep ring;
+//   * activation producer (1 warp): the tokens' fp16 rows (16-byte cp.async gathers) into the
+//     B operand tile and, for the dense shared expert, its fp16 weight tile (one bulk copy)
+//     into the A operand tile, in a 2-deep shared-memory ring;
+//   * dequantising warps (16, four per tensor-memory lane quarter): each thread owns one row
+//     and 32 columns of the chunk, turns its plane words into fp16 centroids (pw_dq.cuh) and
+//     writes them straight into tensor memory (tcgen05.st), a 4-deep ring of A buffers;
+//   * MMA thread (1 warp): per chunk eight tcgen05.mma (M = 128, N, K = 16) with A read from
+//     tensor memory (routed blocks) or from shared memory (shared expert), B from shared
+//     memory, the accumulator in one of two tensor-memory buffers; completions reach the
+//     mbarriers through tcgen05.commit;
+//   * epilogue (4 warps, one per lane quarter): tcgen05.ld of the accumulator, then
+//     h = silu(g) * u (gate_up) or the down output, while the next item is being computed.
 // Every mbarrier wait is bounded: on expiry the kernel records an error (PW_ERR_TIMEOUT on
 // the host), every role stops, the producers and the MMA thread wait (bounded) for what they
 // issued, and tensor memory is freed before the kernel returns.
@@ -27,46 +32,53 @@
 #include <stdint.h>
 
 #include "pw_device.cuh"
+#include "pw_dq.cuh"
 #include "pw_internal.h"
 #include "pw_tc.cuh"
 
 namespace pw {
 
-constexpr int kDq = 16;                     // dequantising warps
-constexpr int kWarpP = kDq;                 // plane producer
-constexpr int kWarpAB = kDq + 1;            // activation / dense-weight producer
-constexpr int kWarpMma = kDq + 2;           // MMA issuer, tensor-memory owner
-constexpr int kTcThreads = (kDq + 3) * 32;
-constexpr int kEpiWarps = 8;                // warps that read the accumulator
+constexpr int kDq = 16;                     // dequantising warps 0..15
+constexpr int kEpi = 4;                     // epilogue warps 16..19
+constexpr int kWarpP = kDq + kEpi;          // plane producer
+constexpr int kWarpAB = kWarpP + 1;         // activation / dense-weight producer
+constexpr int kWarpMma = kWarpP + 2;        // MMA issuer, tensor-memory owner
+constexpr int kTcThreads = (kWarpMma + 1) * 32;
 constexpr int kPStages = 4;                 // plane ring depth
-constexpr int kPStageBytes = kMaxPlanes * kWarpsPerCta * 256;  // 16 KB
-constexpr int kPlaneBytes = kWarpsPerCta * 256;                // one plane of a stage
-constexpr int kATileBytes = kCtaRows * kChunkCols * 2;         // 32 KB
-constexpr int kLutBytes = kCtaRows * 256 * 2;                  // LUT_8 of 128 rows
+constexpr int kPlaneBytes = kCtaRows * 16;  // one plane slab of a 128-row tile and 128 columns
+constexpr int kPStageBytes = kMaxPlanes * kPlaneBytes;  // 16 KB
+constexpr int kAStages = 4;                 // tensor-memory A buffers
+constexpr int kABStages = 2;                // shared-memory operand ring
+constexpr int kATileBytes = kCtaRows * kChunkCols * 2;  // 32 KB dense A tile
+constexpr int kLutSlot = 32 * 1024;         // LUT slot (q <= 7); q = 8 takes both slots
 constexpr int kAccCols = 64;                // tensor-memory columns per accumulator buffer
-constexpr uint32_t kTmemCols = 2 * kAccCols;
+constexpr int kACols = kChunkCols / 2;      // tensor-memory columns per A buffer (fp16 pairs)
+constexpr uint32_t kAColBase = 2 * kAccCols;
+constexpr uint32_t kTmemCols = 512;
 constexpr long kSpinLimit = 1L << 22;
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
 struct TcLayout {
   int npad_max;    // B tile rows (tokens padded to 16)
-  int ab_bytes;    // one A/B stage: A tile then B tile
-  int ab_off;      // offset of the A/B ring
+  int ab_bytes;    // one operand stage: dense A tile then B tile
+  int ab_off;      // offset of the operand ring
   int lut_off;     // LUT region (+512 bytes for alignment)
   int bar_off;     // mbarriers
   int smem;        // total dynamic shared memory
 };
 
 // mbarrier indices
-enum { kPF = 0, kPE = kPF + kPStages, kABF = kPE + kPStages, kABE = kABF + 2, kLF = kABE + 2, kLE = kLF + 1,
-       kAF = kLE + 1, kAE = kAF + 2, kDrain = kAE + 2, kNumBars = kDrain + 1 };
+enum {
+  kPF = 0, kPE = kPF + kPStages, kTAF = kPE + kPStages, kTAE = kTAF + kAStages, kBF = kTAE + kAStages,
+  kBE = kBF + kABStages, kLF = kBE + kABStages, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
+  kNumBars = kDrain + 1
+};
 
 struct ItemView {
   bool routed;
   int q;         // routed: committed bitwidth
-  int nwt;       // warp tiles in this CTA tile
-  int NT;        // warp tiles of the block
-  int KC;        // routed: 128-column chunks of the planes
+  int nr;        // rows of this CTA tile
+  int KC;        // 128-column chunks of the K dimension
   int Kc;        // activation columns
   int N;         // rows of the block
   int ntok, npad;
@@ -99,8 +111,7 @@ __device__ __forceinline__ ItemView view_item(const FwdArgs &a, const WorkItem &
     v.row0 = w.tok0;
     v.W = (PHASE == 1) ? a.lay.wgu : a.lay.wd;
   }
-  v.NT = v.N / 16;
-  v.nwt = cta_warps(w.tile, v.NT);
+  v.nr = tile_rows(w.tile, v.N);
   return v;
 }
 
@@ -118,6 +129,19 @@ __device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const TcLayout &
   return (smem_u32(sm) + L.lut_off + 511u) & ~511u;
 }
 
+// LUT slot schedule, replayed identically by the plane producer and the dequantising warps:
+// tables of q <= 7 alternate between the two slots; a q = 8 table (64 KB) takes both.
+struct LutSched {
+  uint32_t fills[2] = {0u, 0u}, uses[2] = {0u, 0u};
+  int last = 1;
+  __device__ __forceinline__ int next(int q, bool &both) {
+    both = q > 7;
+    const int slot = both ? 0 : (last ^ 1);
+    last = both ? 1 : slot;
+    return slot;
+  }
+};
+
 // Bounded wait on an mbarrier phase; false on expiry or when another warp gave up.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
   for (long i = 0; i < kSpinLimit; ++i) {
@@ -134,47 +158,15 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
-
-// Shared-memory address of LUT entry `code` of a row whose table starts at a base aligned to
-// 2^(Q+1) bytes; Y holds MSB-aligned codes in its bytes and E selects the byte.
-template <int Q, int E>
-__device__ __forceinline__ uint32_t lut_addr(uint32_t Y, uint32_t base) {
-  constexpr int sh = 8 * E + 7 - Q;
-  constexpr uint32_t m = ((1u << Q) - 1u) << 1;
-  const uint32_t v = sh >= 0 ? (Y >> (sh >= 0 ? sh : 0)) : (Y << (sh < 0 ? -sh : 0));
-  return (v & m) | base;
-}
-// fp16 centroids of the codes in bytes E and E+1 of Y, packed low-first.
-template <int Q, int E>
-__device__ __forceinline__ uint32_t lut_pair(uint32_t Y, uint32_t base) {
-  return lds_pair(lut_addr<Q, E>(Y, base), lut_addr<Q, E + 1>(Y, base));
-}
-
-// Dequantise 32 consecutive columns of one row (the thread's plane words) into the A tile.
-template <int Q>
-__device__ __forceinline__ void dq_chunk(const uint8_t *pslot, uint32_t a_tile, uint32_t lut0, int tw, int half,
-                                         int lane) {
-  uint32_t Y[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) Y[i] = 0u;
-#pragma unroll
-  for (int p = 0; p < Q; ++p)
-    Y[7 - p] = *reinterpret_cast<const uint32_t *>(pslot + p * kPlaneBytes + tw * 256 + (lane * 2 + half) * 4);
-  transpose8(Y);
-  const int row = tw * 16 + half * 8 + (lane & 7);
-  const uint32_t lb = lut0 + ((uint32_t)row << (Q + 1));
-  const uint32_t dst = a_tile + (uint32_t)core_offset128(row, (lane >> 3) * 32);
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const uint32_t r0 = lut_pair<Q, 0>(Y[2 * m], lb);
-    const uint32_t r1 = lut_pair<Q, 2>(Y[2 * m], lb);
-    const uint32_t r2 = lut_pair<Q, 0>(Y[2 * m + 1], lb);
-    const uint32_t r3 = lut_pair<Q, 2>(Y[2 * m + 1], lb);
-    sts128(dst + m * 128, r0, r1, r2, r3);
-  }
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
@@ -191,27 +183,34 @@ __device__ void plane_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm,
   if ((threadIdx.x & 31) != 0) return;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  uint32_t p_seq = 0, lut_seq = 0;
+  const uint32_t lut0 = lut_base(sm, L);
+  uint32_t p_seq = 0;
+  LutSched ls;
   bool ok = true;
   for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
     if (!v.routed) continue;
-    const int rt0 = w.tile * kWarpsPerCta;
-    ok = wait_bar(bars + 8 * kLE, (lut_seq & 1) ^ 1, abort_flag, a.s.err);
+    bool both;
+    const int slot = ls.next(v.q, both);
+    ok = wait_bar(bars + 8 * (kLE + slot), (ls.uses[slot] & 1) ^ 1, abort_flag, a.s.err);
+    if (ok && both) ok = wait_bar(bars + 8 * (kLE + 1), (ls.uses[1] & 1) ^ 1, abort_flag, a.s.err);
     if (!ok) break;
-    const uint32_t lbytes = (uint32_t)(v.nwt * 16) << v.q << 1;
-    mbar_arrive_expect_tx(bars + 8 * kLF, lbytes);
-    bulk_g2s(lut_base(sm, L), v.bd->lut[v.q] + ((size_t)rt0 * 16 << v.q), lbytes, bars + 8 * kLF);
-    ++lut_seq;
+    ++ls.uses[slot];
+    if (both) ++ls.uses[1];
+    const uint32_t lbytes = (uint32_t)v.nr << v.q << 1;
+    mbar_arrive_expect_tx(bars + 8 * (kLF + slot), lbytes);
+    bulk_g2s(lut0 + slot * kLutSlot, v.bd->lut[v.q] + ((size_t)w.tile * kCtaRows << v.q), lbytes,
+             bars + 8 * (kLF + slot));
+    ++ls.fills[slot];
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
       const int ps = p_seq % kPStages;
       ok = wait_bar(bars + 8 * (kPE + ps), ((p_seq / kPStages) & 1) ^ 1, abort_flag, a.s.err);
       if (!ok) break;
-      const uint32_t bytes = (uint32_t)v.nwt * 256;
+      const uint32_t bytes = (uint32_t)v.nr * 16;
       const uint32_t full = bars + 8 * (kPF + ps);
       mbar_arrive_expect_tx(full, bytes * v.q);
-      const long off = plane_pair_word(rt0, kc, v.NT, v.KC);
+      const long off = slab_word(w.tile, kc, v.N, v.KC);
       const uint32_t dst = smem_u32(sm) + ps * kPStageBytes;
       for (int p = 0; p < v.q; ++p) bulk_g2s(dst + p * kPlaneBytes, v.bd->plane[p] + off, bytes, full);
       ++p_seq;
@@ -222,7 +221,8 @@ __device__ void plane_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm,
     const uint32_t q = p_seq - 1 - k;
     drain_bar(bars + 8 * (kPF + q % kPStages), (q / kPStages) & 1);
   }
-  if (lut_seq > 0) drain_bar(bars + 8 * kLF, (lut_seq - 1) & 1);
+  for (int s = 0; s < 2; ++s)
+    if (ls.fills[s] > 0) drain_bar(bars + 8 * (kLF + s), (ls.fills[s] - 1) & 1);
 }
 
 template <int PHASE>
@@ -239,11 +239,11 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     const uint16_t *rb0 = lane < v.ntok ? act_row<PHASE>(a, v, lane) : nullptr;
     const uint16_t *rb1 = lane + 32 < v.ntok ? act_row<PHASE>(a, v, lane + 32) : nullptr;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int as = ab_seq % 2;
-      if (lane == 0) ok = wait_bar(bars + 8 * (kABE + as), ((ab_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
+      const int as = ab_seq % kABStages;
+      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + as), ((ab_seq / kABStages) & 1) ^ 1, abort_flag, a.s.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const uint32_t full = bars + 8 * (kABF + as);
+      const uint32_t full = bars + 8 * (kBF + as);
       const uint32_t a_tile = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
       const uint32_t b_tile = a_tile + kATileBytes;
       if (lane == 0) {
@@ -272,9 +272,9 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     }
   }
   if (lane == 0)
-    for (uint32_t k = 0; k < 2 && k < ab_seq; ++k) {
+    for (uint32_t k = 0; k < (uint32_t)kABStages && k < ab_seq; ++k) {
       const uint32_t q = ab_seq - 1 - k;
-      drain_bar(bars + 8 * (kABF + q % 2), (q / 2) & 1);
+      drain_bar(bars + 8 * (kBF + q % kABStages), (q / kABStages) & 1);
     }
 }
 
@@ -284,7 +284,7 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
   if ((threadIdx.x & 31) != 0) return;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  uint32_t ab_seq = 0, item_seq = 0;
+  uint32_t ab_seq = 0, a_seq = 0, item_seq = 0;
   bool ok = true;
   for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
     const WorkItem w = items[it];
@@ -297,23 +297,34 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
     const uint32_t d = tmem + acs * kAccCols;
     bool first = true;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int as = ab_seq % 2;
-      ok = wait_bar(bars + 8 * (kABF + as), (ab_seq / 2) & 1, abort_flag, a.s.err);
+      const int as = ab_seq % kABStages, ts = a_seq % kAStages;
+      if (v.routed) {
+        ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / kAStages) & 1, abort_flag, a.s.err);
+        if (!ok) break;
+      }
+      ok = wait_bar(bars + 8 * (kBF + as), (ab_seq / kABStages) & 1, abort_flag, a.s.err);
       if (!ok) break;
-      // the B rows (and routed A) were written through the generic proxy; the MMAs read
-      // them through the async proxy
+      // the B rows were written through the generic proxy; the MMAs read them through the
+      // async proxy
       fence_async_smem();
       tc_fence_after();
       const uint32_t a0 = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
       const uint32_t b0 = a0 + kATileBytes;
+      if (v.routed) {
+        const uint32_t at = tmem + kAColBase + ts * kACols;
 #pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const uint64_t ad = smem_desc(a0 + 256 * t, 128, 16 * 128);
-        const uint64_t bd = smem_desc(b0 + 256 * t, 128, 16 * 128);
-        tc_mma_f16(d, ad, bd, idesc, (first && t == 0) ? 0u : 1u);
+        for (int t = 0; t < 8; ++t)
+          tc_mma_f16_ta(d, at + 8 * t, smem_desc(b0 + 256 * t, 128, 16 * 128), idesc, (first && t == 0) ? 0u : 1u);
+        tc_commit(bars + 8 * (kTAE + ts));
+        ++a_seq;
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          tc_mma_f16(d, smem_desc(a0 + 256 * t, 128, 16 * 128), smem_desc(b0 + 256 * t, 128, 16 * 128), idesc,
+                     (first && t == 0) ? 0u : 1u);
       }
       first = false;
-      tc_commit(bars + 8 * (kABE + as));
+      tc_commit(bars + 8 * (kBE + as));
       ++ab_seq;
     }
     if (!ok) break;
@@ -325,95 +336,162 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
   drain_bar(bars + 8 * kDrain, 0);
 }
 
+// One routed item for a dequantising thread: row r of the tile, columns [32 cg, 32 cg + 32)
+// of every chunk.
+template <int PHASE, int Q>
+__device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, uint32_t bars,
+                        uint32_t tmem, uint32_t lut_slot, int quarter, int cg, uint32_t &p_seq, uint32_t &a_seq,
+                        volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int r = 32 * quarter + lane;
+  const bool rv = r < v.nr;
+  LutRegs Lr;
+  uint32_t row_addr = 0;
+  if constexpr (Q <= 4) {
+    uint32_t P[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) P[i] = 0u;
+    if (rv) {
+      const uint32_t la = lut_slot + ((uint32_t)r << (Q + 1));
+      if constexpr (Q == 4) {
+        const uint4 x0 = lds128(la), x1 = lds128(la + 16);
+        P[0] = x0.x; P[1] = x0.y; P[2] = x0.z; P[3] = x0.w;
+        P[4] = x1.x; P[5] = x1.y; P[6] = x1.z; P[7] = x1.w;
+      } else if constexpr (Q == 3) {
+        const uint4 x0 = lds128(la);
+        P[0] = x0.x; P[1] = x0.y; P[2] = x0.z; P[3] = x0.w;
+      } else if constexpr (Q == 2) {
+        P[0] = lds32(la);
+        P[1] = lds32(la + 4);
+      } else {
+        P[0] = lds32(la);
+      }
+    }
+    lut_regs(P, Lr);
+  } else {
+    row_addr = lut_slot + ((uint32_t)r << (Q + 1));
+  }
+  const uint32_t word_off = (uint32_t)(cg * v.nr + r) * 4;
+  const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+  for (int kc = w.kc0; kc < w.kc1; ++kc) {
+    const int ps = p_seq % kPStages, ts = a_seq % kAStages;
+    if (!wait_bar(bars + 8 * (kPF + ps), (p_seq / kPStages) & 1, abort_flag, a.s.err)) return false;
+    const uint32_t stage = smem_u32(sm) + ps * kPStageBytes + word_off;
+    uint32_t W[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) W[p] = (p < Q && rv) ? lds32(stage + p * kPlaneBytes) : 0u;
+    uint32_t v16[16];
+    if constexpr (Q <= 4) {
+      uint32_t S[4];
+      codes_nib<Q>(W, S);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (kPE + ps));  // the slab words are in registers
+      dq_nib<Q>(S, Lr, v16);
+    } else {
+      uint32_t Y[8];
+      codes_byte<Q>(W, Y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (kPE + ps));
+      dq_byte<Q>(Y, row_addr, v16);
+    }
+    ++p_seq;
+    if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
+    tc_fence_after();
+    tmem_st16(tmem + lane_base + kAColBase + ts * kACols + 16 * cg, v16);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kTAF + ts));
+    ++a_seq;
+  }
+  return true;
+}
+
 template <int PHASE>
-__device__ void dequant_and_epilogue(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
-                                     volatile int *abort_flag) {
+__device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
+                            volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tw = warp % kWarpsPerCta, half = warp / kWarpsPerCta;
+  const int quarter = warp & 3, cg = warp >> 2;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t lut0 = lut_base(sm, L);
-  uint32_t p_seq = 0, ab_seq = 0, lut_seq = 0, item_seq = 0;
+  uint32_t p_seq = 0, a_seq = 0;
+  LutSched ls;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
-    const bool active = tw < v.nwt;
-    if (v.routed && !wait_bar(bars + 8 * kLF, lut_seq & 1, abort_flag, a.s.err)) return;
-    for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int as = ab_seq % 2;
-      if (!wait_bar(bars + 8 * (kABE + as), ((ab_seq / 2) & 1) ^ 1, abort_flag, a.s.err)) return;
-      if (v.routed) {
-        const int ps = p_seq % kPStages;
-        if (!wait_bar(bars + 8 * (kPF + ps), (p_seq / kPStages) & 1, abort_flag, a.s.err)) return;
-        if (active) {
-          const uint8_t *pslot = sm + ps * kPStageBytes;
-          const uint32_t a_tile = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
-          switch (v.q) {
-            case 1: dq_chunk<1>(pslot, a_tile, lut0, tw, half, lane); break;
-            case 2: dq_chunk<2>(pslot, a_tile, lut0, tw, half, lane); break;
-            case 3: dq_chunk<3>(pslot, a_tile, lut0, tw, half, lane); break;
-            case 4: dq_chunk<4>(pslot, a_tile, lut0, tw, half, lane); break;
-            case 5: dq_chunk<5>(pslot, a_tile, lut0, tw, half, lane); break;
-            case 6: dq_chunk<6>(pslot, a_tile, lut0, tw, half, lane); break;
-            case 7: dq_chunk<7>(pslot, a_tile, lut0, tw, half, lane); break;
-            default: dq_chunk<8>(pslot, a_tile, lut0, tw, half, lane); break;
-          }
-          fence_async_smem();
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (kPE + ps));
-        ++p_seq;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kABF + as));
-      ++ab_seq;
+    if (!v.routed) continue;
+    bool both;
+    const int slot = ls.next(v.q, both);
+    if (!wait_bar(bars + 8 * (kLF + slot), ls.fills[slot] & 1, abort_flag, a.s.err)) return;
+    ++ls.fills[slot];
+    const uint32_t lut_slot = lut0 + slot * kLutSlot;
+    bool ok;
+    switch (v.q) {
+      case 1: ok = dq_item<PHASE, 1>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      case 2: ok = dq_item<PHASE, 2>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      case 3: ok = dq_item<PHASE, 3>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      case 4: ok = dq_item<PHASE, 4>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      case 5: ok = dq_item<PHASE, 5>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      case 6: ok = dq_item<PHASE, 6>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      case 7: ok = dq_item<PHASE, 7>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+      default: ok = dq_item<PHASE, 8>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
     }
-    if (v.routed) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * kLE);
-      ++lut_seq;
+    if (!ok) return;
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(bars + 8 * (kLE + slot));
+      if (both) mbar_arrive(bars + 8 * (kLE + 1));
     }
-    // epilogue: the accumulator of this item (tensor-memory lanes = tile rows, columns = tokens)
-    if (warp < kEpiWarps) {
-      const int acs = item_seq % 2;
-      if (!wait_bar(bars + 8 * (kAF + acs), (item_seq / 2) & 1, abort_flag, a.s.err)) return;
-      tc_fence_after();
-      const int quarter = warp % 4, colhalf = warp / 4;
-      const int ncols = v.npad / 2, col0 = colhalf * ncols;
-      const int row = 32 * quarter + lane;  // tile row
-      const int R = w.tile * kCtaRows + row;
-      const bool empty = w.kc1 <= w.kc0;     // nothing accumulated (an empty split part)
-      const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * kAccCols;
-      for (int c = 0; c < ncols; c += 8) {
-        uint32_t r[8];
-        tmem_ld8(taddr + col0 + c, r);
-        tmem_wait_ld();
+  }
+}
+
+template <int PHASE>
+__device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, volatile int *abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int n_items = a.s.n_items[PHASE - 1];
+  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  uint32_t item_seq = 0;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const WorkItem w = items[it];
+    const ItemView v = view_item<PHASE>(a, w);
+    const int acs = item_seq % 2;
+    if (!wait_bar(bars + 8 * (kAF + acs), (item_seq / 2) & 1, abort_flag, a.s.err)) return;
+    tc_fence_after();
+    const int row = 32 * quarter + lane;  // tile row = tensor-memory lane
+    const int R = w.tile * kCtaRows + row;
+    const bool empty = w.kc1 <= w.kc0;     // nothing accumulated (an empty split part)
+    const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * kAccCols;
+    for (int c = 0; c < v.npad; c += 8) {
+      uint32_t r8[8];
+      tmem_ld8(taddr + c, r8);
+      tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float acc = empty ? 0.f : __uint_as_float(r[i]);
-          const int j = col0 + c + i;
-          if (PHASE == 1) {
-            const float up = __shfl_down_sync(0xffffffffu, acc, 8);
-            if ((row & 15) < 8 && R < v.N && j < v.ntok) {
-              const int f = R / 16 * 8 + (R & 7);
-              const uint16_t hv = f2h(silu(acc) * up);
-              if (v.routed)
-                a.s.h_routed[(size_t)(v.row0 + j) * a.I + f] = hv;
-              else
-                a.s.h_shared[(size_t)(v.row0 + j) * a.Is + f] = hv;
-            }
-          } else if (R < v.N && j < v.ntok) {
+      for (int i = 0; i < 8; ++i) {
+        const float acc = empty ? 0.f : __uint_as_float(r8[i]);
+        const int j = c + i;
+        if (PHASE == 1) {
+          const float up = __shfl_down_sync(0xffffffffu, acc, 8);
+          if ((row & 15) < 8 && R < v.N && j < v.ntok) {
+            const int f = R / 16 * 8 + (R & 7);
+            const uint16_t hv = f2h(silu(acc) * up);
             if (v.routed)
-              a.s.o_routed[(size_t)(v.row0 + j) * a.H + R] = acc;
+              a.s.h_routed[(size_t)(v.row0 + j) * a.I + f] = hv;
             else
-              a.s.o_shared[((size_t)w.part * a.T + v.row0 + j) * a.H + R] = acc;
+              a.s.h_shared[(size_t)(v.row0 + j) * a.Is + f] = hv;
           }
+        } else if (R < v.N && j < v.ntok) {
+          if (v.routed)
+            a.s.o_routed[(size_t)(v.row0 + j) * a.H + R] = acc;
+          else
+            a.s.o_shared[((size_t)w.part * a.T + v.row0 + j) * a.H + R] = acc;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kAE + acs));
     }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kAE + acs));
     ++item_seq;
   }
 }
@@ -430,14 +508,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kPF + i), 1);
       mbar_init(bars + 8 * (kPE + i), kDq);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bars + 8 * (kABF + i), 32 + 1 + kDq);  // cp.async lanes, producer lane 0, dequantisers
-      mbar_init(bars + 8 * (kABE + i), 1);
-      mbar_init(bars + 8 * (kAF + i), 1);
-      mbar_init(bars + 8 * (kAE + i), kEpiWarps);
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(bars + 8 * (kTAF + i), kDq);
+      mbar_init(bars + 8 * (kTAE + i), 1);
     }
-    mbar_init(bars + 8 * kLF, 1);
-    mbar_init(bars + 8 * kLE, kDq);
+    for (int i = 0; i < kABStages; ++i) {
+      mbar_init(bars + 8 * (kBF + i), 32 + 1);  // cp.async lanes, producer lane 0
+      mbar_init(bars + 8 * (kBE + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars + 8 * (kLF + i), 1);
+      mbar_init(bars + 8 * (kLE + i), kDq);
+      mbar_init(bars + 8 * (kAF + i), 1);
+      mbar_init(bars + 8 * (kAE + i), kEpi);
+    }
     mbar_init(bars + 8 * kDrain, 1);
     abort_flag = 0;
     fence_mbar_init();
@@ -451,7 +535,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   if (warp < kDq)
-    dequant_and_epilogue<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+    dequantiser<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+  else if (warp < kWarpP)
+    epilogue<PHASE>(a, bars, tmem, &abort_flag);
   else if (warp == kWarpP)
     plane_producer<PHASE>(a, L, sm, bars, &abort_flag);
   else if (warp == kWarpAB)
@@ -471,8 +557,8 @@ static TcLayout tc_layout(const FwdArgs &a) {
   L.npad_max = max(16, (min(a.T, kTokChunk) + 15) / 16 * 16);
   L.ab_bytes = kATileBytes + L.npad_max * kChunkCols * 2;
   L.ab_off = kPStages * kPStageBytes;
-  L.lut_off = L.ab_off + 2 * L.ab_bytes;
-  L.bar_off = L.lut_off + kLutBytes + 512;
+  L.lut_off = L.ab_off + kABStages * L.ab_bytes;
+  L.bar_off = L.lut_off + 2 * kLutSlot + 512;
   L.smem = L.bar_off + kNumBars * 8;
   return L;
 }
@@ -480,12 +566,8 @@ static TcLayout tc_layout(const FwdArgs &a) {
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
   const TcLayout L = tc_layout(a);
   if (L.smem > kSmemLimit) return (int)cudaErrorInvalidConfiguration;
-  static int attr_done = 0;
-  if (!attr_done) {
-    cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    attr_done = 1;
-  }
+  cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
   const int grid = min(max_items, a.sm_count);

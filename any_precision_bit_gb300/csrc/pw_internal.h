@@ -1,18 +1,16 @@
 // pw_internal.h -- structures and index maps shared by the host runtime and the kernels.
 //
 // Kernel-private plane tiling (the ABI layout is restored by pw_unpack_indices):
-//   A block's rows are grouped in 16-row warp tiles.  For a gate_up block a warp tile holds
-//   8 gate rows followed by the 8 up rows of the same 8 features, so that one warp's MMA
-//   tile yields gate and up of a feature in the same thread.  Columns are grouped in chunks
-//   of 128 (the plane row is zero-padded to a multiple of 128 bits).  Warp tiles are grouped
-//   by 8 into CTA tiles of 128 rows (the last CTA tile may hold fewer).  Within a CTA tile
-//   the data of one plane is ordered [chunk][warp tile][64 words], so one 128-column stage
-//   of a CTA tile is a single contiguous run of (warp tiles x 256) bytes per plane.
-//   Word (lane * 2 + r) of a (chunk, warp tile) holds row (8r + lane % 8) of the warp tile
-//   and the 32 columns [32 (lane / 8), 32 (lane / 8) + 32) of the chunk: bit (8e + s) is
-//   column 32 (lane / 8) + 4 s + e.  After an 8x8 bit transpose of a row's plane words, byte
-//   e of word s is the code of column 4 s + e, so one thread turns a word per plane into 32
-//   consecutive dequantised columns of one row.
+//   A block's device rows are grouped in CTA tiles of 128 rows (the last may hold fewer; N is
+//   a multiple of 16).  For a gate_up block each 16-row group holds 8 gate rows followed by
+//   the 8 up rows of the same 8 features, so that gate and up of a feature sit 8 tensor-
+//   memory lanes apart.  Columns are grouped in chunks of 128 (the plane row is zero-padded
+//   to a multiple of 128 bits) and each chunk in 4 column groups of 32.
+//   One plane of one (CTA tile, chunk) is a contiguous slab of nr x 4 words (nr = rows of
+//   the tile), ordered [column group][row]; slabs are ordered [tile][chunk].  Inside a word,
+//   bit (4 i + j) holds column 8 j + i of the 32-column group (i = 0..7, j = 0..3): a 4x4
+//   bit transpose across the planes of a row then yields 4-bit codes of 8 consecutive
+//   columns per word, and an 8x8 transpose yields 8-bit codes of 4 columns per word.
 #pragma once
 #include <stdint.h>
 
@@ -25,10 +23,8 @@
 namespace pw {
 
 constexpr int kMaxPlanes = 8;
-constexpr int kTileRows = 16;     // rows per warp tile
 constexpr int kChunkCols = 128;   // columns per plane chunk (one pipeline stage)
-constexpr int kWarpsPerCta = 8;   // consumer warps (warp tiles) per CTA tile
-constexpr int kCtaRows = kTileRows * kWarpsPerCta;
+constexpr int kCtaRows = 128;     // rows per CTA tile (tensor-memory lanes of one MMA)
 constexpr int kTokChunk = 64;     // tokens per work item in the decode kernels
 
 // One row of the device weight page table (PagedWeight Sec. 3.1).  The kernels read q and
@@ -78,27 +74,21 @@ PW_HD int orig_row(int d, int u, int I) {
   return (ri >= 8) ? I + f : f;
 }
 
-// warp tiles in CTA tile ct of a block with NT warp tiles
-PW_HD int cta_warps(int ct, int NT) {
-  return NT - ct * kWarpsPerCta < kWarpsPerCta ? NT - ct * kWarpsPerCta : kWarpsPerCta;
-}
+// rows of CTA tile ct of a block with N rows
+PW_HD int tile_rows(int ct, int N) { return N - ct * kCtaRows < kCtaRows ? N - ct * kCtaRows : kCtaRows; }
 
-// first word of (warp tile rt, chunk kc) inside a tiled plane; its 64 words follow
-PW_HD long plane_pair_word(int rt, int kc, int NT, int KC) {
-  const int ct = rt / kWarpsPerCta, w = rt % kWarpsPerCta;
-  return ((long)ct * kWarpsPerCta * KC + (long)kc * cta_warps(ct, NT) + w) * 64;
+// first word of the slab of (CTA tile ct, chunk kc) inside a tiled plane; nr x 4 words follow
+PW_HD long slab_word(int ct, int kc, int N, int KC) {
+  return ((long)ct * kCtaRows * KC + (long)kc * tile_rows(ct, N)) * 4;
 }
 
 // word index inside a tiled plane and bit inside that word for (device row d, column k)
 PW_HD void tile_pos(int d, int k, int N, int KC, long *word, int *bit) {
-  const int rt = d / 16, ri = d % 16;
-  const int r = ri / 8, g8 = ri % 8;
-  const int kc = k / 128, kk = k % 128;
-  const int seg = kk / 32, kin = kk % 32;
-  const int s = kin / 4, e = kin % 4;
-  const int lane = seg * 8 + g8;
-  *word = plane_pair_word(rt, kc, N / 16, KC) + lane * 2 + r;
-  *bit = 8 * e + s;
+  const int ct = d / kCtaRows, r = d % kCtaRows;
+  const int kc = k / kChunkCols, kk = k % kChunkCols;
+  const int cg = kk / 32, j = (kk % 32) / 8, i = kk % 8;
+  *word = slab_word(ct, kc, N, KC) + (long)cg * tile_rows(ct, N) + r;
+  *bit = 4 * i + j;
 }
 
 // Operand tiles of the tensor-core MMAs are stored as 8x8 "core matrices" of fp16 (128

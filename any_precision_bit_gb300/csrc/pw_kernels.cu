@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "pw_device.cuh"
+#include "pw_dq.cuh"
 #include "pw_internal.h"
 
 namespace pw {
@@ -107,33 +108,30 @@ int launch_commit(BlockDev *table, int block, const BlockDev &val, void *stream)
   return (int)cudaGetLastError();
 }
 
-// One thread per (warp tile, chunk, lane, row half); writes that word of every plane.
+// One thread per (CTA tile, chunk, column group, row); writes that word of every plane.
 __global__ void pack_kernel(const uint8_t *idx, int N, int K, int KC, int u, int I, int bmax,
                             uint32_t *const *planes, long nwords) {
-  long li = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long li = (long)blockIdx.x * blockDim.x + threadIdx.x;
   if (li >= nwords) return;
-  const int r = (int)(li & 1);
-  const int lane = (int)((li >> 1) & 31);
-  const long tk = li >> 6;
-  const int kc = (int)(tk % KC);
-  const int rt = (int)(tk / KC);
-  const int d = rt * 16 + 8 * r + (lane & 7);
-  const int row = orig_row(d, u, I);
+  const long full = (long)kCtaRows * KC * 4;  // words of a full CTA tile
+  const int ct = (int)(li / full);
+  const int nr = tile_rows(ct, N);
+  const int off = (int)(li - ct * full);
+  const int kc = off / (nr * 4), rem = off % (nr * 4);
+  const int cg = rem / nr, r = rem % nr;
+  const int row = orig_row(ct * kCtaRows + r, u, I);
   uint32_t words[kMaxPlanes] = {0, 0, 0, 0, 0, 0, 0, 0};
-  for (int e = 0; e < 4; ++e) {
-    for (int s = 0; s < 8; ++s) {
-      const int col = kc * 128 + 32 * (lane >> 3) + 4 * s + e;
-      const uint32_t code = (col < K) ? idx[(size_t)row * K + col] : 0u;
-      for (int p = 0; p < bmax; ++p) words[p] |= ((code >> (bmax - 1 - p)) & 1u) << (8 * e + s);
-    }
+  for (int b = 0; b < 32; ++b) {
+    const int col = kc * kChunkCols + 32 * cg + 8 * (b & 3) + (b >> 2);
+    const uint32_t code = (col < K) ? idx[(size_t)row * K + col] : 0u;
+    for (int p = 0; p < bmax; ++p) words[p] |= ((code >> (bmax - 1 - p)) & 1u) << b;
   }
-  const long dst = plane_pair_word(rt, kc, N / 16, KC) + lane * 2 + r;
-  for (int p = 0; p < bmax; ++p) planes[p][dst] = words[p];
+  for (int p = 0; p < bmax; ++p) planes[p][li] = words[p];
 }
 
 int launch_pack(const uint8_t *idx, int N, int K, int KC, int u, int I, int bmax,
                 uint32_t *const *plane_out, void *stream) {
-  const long nwords = (long)N * KC * 4;  // N/16 warp tiles * KC chunks * 64 words
+  const long nwords = (long)N * KC * 4;  // 4 words (128 bits) per row and chunk
   const int thr = 256;
   const long blocks = (nwords + thr - 1) / thr;
   pack_kernel<<<(unsigned)blocks, thr, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
@@ -174,61 +172,85 @@ int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_
   return (int)cudaGetLastError();
 }
 
-// Debug read-back through the forward's extraction code: one warp per (warp tile, chunk).
+// Debug read-back through the forward's dequantisation code (pw_dq.cuh): one CTA per
+// (CTA tile, chunk), one thread per (column group, row); the tile's LUT is staged in shared
+// memory as in the expert kernels.
 template <int Q>
-__device__ void unpack_chunk(const BlockDev &bd, int rt, int kc, int u, int I, uint8_t *idx_out,
-                             uint16_t *w_out) {
-  const int lane = threadIdx.x & 31;
-  const long base = plane_pair_word(rt, kc, bd.N / 16, bd.KC) / 2 + lane;
-  uint2 pw_[Q];
+__device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, int u, int I, uint32_t lut_s,
+                             uint8_t *idx_out, uint16_t *w_out) {
+  const int nr = tile_rows(ct, bd.N);
+  const long w0 = slab_word(ct, kc, bd.N, bd.KC) + (long)cg * nr + r;
+  uint32_t W[8];
 #pragma unroll
-  for (int p = 0; p < Q; ++p) pw_[p] = reinterpret_cast<const uint2 *>(bd.plane[p])[base];
-  uint32_t Yg[8], Y8[8];
-  codes_from_planes<Q>(pw_, Yg, Y8);
+  for (int p = 0; p < 8; ++p) W[p] = p < Q ? bd.plane[p][w0] : 0u;
+  const int d = ct * kCtaRows + r;
+  uint32_t v[16], codes[32];
+  if constexpr (Q <= 4) {
+    uint32_t S[4];
+    codes_nib<Q>(W, S);
+    uint32_t P[8];
+    const uint16_t *lr = bd.lut[Q] + (size_t)d * (1 << Q);
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const int d = rt * 16 + 8 * r + (lane & 7);
-    const int row = orig_row(d, u, I);
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int col = kc * 128 + 32 * (lane >> 3) + 4 * s + e;
-        if (col >= bd.K) continue;
-        const uint32_t code = code_at<Q>(r ? Y8[s] : Yg[s], e);
-        if (idx_out) idx_out[(size_t)row * bd.K + col] = (uint8_t)code;
-        if (w_out) w_out[(size_t)row * bd.K + col] = bd.lut[Q][(size_t)d * (1 << Q) + code];
-      }
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t a0 = 2 * i < (1 << Q) ? lr[2 * i] : 0u, a1 = 2 * i + 1 < (1 << Q) ? lr[2 * i + 1] : 0u;
+      P[i] = a0 | (a1 << 16);
     }
+    LutRegs L;
+    lut_regs(P, L);
+    dq_nib<Q>(S, L, v);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) codes[c] = code_nib<Q>(S, c);
+  } else {
+    uint32_t Y[8];
+    codes_byte<Q>(W, Y);
+    dq_byte<Q>(Y, lut_s + ((uint32_t)r << (Q + 1)), v);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) codes[c] = code_byte<Q>(Y, c);
+  }
+  const int row = orig_row(d, u, I);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const int col = kc * kChunkCols + 32 * cg + c;
+    if (col >= bd.K) continue;
+    if (idx_out) idx_out[(size_t)row * bd.K + col] = (uint8_t)codes[c];
+    if (w_out) w_out[(size_t)row * bd.K + col] = (uint16_t)((c & 1) ? (v[c >> 1] >> 16) : (v[c >> 1] & 0xFFFFu));
   }
 }
 
-__global__ void unpack_kernel(const BlockDev *table, int block, int b, int u, int I,
-                              uint8_t *idx_out, uint16_t *w_out) {
+__global__ void __launch_bounds__(512) unpack_kernel(const BlockDev *table, int block, int b, int u, int I,
+                                                     uint8_t *idx_out, uint16_t *w_out) {
+  extern __shared__ __align__(512) uint8_t lut_smem[];
   const BlockDev &bd = table[block];
-  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int ntk = (bd.N / 16) * bd.KC;
-  if (warp_global >= ntk) return;
-  const int rt = warp_global / bd.KC, kc = warp_global % bd.KC;
+  const int ct = blockIdx.x, kc = blockIdx.y;
+  const int nr = tile_rows(ct, bd.N);
+  const int cg = threadIdx.x / kCtaRows, r = threadIdx.x % kCtaRows;
+  if (b >= 5) {  // stage the tile's LUT rows as the expert kernels do
+    const int n16 = nr * (1 << b) / 8;
+    const uint4 *src = reinterpret_cast<const uint4 *>(bd.lut[b] + (size_t)ct * kCtaRows * (1 << b));
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4 *>(lut_smem)[i] = src[i];
+  }
+  __syncthreads();
+  if (r >= nr) return;
+  const uint32_t ls = smem_u32(lut_smem);
   switch (b) {
-    case 1: unpack_chunk<1>(bd, rt, kc, u, I, idx_out, w_out); break;
-    case 2: unpack_chunk<2>(bd, rt, kc, u, I, idx_out, w_out); break;
-    case 3: unpack_chunk<3>(bd, rt, kc, u, I, idx_out, w_out); break;
-    case 4: unpack_chunk<4>(bd, rt, kc, u, I, idx_out, w_out); break;
-    case 5: unpack_chunk<5>(bd, rt, kc, u, I, idx_out, w_out); break;
-    case 6: unpack_chunk<6>(bd, rt, kc, u, I, idx_out, w_out); break;
-    case 7: unpack_chunk<7>(bd, rt, kc, u, I, idx_out, w_out); break;
-    default: unpack_chunk<8>(bd, rt, kc, u, I, idx_out, w_out); break;
+    case 1: unpack_group<1>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 2: unpack_group<2>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 3: unpack_group<3>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 4: unpack_group<4>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 5: unpack_group<5>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 6: unpack_group<6>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 7: unpack_group<7>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    default: unpack_group<8>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
   }
 }
 
 int launch_unpack(const BlockDev *table, int block, int b, int u, int I, int N, int KC, uint8_t *idx_out,
                   uint16_t *w_out, void *stream) {
-  const long warps = (long)(N / 16) * KC;
-  const int thr = 128;
-  const long blocks = (warps * 32 + thr - 1) / thr;
-  unpack_kernel<<<(unsigned)blocks, thr, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      table, block, b, u, I, idx_out, w_out);
+  const int smem = b >= 5 ? kCtaRows * (1 << b) * 2 : 0;
+  cudaFuncSetAttribute(unpack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCtaRows * 256 * 2);
+  dim3 grid((N + kCtaRows - 1) / kCtaRows, KC);
+  unpack_kernel<<<grid, 4 * kCtaRows, smem, reinterpret_cast<cudaStream_t>(stream)>>>(table, block, b, u, I,
+                                                                                      idx_out, w_out);
   return (int)cudaGetLastError();
 }
 

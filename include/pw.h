@@ -318,9 +318,12 @@ pw_status pw_dequant(pw_ctx *ctx, int block, int b, uint16_t *host_out);
 
 /* Self-check of the 5th-generation tensor-core path (tcgen05) on one CTA: D[128][N] =
  * A[128][K] * B[N][K]^T with fp16 A, B (row-major, device) and fp32 D (row-major, device),
- * 16 <= N <= 256 and 16 <= K <= 128, both multiples of 16.  *err (device int) is set to 1
- * if the bounded wait for the MMAs expired.  Asynchronous on `stream`. */
-pw_status pw_tc_selftest(const uint16_t *A, const uint16_t *B, int N, int K, float *D, int *err,
+ * 16 <= N <= 256 and 16 <= K <= 128, both multiples of 16.  flags bit 0: A goes through
+ * tensor memory (written with tcgen05.st, read by the MMA from there) as the expert kernels'
+ * dequantised weights do; otherwise both operands come from shared memory.  Other flag
+ * bits are invalid.  *err (device int) is set to 1 if the bounded wait for the MMAs
+ * expired.  Asynchronous on `stream`.  No counterpart in the paper: a hardware check. */
+pw_status pw_tc_selftest(const uint16_t *A, const uint16_t *B, int N, int K, int flags, float *D, int *err,
                          pw_stream stream);
 
 /* Pure host helpers (no context, no GPU) for checking the packer.

@@ -1,5 +1,6 @@
-"""The tcgen05 building blocks (tensor memory, shared-memory operand descriptors, MMA,
-commit, tensor-memory loads) against a float64 matrix product."""
+"""The tcgen05 building blocks (tensor memory, shared-memory operand descriptors, MMA with A
+from shared memory or from tensor memory, commit, tensor-memory stores and loads) against a
+float64 matrix product."""
 import numpy as np
 import pytest
 
@@ -17,8 +18,9 @@ def gpu_ready():
     _build.build()
 
 
+@pytest.mark.parametrize("a_in_tmem", [False, True])
 @pytest.mark.parametrize("N,K", [(16, 16), (16, 128), (64, 128), (128, 64), (256, 128)])
-def test_tc_gemm_matches_float64(N, K):
+def test_tc_gemm_matches_float64(N, K, a_in_tmem):
     rng = np.random.default_rng(N * 1000 + K)
     A = rng.standard_normal((128, K)).astype(np.float16)
     B = rng.standard_normal((N, K)).astype(np.float16)
@@ -28,7 +30,7 @@ def test_tc_gemm_matches_float64(N, K):
     D = torch.full((128, N), float("nan"), dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     torch.cuda.synchronize()
-    pw.pw_tc_selftest(Ad, Bd, N, K, D, err)
+    pw.pw_tc_selftest(Ad, Bd, N, K, D, err, a_in_tmem=a_in_tmem)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     got = D.cpu().numpy().astype(np.float64)
