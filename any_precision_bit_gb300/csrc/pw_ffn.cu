@@ -9,20 +9,23 @@
 // A work item is a 128-row tile of one block times up to 64 tokens: D[128][N] = W x X^T,
 // N = tokens padded to 16, accumulated in tensor memory.  One persistent CTA per SM, warp-
 // specialised:
-//   * plane producer (1 warp): the tile's LUT_q rows (one TMA bulk copy per item, into one
-//     of two LUT slots so that the next item's table loads while this one runs; a q = 8
-//     table takes both) and, per 128-column chunk, the q bit-plane slabs (one bulk copy per
-//     plane) into a 4-deep ring;
+//   * LUT producer (1 warp): per routed item the tile's LUT_q rows (one TMA bulk copy) into
+//     one of two LUT slots, so that the next item's table loads while this one runs (a q = 8
+//     table takes both);
+//   * weight producer (1 warp): per 128-column chunk the weights into a ring of 2 KB slabs:
+//     the q bit-plane slabs of a routed chunk (lane p copies plane p) or the eight 4 KB K-step
+//     pieces of a dense shared-expert tile (lane t copies piece t).  A chunk takes exactly the
+//     bytes it needs, so low bitwidths keep more chunks in flight;
 //   * activation producer (1 warp): the tokens' fp16 rows (16-byte cp.async gathers) into the
-//     B operand tile and, for the dense shared expert, its fp16 weight tile (one bulk copy)
-//     into the A operand tile, in a 2-deep shared-memory ring;
+//     B operand tile, a 3-deep ring; each lane fences its landed copies to the async proxy
+//     before the tile is released to the MMA thread;
 //   * dequantising warps (16, four per tensor-memory lane quarter): each thread owns one row
 //     and 32 columns of the chunk, turns its plane words into fp16 centroids (pw_dq.cuh) and
 //     writes them straight into tensor memory (tcgen05.st), a 4-deep ring of A buffers;
 //   * MMA thread (1 warp): per chunk eight tcgen05.mma (M = 128, N, K = 16) with A read from
-//     tensor memory (routed blocks) or from shared memory (shared expert), B from shared
-//     memory, the accumulator in one of two tensor-memory buffers; completions reach the
-//     mbarriers through tcgen05.commit;
+//     tensor memory (routed blocks) or from the slab ring (shared expert), B from shared
+//     memory, the accumulator in one of two tensor-memory buffers; tcgen05.commit releases
+//     the chunk's slabs, A buffer and B tile when the MMAs are done;
 //   * epilogue (4 warps, one per lane quarter): tcgen05.ld of the accumulator, then
 //     h = silu(g) * u (gate_up) or the down output, while the next item is being computed.
 // Every mbarrier wait is bounded: on expiry the kernel records an error (PW_ERR_TIMEOUT on
@@ -40,16 +43,17 @@ namespace pw {
 
 constexpr int kDq = 16;                     // dequantising warps 0..15
 constexpr int kEpi = 4;                     // epilogue warps 16..19
-constexpr int kWarpP = kDq + kEpi;          // plane producer
-constexpr int kWarpAB = kWarpP + 1;         // activation / dense-weight producer
+constexpr int kWarpP = kDq + kEpi;          // weight producer
+constexpr int kWarpAB = kWarpP + 1;         // activation producer
 constexpr int kWarpMma = kWarpP + 2;        // MMA issuer, tensor-memory owner
-constexpr int kTcThreads = (kWarpMma + 1) * 32;
-constexpr int kPStages = 4;                 // plane ring depth
-constexpr int kPlaneBytes = kCtaRows * 16;  // one plane slab of a 128-row tile and 128 columns
-constexpr int kPStageBytes = kMaxPlanes * kPlaneBytes;  // 16 KB
+constexpr int kWarpLut = kWarpP + 3;        // LUT producer
+constexpr int kTcThreads = (kWarpLut + 1) * 32;
+constexpr int kSlab = kCtaRows * 16;        // 2 KB: one plane of a 128-row tile and 128 columns
+constexpr int kMaxSlabs = 64;               // slab ring size cap (even)
+constexpr int kRing = 16;                   // chunks in flight (full/empty barrier pairs)
 constexpr int kAStages = 4;                 // tensor-memory A buffers
-constexpr int kABStages = 2;                // shared-memory operand ring
-constexpr int kATileBytes = kCtaRows * kChunkCols * 2;  // 32 KB dense A tile
+constexpr int kBStages = 3;                 // activation tiles
+constexpr int kDenseSlabs = 16;             // a dense 32 KB A tile: 8 pieces of 2 slabs
 constexpr int kLutSlot = 32 * 1024;         // LUT slot (q <= 7); q = 8 takes both slots
 constexpr int kAccCols = 64;                // tensor-memory columns per accumulator buffer
 constexpr int kACols = kChunkCols / 2;      // tensor-memory columns per A buffer (fp16 pairs)
@@ -60,8 +64,9 @@ constexpr int kSmemLimit = 227 * 1024 - 1024;
 
 struct TcLayout {
   int npad_max;    // B tile rows (tokens padded to 16)
-  int ab_bytes;    // one operand stage: dense A tile then B tile
-  int ab_off;      // offset of the operand ring
+  int b_bytes;     // one activation tile
+  int slabs;       // slab ring size (even)
+  int b_off;       // offset of the activation ring
   int lut_off;     // LUT region (+512 bytes for alignment)
   int bar_off;     // mbarriers
   int smem;        // total dynamic shared memory
@@ -69,8 +74,8 @@ struct TcLayout {
 
 // mbarrier indices
 enum {
-  kPF = 0, kPE = kPF + kPStages, kTAF = kPE + kPStages, kTAE = kTAF + kAStages, kBF = kTAE + kAStages,
-  kBE = kBF + kABStages, kLF = kBE + kABStages, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
+  kWFR = 0, kWFD = kWFR + kRing, kWE = kWFD + kRing, kTAF = kWE + kRing, kTAE = kTAF + kAStages, kBF = kTAE + kAStages,
+  kBE = kBF + kBStages, kLF = kBE + kBStages, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
   kNumBars = kDrain + 1
 };
 
@@ -129,7 +134,7 @@ __device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const TcLayout &
   return (smem_u32(sm) + L.lut_off + 511u) & ~511u;
 }
 
-// LUT slot schedule, replayed identically by the plane producer and the dequantising warps:
+// LUT slot schedule, replayed identically by the weight producer and the dequantising warps:
 // tables of q <= 7 alternate between the two slots; a q = 8 table (64 KB) takes both.
 struct LutSched {
   uint32_t fills[2] = {0u, 0u}, uses[2] = {0u, 0u};
@@ -141,6 +146,37 @@ struct LutSched {
     return slot;
   }
 };
+
+// Position in the slab ring, replayed identically by every role: chunk c (all items, in
+// order) takes q slabs (routed) or 16 slabs starting at an even slab (dense; one padding
+// slab when needed, so that no 4 KB piece wraps).  n = slabs consumed, padding included.
+// Routed and dense chunks also count separately (seq): their "weights landed" barriers are
+// separate sequences, because the dequantising warps wait only on routed chunks and skip
+// the dense ones.  A waiter that skipped fills of a barrier could otherwise run two phases
+// ahead of it, where a parity wait cannot tell the phase it wants from an old one.
+struct RingPos {
+  uint32_t slot = 0, c = 0, rc = 0, dc = 0;
+  __device__ __forceinline__ uint32_t take(bool routed, int q, int S, uint32_t &n, uint32_t &seq) {
+    const uint32_t pad = routed ? 0u : (slot & 1u);
+    const uint32_t nd = routed ? (uint32_t)q : (uint32_t)kDenseSlabs;
+    uint32_t base = slot + pad;
+    if (base >= (uint32_t)S) base -= (uint32_t)S;
+    slot = base + nd;
+    if (slot >= (uint32_t)S) slot -= (uint32_t)S;
+    n = pad + nd;
+    seq = routed ? rc++ : dc++;
+    ++c;
+    return base;
+  }
+};
+// "weights landed" barrier of a chunk: routed and dense sequences
+__device__ __forceinline__ uint32_t wf_bar(uint32_t bars, bool routed, uint32_t seq) {
+  return bars + 8 * ((routed ? kWFR : kWFD) + seq % kRing);
+}
+__device__ __forceinline__ uint32_t ring_add(uint32_t a, uint32_t b, int S) {
+  const uint32_t r = a + b;
+  return r >= (uint32_t)S ? r - (uint32_t)S : r;
+}
 
 // Bounded wait on an mbarrier phase; false on expiry or when another warp gave up.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
@@ -178,51 +214,103 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 
 // ------------------------------------------------------------------ roles
 template <int PHASE>
-__device__ void plane_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
-                               volatile int *abort_flag) {
-  if ((threadIdx.x & 31) != 0) return;
+__device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                                volatile int *abort_flag) {
+  const int lane = threadIdx.x & 31;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  const uint32_t lut0 = lut_base(sm, L);
-  uint32_t p_seq = 0;
-  LutSched ls;
+  const uint32_t ring = smem_u32(sm);
+  const int S = L.slabs;
+  RingPos pos;
+  uint32_t head = 0, released = 0, oldest = 0;  // lane 0's room accounting
+  uint8_t nslab[kRing];
+  uint32_t wfseq[kRing];  // in-flight chunk: routed flag (bit 31) and sequence number
   bool ok = true;
   for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
-    if (!v.routed) continue;
+    // lane p < q copies plane p of every chunk; lane t < 8 copies K-step piece t of a dense tile
+    const uint32_t *plane = (v.routed && lane < v.q) ? v.bd->plane[lane] : nullptr;
+    const uint32_t bytes = (uint32_t)v.nr * 16;
+    for (int kc = w.kc0; kc < w.kc1 && ok; ++kc) {
+      const uint32_t c = pos.c;
+      uint32_t n, seq;
+      const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
+      const uint32_t full = wf_bar(bars, v.routed, seq);
+      if (lane == 0) {
+        // room: at most kRing chunks in flight and their slabs within the ring
+        while (ok && (head + n > released + (uint32_t)S || c - oldest >= (uint32_t)kRing)) {
+          ok = wait_bar(bars + 8 * (kWE + oldest % kRing), (oldest / kRing) & 1, abort_flag, a.s.err);
+          if (ok) {
+            released += nslab[oldest % kRing];
+            ++oldest;
+          }
+        }
+        if (ok) {
+          nslab[c % kRing] = (uint8_t)n;
+          wfseq[c % kRing] = seq | (v.routed ? 0x80000000u : 0u);
+          head += n;
+          mbar_arrive_expect_tx(full, v.routed ? bytes * v.q : (uint32_t)(kCtaRows * kChunkCols * 2));
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      if (v.routed) {
+        if (lane < v.q)
+          bulk_g2s(ring + ring_add(base, lane, S) * kSlab, plane + slab_word(w.tile, kc, v.N, v.KC), bytes, full);
+      } else if (lane < 8) {
+        const uint16_t *src = v.W + ((long)w.tile * v.KC + kc) * (kCtaRows * kChunkCols) + lane * 2048;
+        bulk_g2s(ring + ring_add(base, 2 * lane, S) * kSlab, src, 2 * kSlab, full);
+      }
+    }
+  }
+  // every copy issued must land before the CTA may exit
+  __syncwarp();
+  if (lane == 0)
+    for (uint32_t k = oldest; k < pos.c; ++k) {
+      const uint32_t sq = wfseq[k % kRing] & 0x7FFFFFFFu;
+      drain_bar(wf_bar(bars, (wfseq[k % kRing] >> 31) != 0, sq), (sq / kRing) & 1);
+    }
+}
+
+// LUT_q rows of every routed item's tile, as far ahead as the two slots allow.
+template <int PHASE>
+__device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                             volatile int *abort_flag) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int n_items = a.s.n_items[PHASE - 1];
+  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  const uint32_t lut0 = lut_base(sm, L);
+  LutSched ls;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const WorkItem w = items[it];
+    if (w.kind != 0) continue;
+    const BlockDev *bd = &a.table[(a.layer * a.E + w.expert) * 2 + (PHASE - 1)];
+    const int q = bd->q, nr = tile_rows(w.tile, bd->N);
     bool both;
-    const int slot = ls.next(v.q, both);
-    ok = wait_bar(bars + 8 * (kLE + slot), (ls.uses[slot] & 1) ^ 1, abort_flag, a.s.err);
+    const int slot = ls.next(q, both);
+    bool ok = wait_bar(bars + 8 * (kLE + slot), (ls.uses[slot] & 1) ^ 1, abort_flag, a.s.err);
     if (ok && both) ok = wait_bar(bars + 8 * (kLE + 1), (ls.uses[1] & 1) ^ 1, abort_flag, a.s.err);
     if (!ok) break;
     ++ls.uses[slot];
     if (both) ++ls.uses[1];
-    const uint32_t lbytes = (uint32_t)v.nr << v.q << 1;
+    const uint32_t lbytes = (uint32_t)nr << q << 1;
     mbar_arrive_expect_tx(bars + 8 * (kLF + slot), lbytes);
-    bulk_g2s(lut0 + slot * kLutSlot, v.bd->lut[v.q] + ((size_t)w.tile * kCtaRows << v.q), lbytes,
-             bars + 8 * (kLF + slot));
+    bulk_g2s(lut0 + slot * kLutSlot, bd->lut[q] + ((size_t)w.tile * kCtaRows << q), lbytes, bars + 8 * (kLF + slot));
     ++ls.fills[slot];
-    for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int ps = p_seq % kPStages;
-      ok = wait_bar(bars + 8 * (kPE + ps), ((p_seq / kPStages) & 1) ^ 1, abort_flag, a.s.err);
-      if (!ok) break;
-      const uint32_t bytes = (uint32_t)v.nr * 16;
-      const uint32_t full = bars + 8 * (kPF + ps);
-      mbar_arrive_expect_tx(full, bytes * v.q);
-      const long off = slab_word(w.tile, kc, v.N, v.KC);
-      const uint32_t dst = smem_u32(sm) + ps * kPStageBytes;
-      for (int p = 0; p < v.q; ++p) bulk_g2s(dst + p * kPlaneBytes, v.bd->plane[p] + off, bytes, full);
-      ++p_seq;
-    }
-  }
-  // every copy issued must land before the CTA may exit
-  for (uint32_t k = 0; k < (uint32_t)kPStages && k < p_seq; ++k) {
-    const uint32_t q = p_seq - 1 - k;
-    drain_bar(bars + 8 * (kPF + q % kPStages), (q / kPStages) & 1);
   }
   for (int s = 0; s < 2; ++s)
     if (ls.fills[s] > 0) drain_bar(bars + 8 * (kLF + s), (ls.fills[s] - 1) & 1);
+}
+
+// The activation tiles are written with cp.async, a generic-proxy write; the MMAs read them
+// through the async proxy.  So each lane waits for its own copies of a chunk, fences them to
+// the async proxy, and only then does lane 0 release the tile, one chunk behind the copies
+// in flight so that their latency stays hidden.
+__device__ __forceinline__ void release_b(uint32_t bars, uint32_t seq, int lane) {
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bars + 8 * (kBF + seq % kBStages));
 }
 
 template <int PHASE>
@@ -231,7 +319,7 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
   const int lane = threadIdx.x & 31;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  uint32_t ab_seq = 0;
+  uint32_t b_seq = 0;
   bool ok = true;
   for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
     const WorkItem w = items[it];
@@ -239,22 +327,11 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     const uint16_t *rb0 = lane < v.ntok ? act_row<PHASE>(a, v, lane) : nullptr;
     const uint16_t *rb1 = lane + 32 < v.ntok ? act_row<PHASE>(a, v, lane + 32) : nullptr;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int as = ab_seq % kABStages;
-      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + as), ((ab_seq / kABStages) & 1) ^ 1, abort_flag, a.s.err);
+      const int bs = b_seq % kBStages;
+      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / kBStages) & 1) ^ 1, abort_flag, a.s.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const uint32_t full = bars + 8 * (kBF + as);
-      const uint32_t a_tile = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
-      const uint32_t b_tile = a_tile + kATileBytes;
-      if (lane == 0) {
-        if (v.routed) {
-          mbar_arrive(full);
-        } else {
-          mbar_arrive_expect_tx(full, kATileBytes);
-          const long tile_elem = ((long)w.tile * v.KC + kc) * (kCtaRows * kChunkCols);
-          bulk_g2s(a_tile, v.W + tile_elem, kATileBytes, full);
-        }
-      }
+      const uint32_t b_tile = smem_u32(sm) + L.b_off + bs * L.b_bytes;
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int j = lane + 32 * r;
@@ -267,15 +344,17 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
           cp_async16(b_tile + core_offset128(j, c16 * 8), valid ? rb + col : a.s.xh, valid ? 16u : 0u);
         }
       }
-      cp_async_arrive(full);
-      ++ab_seq;
+      cp_async_commit();
+      if (b_seq > 0) {  // the previous chunk's copies: landed, fenced, released
+        cp_async_wait<1>();
+        release_b(bars, b_seq - 1, lane);
+      }
+      ++b_seq;
     }
   }
-  if (lane == 0)
-    for (uint32_t k = 0; k < (uint32_t)kABStages && k < ab_seq; ++k) {
-      const uint32_t q = ab_seq - 1 - k;
-      drain_bar(bars + 8 * (kBF + q % kABStages), (q / kABStages) & 1);
-    }
+  // the last chunk (also on the way out after an abort: nothing may be left in flight)
+  cp_async_wait<0>();
+  if (b_seq > 0) release_b(bars, b_seq - 1, lane);
 }
 
 template <int PHASE>
@@ -284,7 +363,10 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
   if ((threadIdx.x & 31) != 0) return;
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  uint32_t ab_seq = 0, a_seq = 0, item_seq = 0;
+  const uint32_t ring = smem_u32(sm);
+  const int S = L.slabs;
+  RingPos pos;
+  uint32_t b_seq = 0, a_seq = 0, item_seq = 0;
   bool ok = true;
   for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
     const WorkItem w = items[it];
@@ -297,19 +379,18 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
     const uint32_t d = tmem + acs * kAccCols;
     bool first = true;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int as = ab_seq % kABStages, ts = a_seq % kAStages;
-      if (v.routed) {
+      const uint32_t c = pos.c;
+      uint32_t n, seq;
+      const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
+      const int bs = b_seq % kBStages, ts = a_seq % kAStages;
+      if (v.routed)
         ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / kAStages) & 1, abort_flag, a.s.err);
-        if (!ok) break;
-      }
-      ok = wait_bar(bars + 8 * (kBF + as), (ab_seq / kABStages) & 1, abort_flag, a.s.err);
+      else
+        ok = wait_bar(wf_bar(bars, false, seq), (seq / kRing) & 1, abort_flag, a.s.err);
+      if (ok) ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / kBStages) & 1, abort_flag, a.s.err);
       if (!ok) break;
-      // the B rows were written through the generic proxy; the MMAs read them through the
-      // async proxy
-      fence_async_smem();
       tc_fence_after();
-      const uint32_t a0 = smem_u32(sm) + L.ab_off + as * L.ab_bytes;
-      const uint32_t b0 = a0 + kATileBytes;
+      const uint32_t b0 = smem_u32(sm) + L.b_off + bs * L.b_bytes;
       if (v.routed) {
         const uint32_t at = tmem + kAColBase + ts * kACols;
 #pragma unroll
@@ -320,12 +401,13 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
       } else {
 #pragma unroll
         for (int t = 0; t < 8; ++t)
-          tc_mma_f16(d, smem_desc(a0 + 256 * t, 128, 16 * 128), smem_desc(b0 + 256 * t, 128, 16 * 128), idesc,
-                     (first && t == 0) ? 0u : 1u);
+          tc_mma_f16(d, smem_desc(ring + ring_add(base, 2 * t, S) * kSlab, 128, 256),
+                     smem_desc(b0 + 256 * t, 128, 16 * 128), idesc, (first && t == 0) ? 0u : 1u);
       }
       first = false;
-      tc_commit(bars + 8 * (kBE + as));
-      ++ab_seq;
+      tc_commit(bars + 8 * (kBE + bs));
+      tc_commit(bars + 8 * (kWE + c % kRing));  // the chunk's slabs
+      ++b_seq;
     }
     if (!ok) break;
     tc_commit(bars + 8 * (kAF + acs));
@@ -336,15 +418,28 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
   drain_bar(bars + 8 * kDrain, 0);
 }
 
+// Dequantising thread's pending tensor-memory store: completed, made visible and signalled to
+// the MMA thread during the next chunk, so that its latency hides behind that chunk's plane
+// loads and bit transpose.
+__device__ __forceinline__ void flush_store(uint32_t bars, int &pending_ts, int lane) {
+  if (pending_ts < 0) return;
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bars + 8 * (kTAF + pending_ts));
+  pending_ts = -1;
+}
+
 // One routed item for a dequantising thread: row r of the tile, columns [32 cg, 32 cg + 32)
 // of every chunk.
 template <int PHASE, int Q>
-__device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, uint32_t bars,
-                        uint32_t tmem, uint32_t lut_slot, int quarter, int cg, uint32_t &p_seq, uint32_t &a_seq,
-                        volatile int *abort_flag) {
+__device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, const TcLayout &L,
+                        uint32_t bars, uint32_t tmem, uint32_t lut_slot, int quarter, int cg, RingPos &pos,
+                        uint32_t &a_seq, int &pending_ts, volatile int *abort_flag) {
   const int lane = threadIdx.x & 31;
   const int r = 32 * quarter + lane;
   const bool rv = r < v.nr;
+  const int S = L.slabs;
   LutRegs Lr;
   uint32_t row_addr = 0;
   if constexpr (Q <= 4) {
@@ -371,39 +466,46 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   } else {
     row_addr = lut_slot + ((uint32_t)r << (Q + 1));
   }
-  const uint32_t word_off = (uint32_t)(cg * v.nr + r) * 4;
+  const uint32_t ring = smem_u32(sm) + (uint32_t)(cg * v.nr + r) * 4;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+  uint32_t v16[16];
   for (int kc = w.kc0; kc < w.kc1; ++kc) {
-    const int ps = p_seq % kPStages, ts = a_seq % kAStages;
-    if (!wait_bar(bars + 8 * (kPF + ps), (p_seq / kPStages) & 1, abort_flag, a.s.err)) return false;
-    const uint32_t stage = smem_u32(sm) + ps * kPStageBytes + word_off;
+    uint32_t n, seq;
+    uint32_t sl = pos.take(true, Q, S, n, seq);
+    const int ts = a_seq % kAStages;
+    if (!wait_bar(wf_bar(bars, true, seq), (seq / kRing) & 1, abort_flag, a.s.err)) return false;
     uint32_t W[8];
 #pragma unroll
-    for (int p = 0; p < 8; ++p) W[p] = (p < Q && rv) ? lds32(stage + p * kPlaneBytes) : 0u;
-    uint32_t v16[16];
+    for (int p = 0; p < 8; ++p) {
+      W[p] = 0u;
+      if (p < Q) {
+        if (rv) W[p] = lds32(ring + sl * kSlab);
+        sl = (sl + 1 == (uint32_t)S) ? 0u : sl + 1;
+      }
+    }
+    // tcgen05.st reads its source registers asynchronously: the previous chunk's store must
+    // be complete (flush_store) before v16 is rewritten; the plane loads and the bit
+    // transpose of this chunk overlap it
     if constexpr (Q <= 4) {
-      uint32_t S[4];
-      codes_nib<Q>(W, S);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kPE + ps));  // the slab words are in registers
-      dq_nib<Q>(S, Lr, v16);
+      uint32_t S4[4];
+      codes_nib<Q>(W, S4);
+      flush_store(bars, pending_ts, lane);
+      dq_nib<Q>(S4, Lr, v16);
     } else {
       uint32_t Y[8];
       codes_byte<Q>(W, Y);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kPE + ps));
+      flush_store(bars, pending_ts, lane);
       dq_byte<Q>(Y, row_addr, v16);
     }
-    ++p_seq;
     if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
     tc_fence_after();
     tmem_st16(tmem + lane_base + kAColBase + ts * kACols + 16 * cg, v16);
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * (kTAF + ts));
+    pending_ts = ts;
     ++a_seq;
   }
+  // the item's last store is signalled now: what follows may need the MMA thread to have
+  // released slabs, which it does only after this chunk's MMAs
+  flush_store(bars, pending_ts, lane);
   return true;
 }
 
@@ -415,12 +517,20 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
   const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t lut0 = lut_base(sm, L);
-  uint32_t p_seq = 0, a_seq = 0;
+  RingPos pos;
+  uint32_t a_seq = 0;
+  int pending_ts = -1;
   LutSched ls;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
-    if (!v.routed) continue;
+    if (!v.routed) {  // dense chunks: only the ring position moves
+      for (int kc = w.kc0; kc < w.kc1; ++kc) {
+        uint32_t n, seq;
+        pos.take(false, 0, L.slabs, n, seq);
+      }
+      continue;
+    }
     bool both;
     const int slot = ls.next(v.q, both);
     if (!wait_bar(bars + 8 * (kLF + slot), ls.fills[slot] & 1, abort_flag, a.s.err)) return;
@@ -428,16 +538,24 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     const uint32_t lut_slot = lut0 + slot * kLutSlot;
     bool ok;
     switch (v.q) {
-      case 1: ok = dq_item<PHASE, 1>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      case 2: ok = dq_item<PHASE, 2>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      case 3: ok = dq_item<PHASE, 3>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      case 4: ok = dq_item<PHASE, 4>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      case 5: ok = dq_item<PHASE, 5>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      case 6: ok = dq_item<PHASE, 6>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      case 7: ok = dq_item<PHASE, 7>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
-      default: ok = dq_item<PHASE, 8>(a, w, v, sm, bars, tmem, lut_slot, quarter, cg, p_seq, a_seq, abort_flag); break;
+#define PW_DQ_CASE(QQ)                                                                                       \
+  case QQ:                                                                                                   \
+    ok = dq_item<PHASE, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts, abort_flag); \
+    break;
+      PW_DQ_CASE(1)
+      PW_DQ_CASE(2)
+      PW_DQ_CASE(3)
+      PW_DQ_CASE(4)
+      PW_DQ_CASE(5)
+      PW_DQ_CASE(6)
+      PW_DQ_CASE(7)
+      default:
+        ok = dq_item<PHASE, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts, abort_flag);
+        break;
+#undef PW_DQ_CASE
     }
     if (!ok) return;
+    // the LUT slot is free once this item's last centroids are in registers
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(bars + 8 * (kLE + slot));
@@ -504,16 +622,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   const int warp = threadIdx.x >> 5;
   const uint32_t bars = smem_u32(sm + L.bar_off);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kPStages; ++i) {
-      mbar_init(bars + 8 * (kPF + i), 1);
-      mbar_init(bars + 8 * (kPE + i), kDq);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(bars + 8 * (kWFR + i), 1);
+      mbar_init(bars + 8 * (kWFD + i), 1);
+      mbar_init(bars + 8 * (kWE + i), 1);
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(bars + 8 * (kTAF + i), kDq);
       mbar_init(bars + 8 * (kTAE + i), 1);
     }
-    for (int i = 0; i < kABStages; ++i) {
-      mbar_init(bars + 8 * (kBF + i), 32 + 1);  // cp.async lanes, producer lane 0
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(bars + 8 * (kBF + i), 1);  // lane 0 of the activation producer
       mbar_init(bars + 8 * (kBE + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -539,11 +658,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   else if (warp < kWarpP)
     epilogue<PHASE>(a, bars, tmem, &abort_flag);
   else if (warp == kWarpP)
-    plane_producer<PHASE>(a, L, sm, bars, &abort_flag);
+    weight_producer<PHASE>(a, L, sm, bars, &abort_flag);
   else if (warp == kWarpAB)
     ab_producer<PHASE>(a, L, sm, bars, &abort_flag);
-  else
+  else if (warp == kWarpMma)
     mma_issuer<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+  else
+    lut_producer<PHASE>(a, L, sm, bars, &abort_flag);
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -555,9 +676,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
 static TcLayout tc_layout(const FwdArgs &a) {
   TcLayout L{};
   L.npad_max = max(16, (min(a.T, kTokChunk) + 15) / 16 * 16);
-  L.ab_bytes = kATileBytes + L.npad_max * kChunkCols * 2;
-  L.ab_off = kPStages * kPStageBytes;
-  L.lut_off = L.ab_off + kABStages * L.ab_bytes;
+  L.b_bytes = L.npad_max * kChunkCols * 2;
+  const int fixed = kBStages * L.b_bytes + 2 * kLutSlot + 512 + kNumBars * 8;
+  L.slabs = min(kMaxSlabs, (kSmemLimit - fixed) / kSlab) & ~1;
+  L.b_off = L.slabs * kSlab;
+  L.lut_off = L.b_off + kBStages * L.b_bytes;
   L.bar_off = L.lut_off + 2 * kLutSlot + 512;
   L.smem = L.bar_off + kNumBars * 8;
   return L;
@@ -565,7 +688,7 @@ static TcLayout tc_layout(const FwdArgs &a) {
 
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
   const TcLayout L = tc_layout(a);
-  if (L.smem > kSmemLimit) return (int)cudaErrorInvalidConfiguration;
+  if (L.smem > kSmemLimit || L.slabs < 2 * kDenseSlabs) return (int)cudaErrorInvalidConfiguration;
   cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

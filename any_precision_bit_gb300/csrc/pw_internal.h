@@ -99,12 +99,17 @@ PW_HD int core_offset128(int row, int col) {
 }
 
 // Kernel-private layout of dense fp16 shared-expert weights (N x K): rows padded to a
-// multiple of 128, columns to a multiple of 128; each (128-row tile, 128-column chunk) is a
-// contiguous 32 KB operand tile in the core-matrix order above, tiles ordered [tile][chunk].
+// multiple of 128, columns to a multiple of 128.  Each (128-row tile, 128-column chunk) is a
+// contiguous 32 KB operand tile, tiles ordered [tile][chunk]; inside it, the eight 16-column
+// K-steps of one MMA each are contiguous 4 KB pieces, and a piece holds the 16 row groups of
+// 8 rows, each as two 8x8 core matrices (columns 0..7, 8..15 of the step) of 128 bytes.
+// One piece is thus one MMA's A operand with a 128-byte K stride and a 256-byte row-group
+// stride, and the pieces of a tile may sit anywhere in shared memory.
 PW_HD long shared_tile_index(int d, int k, int K) {
   const int KCh = kpad_cols(K) / kChunkCols;
-  return ((long)(d / kCtaRows) * KCh + k / kChunkCols) * (kCtaRows * kChunkCols) +
-         core_offset128(d % kCtaRows, k % kChunkCols) / 2;
+  const int r = d % kCtaRows, c = k % kChunkCols;
+  return ((long)(d / kCtaRows) * KCh + k / kChunkCols) * (kCtaRows * kChunkCols) + (c / 16) * 2048 +
+         (r / 8) * 128 + ((c % 16) / 8) * 64 + (r % 8) * 8 + (c % 8);
 }
 
 }  // namespace pw
