@@ -12,7 +12,10 @@
 //   * LUT producer (1 warp): per routed item the tile's LUT_q rows (one TMA bulk copy) into
 //     one of two LUT slots, so that the next item's table loads while this one runs (a q = 8
 //     table takes both);
-//   * weight producer (1 warp): per 128-column chunk the weights into a ring of 2 KB slabs:
+//   * weight producer (1 warp): claims the work items one at a time from the launch's atomic
+//     counter when it is ready to stream the next one (so CTAs that finish early take more),
+//     publishes them in order to the other roles through a shared-memory queue, and copies
+//     per 128-column chunk the weights into a ring of 2 KB slabs:
 //     the q bit-plane slabs of a routed chunk (lane p copies plane p) or the eight 4 KB K-step
 //     pieces of a dense shared-expert tile (lane t copies piece t).  A chunk takes exactly the
 //     bytes it needs, so low bitwidths keep more chunks in flight;
@@ -51,6 +54,8 @@ constexpr int kTcThreads = (kWarpLut + 1) * 32;
 constexpr int kSlab = kCtaRows * 16;        // 2 KB: one plane of a 128-row tile and 128 columns
 constexpr int kMaxSlabs = 64;               // slab ring size cap (even)
 constexpr int kRing = 16;                   // chunks in flight (full/empty barrier pairs)
+constexpr int kQueue = 8;                   // claimed work items published to the roles
+constexpr int kQueueReaders = kDq + kEpi + 3;  // warps that read the queue (all but the weight producer)
 constexpr int kAStages = 4;                 // tensor-memory A buffers
 constexpr int kBStages = 3;                 // activation tiles
 constexpr int kDenseSlabs = 16;             // a dense 32 KB A tile: 8 pieces of 2 slabs
@@ -76,7 +81,7 @@ struct TcLayout {
 enum {
   kWFR = 0, kWFD = kWFR + kRing, kWE = kWFD + kRing, kTAF = kWE + kRing, kTAE = kTAF + kAStages, kBF = kTAE + kAStages,
   kBE = kBF + kBStages, kLF = kBE + kBStages, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
-  kNumBars = kDrain + 1
+  kIQF = kDrain + 1, kIQE = kIQF + kQueue, kNumBars = kIQE + kQueue
 };
 
 struct ItemView {
@@ -194,6 +199,24 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Work items are claimed one at a time (atomic counter) by the weight producer and published,
+// in order, in a shared-memory queue that every other role reads.  Entry k of a role's
+// sequence: the item index, or -1 once the items are exhausted.
+struct ItemQueue {
+  volatile int *slot;  // [kQueue]
+  uint32_t bars;
+};
+// Reader side, one call per warp and entry (lane 0 releases the entry after the warp read it).
+// `lanes`: the lanes of the warp that run the role (all, or lane 0 alone).
+__device__ __forceinline__ int queue_read(const ItemQueue &qu, uint32_t k, unsigned lanes, volatile int *abort_flag,
+                                          int *err) {
+  if (!wait_bar(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1, abort_flag, err)) return -1;
+  const int it = qu.slot[k % kQueue];
+  __syncwarp(lanes);
+  if ((threadIdx.x & 31) == 0) mbar_arrive(qu.bars + 8 * (kIQE + k % kQueue));
+  return it;
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -215,74 +238,97 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
 // ------------------------------------------------------------------ roles
 template <int PHASE>
 __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
-                                volatile int *abort_flag) {
+                                const ItemQueue &qu, volatile int *abort_flag) {
   const int lane = threadIdx.x & 31;
-  const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t ring = smem_u32(sm);
   const int S = L.slabs;
+  const int n_items = a.s.n_items[PHASE - 1];
   RingPos pos;
-  uint32_t head = 0, released = 0, oldest = 0;  // lane 0's room accounting
-  uint8_t nslab[kRing];
-  uint32_t wfseq[kRing];  // in-flight chunk: routed flag (bit 31) and sequence number
+  // room accounting (the same in every lane); the chunks in flight are kept across the
+  // lanes: lane i holds chunk c with c % kRing == i (its slab count and landed barrier)
+  uint32_t head = 0, released = 0, oldest = 0;
+  uint32_t my_n = 0, my_wf = 0, my_par = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+  for (uint32_t k = 0; ok; ++k) {
+    // claim the next work item only now that this one is needed, and publish it to the other
+    // roles; entry k % kQueue is free once every reader has read its previous use
+    int it = -1;
+    if (lane == 0) {
+      ok = wait_bar(qu.bars + 8 * (kIQE + k % kQueue), ((k / kQueue) & 1) ^ 1, abort_flag, a.s.err);
+      if (ok) {
+        it = atomicAdd(a.s.work + (PHASE - 1), 1);
+        if (it >= n_items) it = -1;
+        qu.slot[k % kQueue] = it;
+        mbar_arrive(qu.bars + 8 * (kIQF + k % kQueue));
+      }
+    }
+    it = __shfl_sync(0xffffffffu, it, 0);
+    if (it < 0) break;
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
     // lane p < q copies plane p of every chunk; lane t < 8 copies K-step piece t of a dense tile
-    const uint32_t *plane = (v.routed && lane < v.q) ? v.bd->plane[lane] : nullptr;
     const uint32_t bytes = (uint32_t)v.nr * 16;
-    for (int kc = w.kc0; kc < w.kc1 && ok; ++kc) {
+    const uint32_t tx = v.routed ? bytes * v.q : (uint32_t)(kCtaRows * kChunkCols * 2);
+    const uint8_t *src = nullptr;
+    uint32_t src_step = 0, lane_slab = 0;
+    if (v.routed) {
+      if (lane < v.q)
+        src = reinterpret_cast<const uint8_t *>(v.bd->plane[lane] + slab_word(w.tile, w.kc0, v.N, v.KC));
+      src_step = bytes;  // slabs of consecutive chunks are consecutive
+      lane_slab = lane;
+    } else {
+      src = reinterpret_cast<const uint8_t *>(v.W + ((long)w.tile * v.KC + w.kc0) * (kCtaRows * kChunkCols) +
+                                              lane * 2048);
+      src_step = kCtaRows * kChunkCols * 2;
+      lane_slab = 2 * lane;
+    }
+    const bool copies = v.routed ? lane < v.q : lane < 8;
+    const uint32_t cbytes = v.routed ? bytes : 2 * kSlab;
+    for (int kc = w.kc0; kc < w.kc1; ++kc) {
       const uint32_t c = pos.c;
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
       const uint32_t full = wf_bar(bars, v.routed, seq);
-      if (lane == 0) {
-        // room: at most kRing chunks in flight and their slabs within the ring
-        while (ok && (head + n > released + (uint32_t)S || c - oldest >= (uint32_t)kRing)) {
-          ok = wait_bar(bars + 8 * (kWE + oldest % kRing), (oldest / kRing) & 1, abort_flag, a.s.err);
-          if (ok) {
-            released += nslab[oldest % kRing];
-            ++oldest;
-          }
-        }
-        if (ok) {
-          nslab[c % kRing] = (uint8_t)n;
-          wfseq[c % kRing] = seq | (v.routed ? 0x80000000u : 0u);
-          head += n;
-          mbar_arrive_expect_tx(full, v.routed ? bytes * v.q : (uint32_t)(kCtaRows * kChunkCols * 2));
-        }
+      // room: at most kRing chunks in flight and their slabs within the ring
+      while (head + n > released + (uint32_t)S || c - oldest >= (uint32_t)kRing) {
+        if (lane == 0) ok = wait_bar(bars + 8 * (kWE + oldest % kRing), (oldest / kRing) & 1, abort_flag, a.s.err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        released += __shfl_sync(0xffffffffu, my_n, oldest % kRing);
+        ++oldest;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      if (v.routed) {
-        if (lane < v.q)
-          bulk_g2s(ring + ring_add(base, lane, S) * kSlab, plane + slab_word(w.tile, kc, v.N, v.KC), bytes, full);
-      } else if (lane < 8) {
-        const uint16_t *src = v.W + ((long)w.tile * v.KC + kc) * (kCtaRows * kChunkCols) + lane * 2048;
-        bulk_g2s(ring + ring_add(base, 2 * lane, S) * kSlab, src, 2 * kSlab, full);
+      if (lane == (int)(c % kRing)) {
+        my_n = n;
+        my_wf = full;
+        my_par = (seq / kRing) & 1;
       }
+      head += n;
+      if (lane == 0) mbar_arrive_expect_tx(full, tx);
+      __syncwarp();
+      if (copies) bulk_g2s(ring + ring_add(base, lane_slab, S) * kSlab, src, cbytes, full);
+      src += src_step;
     }
   }
-  // every copy issued must land before the CTA may exit
+  // every copy issued must land before the CTA may exit: each lane drains its chunk in flight
   __syncwarp();
-  if (lane == 0)
-    for (uint32_t k = oldest; k < pos.c; ++k) {
-      const uint32_t sq = wfseq[k % kRing] & 0x7FFFFFFFu;
-      drain_bar(wf_bar(bars, (wfseq[k % kRing] >> 31) != 0, sq), (sq / kRing) & 1);
-    }
+  if (lane < kRing && oldest + (uint32_t)((lane - (int)(oldest % kRing) + kRing) % kRing) < pos.c)
+    drain_bar(my_wf, my_par);
 }
 
-// LUT_q rows of every routed item's tile, as far ahead as the two slots allow.
+// LUT_q rows of every routed item's tile (one TMA bulk copy), as far ahead as the two slots
+// allow.
 template <int PHASE>
-__device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
+__device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, const ItemQueue &qu,
                              volatile int *abort_flag) {
   if ((threadIdx.x & 31) != 0) return;
-  const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t lut0 = lut_base(sm, L);
   LutSched ls;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    const int it = queue_read(qu, k, 1u, abort_flag, a.s.err);
+    if (it < 0) break;
     const WorkItem w = items[it];
     if (w.kind != 0) continue;
     const BlockDev *bd = &a.table[(a.layer * a.E + w.expert) * 2 + (PHASE - 1)];
@@ -315,17 +361,24 @@ __device__ __forceinline__ void release_b(uint32_t bars, uint32_t seq, int lane)
 
 template <int PHASE>
 __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
-                            volatile int *abort_flag) {
+                            const ItemQueue &qu, volatile int *abort_flag) {
   const int lane = threadIdx.x & 31;
-  const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  // lane L copies rows L % 16 + 16 k of the tile, 16-byte segments 8 (L / 16) .. 8 (L / 16) + 7
+  const int r0 = lane & 15, seg0 = (lane >> 4) * 8;
   uint32_t b_seq = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+  for (uint32_t k = 0; ok; ++k) {
+    const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
+    if (it < 0) break;
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
-    const uint16_t *rb0 = lane < v.ntok ? act_row<PHASE>(a, v, lane) : nullptr;
-    const uint16_t *rb1 = lane + 32 < v.ntok ? act_row<PHASE>(a, v, lane + 32) : nullptr;
+    const uint16_t *rb[4];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      const int j = r0 + 16 * q4;
+      rb[q4] = j < v.ntok ? act_row<PHASE>(a, v, j) : nullptr;
+    }
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
       const int bs = b_seq % kBStages;
       if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / kBStages) & 1) ^ 1, abort_flag, a.s.err);
@@ -333,15 +386,15 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       if (!ok) break;
       const uint32_t b_tile = smem_u32(sm) + L.b_off + bs * L.b_bytes;
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int j = lane + 32 * r;
-        if (j >= v.npad) break;
-        const uint16_t *rb = r ? rb1 : rb0;
-#pragma unroll 4
-        for (int c16 = 0; c16 < 16; ++c16) {
-          const int col = kc * kChunkCols + c16 * 8;
-          const bool valid = rb != nullptr && col < v.Kc;
-          cp_async16(b_tile + core_offset128(j, c16 * 8), valid ? rb + col : a.s.xh, valid ? 16u : 0u);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int j = r0 + 16 * q4;
+        if (16 * q4 >= v.npad) break;
+        const uint32_t dst = b_tile + core_offset128(j, seg0 * 8);
+        const uint16_t *src = rb[q4] ? rb[q4] + kc * kChunkCols + seg0 * 8 : nullptr;
+#pragma unroll
+        for (int sg = 0; sg < 8; ++sg) {
+          const bool valid = src != nullptr && kc * kChunkCols + (seg0 + sg) * 8 < v.Kc;
+          cp_async16(dst + sg * 128, valid ? src + sg * 8 : a.s.xh, valid ? 16u : 0u);
         }
       }
       cp_async_commit();
@@ -359,16 +412,17 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
 
 template <int PHASE>
 __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
-                           volatile int *abort_flag) {
+                           const ItemQueue &qu, volatile int *abort_flag) {
   if ((threadIdx.x & 31) != 0) return;
-  const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t ring = smem_u32(sm);
   const int S = L.slabs;
   RingPos pos;
   uint32_t b_seq = 0, a_seq = 0, item_seq = 0;
   bool ok = true;
-  for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+  for (uint32_t k = 0; ok; ++k) {
+    const int it = queue_read(qu, k, 1u, abort_flag, a.s.err);
+    if (it < 0) break;
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
     const uint32_t idesc = idesc_f16_f32(128, v.npad);
@@ -511,17 +565,18 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
 
 template <int PHASE>
 __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
-                            volatile int *abort_flag) {
+                            const ItemQueue &qu, volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, cg = warp >> 2;
-  const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t lut0 = lut_base(sm, L);
   RingPos pos;
   uint32_t a_seq = 0;
   int pending_ts = -1;
   LutSched ls;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
+    if (it < 0) break;
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
     if (!v.routed) {  // dense chunks: only the ring position moves
@@ -565,13 +620,15 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
 }
 
 template <int PHASE>
-__device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, volatile int *abort_flag) {
+__device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const ItemQueue &qu,
+                         volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const int n_items = a.s.n_items[PHASE - 1];
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   uint32_t item_seq = 0;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
+    if (it < 0) break;
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
     const int acs = item_seq % 2;
@@ -619,6 +676,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
+  __shared__ int queue_slot[kQueue];
   const int warp = threadIdx.x >> 5;
   const uint32_t bars = smem_u32(sm + L.bar_off);
   if (threadIdx.x == 0) {
@@ -642,6 +700,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kAE + i), kEpi);
     }
     mbar_init(bars + 8 * kDrain, 1);
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(bars + 8 * (kIQF + i), 1);
+      mbar_init(bars + 8 * (kIQE + i), kQueueReaders);
+    }
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -653,18 +715,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  const ItemQueue qu{queue_slot, bars};
   if (warp < kDq)
-    dequantiser<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+    dequantiser<PHASE>(a, L, sm, bars, tmem, qu, &abort_flag);
   else if (warp < kWarpP)
-    epilogue<PHASE>(a, bars, tmem, &abort_flag);
+    epilogue<PHASE>(a, bars, tmem, qu, &abort_flag);
   else if (warp == kWarpP)
-    weight_producer<PHASE>(a, L, sm, bars, &abort_flag);
+    weight_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
   else if (warp == kWarpAB)
-    ab_producer<PHASE>(a, L, sm, bars, &abort_flag);
+    ab_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
   else if (warp == kWarpMma)
-    mma_issuer<PHASE>(a, L, sm, bars, tmem, &abort_flag);
+    mma_issuer<PHASE>(a, L, sm, bars, tmem, qu, &abort_flag);
   else
-    lut_producer<PHASE>(a, L, sm, bars, &abort_flag);
+    lut_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {

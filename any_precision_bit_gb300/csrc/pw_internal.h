@@ -141,6 +141,7 @@ struct Scratch {
   double *stat_count;  // [L][E]
   double *stat_wsum;   // [L][E]
   int *err;            // [1] bounded-wait timeouts in the expert kernels (0 = none)
+  int *work;           // [2] next unclaimed work item of the two expert kernels (reset by the router)
   int max_items1, max_items2;
 };
 

@@ -441,7 +441,13 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
     a.s.stat_count[(size_t)a.layer * E + ee] += (double)s_cnt[ee];
     a.s.stat_wsum[(size_t)a.layer * E + ee] += (double)s_fsum[ee];
   }
-  if (tid == 0) *a.s.ticket = 0u;
+  if (tid == 0) {
+    *a.s.ticket = 0u;
+    if (a.s.work) {  // the expert kernels that follow claim their work items from zero
+      a.s.work[0] = 0;
+      a.s.work[1] = 0;
+    }
+  }
 }
 
 int launch_route(const FwdArgs &a, void *stream_) {
