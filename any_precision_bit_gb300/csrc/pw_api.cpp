@@ -303,7 +303,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
     block_shape(c, b.u, &b.N, &b.K);
     b.KC = kpad_cols(b.K) / kChunkCols;
     b.plane_bytes = (size_t)b.N * kpad_cols(b.K) / 8;
-    for (int bb = 1; bb <= 8; ++bb) b.lut_bytes[bb] = (size_t)b.N * (1u << bb) * 2;
+    for (int bb = 1; bb <= 8; ++bb) b.lut_bytes[bb] = (size_t)lut_dev_bytes(b.N, bb);  // device layout
     for (int p = 0; p < kMaxPlanes; ++p) b.state[p] = PW_PAGE_CPU;
     if (cudaEventCreateWithFlags(&b.ev, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
@@ -317,7 +317,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
     int N, K;
     block_shape(c, u, &N, &K);
     pmax = std::max(pmax, (size_t)N * kpad_cols(K) / 8);
-    pmax = std::max(pmax, (size_t)N * 256 * 2);
+    pmax = std::max(pmax, (size_t)lut_dev_bytes(N, 8));
   }
   c->poison_bytes = pmax;
   if (cudaMalloc(&c->poison, pmax) != cudaSuccess || cudaMemset(c->poison, 0xFF, pmax) != cudaSuccess) {
@@ -468,8 +468,9 @@ pw_status pw_pack(pw_ctx *c, int layer, int expert, int u, const uint8_t *idx, c
     c->packed_count[layer]--;
     b.packed = false;
   }
+  // the caller's LUTs: [N][2^b] fp16 per supported b, concatenated
   size_t lut_total = 0;
-  for (int i = 0; i < c->n_bits; ++i) lut_total += b.lut_bytes[c->bits[i]];
+  for (int i = 0; i < c->n_bits; ++i) lut_total += (size_t)b.N * (1u << c->bits[i]) * 2;
   const size_t idx_bytes = (size_t)b.N * b.K;
   const size_t idx_al = (idx_bytes + 255) & ~size_t(255);
   const size_t lut_al = (lut_total + 255) & ~size_t(255);
@@ -512,7 +513,7 @@ pw_status pw_pack(pw_ctx *c, int layer, int expert, int u, const uint8_t *idx, c
   for (int i = 0; i < c->n_bits; ++i) {
     const int bb = c->bits[i];
     const uint16_t *src = d_lut + off / 2;
-    off += b.lut_bytes[bb];
+    off += (size_t)b.N * (1u << bb) * 2;
     if (bb <= q_init) {
       b.dlut[bb] = dev_alloc_page(c, b.lut_bytes[bb]);
       if (!b.dlut[bb]) return fail(c, PW_ERR_OOM, "device pool exhausted packing block %d", id);

@@ -11,8 +11,10 @@
 //           low bytes and the high bytes of its centroids; byte permutes (prmt) look up four
 //           codes at a time and interleave the bytes into fp16 pairs.
 //   Q >= 5: an 8x8 bit transpose gives word s, byte e = the code (MSB-aligned) of column
-//           8 (s & 3) + 2e + (s >> 2).  One byte permute turns a code into the shared-memory
-//           address of its centroid in the row's LUT, and a 16-bit shared load fetches it.
+//           8 (s & 3) + 2e + (s >> 2).  The LUT is in shared memory in the tiled layout of
+//           lut_dev_index (pw_internal.h): the code is byte 1 of its entry's address, so one
+//           byte permute forms the address, every lane of a warp reads its own bank, and a
+//           second permute picks the row's half of each word.
 #pragma once
 #include <stdint.h>
 
@@ -109,30 +111,50 @@ __device__ __forceinline__ void codes_byte(const uint32_t (&W)[8], uint32_t (&Y)
   transpose8(Y);
 }
 
-// Q >= 5: centroids from the row's LUT in shared memory at row_addr (aligned to 2^(Q+1)
-// bytes; the table region is aligned to 512 bytes).
+// Shared-memory LUT of the tiled layout (lut_dev_index) as seen by one lane: `word0` is the
+// address of the lane's word for code 0 (table base + 128 (m >> 1) + 4 L for lane quarter m,
+// lane L; the table base is 64 KB-aligned, or 32 KB past that for a table of at most 128
+// codes), `half` selects the lane's row in each word (0x5410: low halves, 0x7632: high).
+struct LutLane {
+  uint32_t word0, half;
+};
+__device__ __forceinline__ LutLane lut_lane(uint32_t table, int quarter, int lane) {
+  return LutLane{table + 128u * (uint32_t)(quarter >> 1) + 4u * (uint32_t)lane, (quarter & 1) ? 0x7632u : 0x5410u};
+}
+__device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// Q <= 4: the lane's row of LUT_Q from shared memory as fp16 pairs P[i] = entries 2i, 2i+1.
 template <int Q>
-__device__ __forceinline__ void dq_byte(const uint32_t (&Y)[8], uint32_t row_addr, uint32_t (&v)[16]) {
-  if constexpr (Q <= 7) {
-    // byte e of Z = (code << 1) | the row's low address byte; its permute with the row
-    // address's upper bytes is the entry's address
-    const uint32_t rlo = (row_addr & 0xFFu) * 0x01010101u;
-    uint32_t Z[8];
+__device__ __forceinline__ void lut_pairs_smem(const LutLane &lu, uint32_t (&P)[8]) {
 #pragma unroll
-    for (int s = 0; s < 8; ++s) Z[s] = (Y[s] >> (7 - Q)) | rlo;
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        v[4 * s + e] = lds_pair(prmt(Z[s], row_addr, 0x7650u | e), prmt(Z[s + 4], row_addr, 0x7650u | e));
-  } else {
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        v[4 * s + e] = lds_pair(row_addr + (prmt(Y[s], 0u, 0x4440u + e) << 1),
-                                row_addr + (prmt(Y[s + 4], 0u, 0x4440u + e) << 1));
+  for (int i = 0; i < 8; ++i) {
+    P[i] = 0u;
+    if (2 * i + 1 < (1 << Q))
+      P[i] = prmt(lds_b32(lu.word0 + 512u * i), lds_b32(lu.word0 + 512u * i + 256u), lu.half);
   }
+}
+
+// Q >= 5: centroids from the lane's LUT in shared memory.
+template <int Q>
+__device__ __forceinline__ void dq_byte(const uint32_t (&Y)[8], const LutLane &lu, uint32_t (&v)[16]) {
+  // byte e of Z = the code (LSB-aligned) | byte 1 of the lane's word address; a permute with
+  // the address's other bytes is the entry's word address
+  const uint32_t hib = ((lu.word0 >> 8) & 0xFFu) * 0x01010101u;
+  uint32_t Z[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) Z[s] = (Y[s] >> (8 - Q)) | hib;
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t lo = lds_b32(prmt(Z[s], lu.word0, 0x7604u | ((uint32_t)e << 4)));
+      const uint32_t hi = lds_b32(prmt(Z[s + 4], lu.word0, 0x7604u | ((uint32_t)e << 4)));
+      v[4 * s + e] = prmt(lo, hi, lu.half);
+    }
 }
 
 // code of column c (0..31) of the group, from the outputs of codes_nib / codes_byte

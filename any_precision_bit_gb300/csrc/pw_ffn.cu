@@ -52,12 +52,11 @@ constexpr int kWarpMma = kWarpP + 2;        // MMA issuer, tensor-memory owner
 constexpr int kWarpLut = kWarpP + 3;        // LUT producer
 constexpr int kTcThreads = (kWarpLut + 1) * 32;
 constexpr int kSlab = kCtaRows * 16;        // 2 KB: one plane of a 128-row tile and 128 columns
-constexpr int kMaxSlabs = 64;               // slab ring size cap (even)
 constexpr int kRing = 16;                   // chunks in flight (full/empty barrier pairs)
 constexpr int kQueue = 8;                   // claimed work items published to the roles
 constexpr int kQueueReaders = kDq + kEpi + 3;  // warps that read the queue (all but the weight producer)
 constexpr int kAStages = 4;                 // tensor-memory A buffers
-constexpr int kBStages = 3;                 // activation tiles
+constexpr int kBStages = 3;                 // activation tiles (at most)
 constexpr int kDenseSlabs = 16;             // a dense 32 KB A tile: 8 pieces of 2 slabs
 constexpr int kLutSlot = 32 * 1024;         // LUT slot (q <= 7); q = 8 takes both slots
 constexpr int kAccCols = 64;                // tensor-memory columns per accumulator buffer
@@ -67,15 +66,25 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long kSpinLimit = 1L << 22;
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
+// Shared-memory map.  The host fills npad_max, b_bytes, bstages and smem (the dynamic size);
+// the kernel places the regions by absolute shared address: the activation ring, the
+// mbarriers and the item queue at the start of the dynamic area, the two LUT slots at
+// [64 KB, 128 KB) (the tiled LUT layout needs a 64 KB-aligned table), and the slab ring from
+// 128 KB to the end.
 struct TcLayout {
   int npad_max;    // B tile rows (tokens padded to 16)
   int b_bytes;     // one activation tile
+  int bstages;     // activation tiles in the ring (<= kBStages)
+  int smem;        // dynamic shared memory of the launch
+  // filled in by the kernel, offsets from the dynamic area
   int slabs;       // slab ring size (even)
-  int b_off;       // offset of the activation ring
-  int lut_off;     // LUT region (+512 bytes for alignment)
+  int ring_off;    // slab ring
+  int b_off;       // activation ring
+  int lut_off;     // LUT slots
   int bar_off;     // mbarriers
-  int smem;        // total dynamic shared memory
 };
+constexpr uint32_t kLutAddr = 64 * 1024;
+constexpr uint32_t kRingAddr = 128 * 1024;
 
 // mbarrier indices
 enum {
@@ -136,7 +145,7 @@ __device__ __forceinline__ const uint16_t *act_row(const FwdArgs &a, const ItemV
 }
 
 __device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const TcLayout &L) {
-  return (smem_u32(sm) + L.lut_off + 511u) & ~511u;
+  return smem_u32(sm) + (uint32_t)L.lut_off;
 }
 
 // LUT slot schedule, replayed identically by the weight producer and the dequantising warps:
@@ -241,7 +250,7 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
                                 const ItemQueue &qu, volatile int *abort_flag) {
   const int lane = threadIdx.x & 31;
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  const uint32_t ring = smem_u32(sm);
+  const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
   const int S = L.slabs;
   const int n_items = a.s.n_items[PHASE - 1];
   RingPos pos;
@@ -332,7 +341,7 @@ __device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, u
     const WorkItem w = items[it];
     if (w.kind != 0) continue;
     const BlockDev *bd = &a.table[(a.layer * a.E + w.expert) * 2 + (PHASE - 1)];
-    const int q = bd->q, nr = tile_rows(w.tile, bd->N);
+    const int q = bd->q;
     bool both;
     const int slot = ls.next(q, both);
     bool ok = wait_bar(bars + 8 * (kLE + slot), (ls.uses[slot] & 1) ^ 1, abort_flag, a.s.err);
@@ -340,9 +349,9 @@ __device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, u
     if (!ok) break;
     ++ls.uses[slot];
     if (both) ++ls.uses[1];
-    const uint32_t lbytes = (uint32_t)nr << q << 1;
+    const uint32_t lbytes = (uint32_t)lut_tile_bytes(q);
     mbar_arrive_expect_tx(bars + 8 * (kLF + slot), lbytes);
-    bulk_g2s(lut0 + slot * kLutSlot, bd->lut[q] + ((size_t)w.tile * kCtaRows << q), lbytes, bars + 8 * (kLF + slot));
+    bulk_g2s(lut0 + slot * kLutSlot, bd->lut[q] + (size_t)w.tile * (lbytes / 2), lbytes, bars + 8 * (kLF + slot));
     ++ls.fills[slot];
   }
   for (int s = 0; s < 2; ++s)
@@ -353,10 +362,10 @@ __device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, u
 // through the async proxy.  So each lane waits for its own copies of a chunk, fences them to
 // the async proxy, and only then does lane 0 release the tile, one chunk behind the copies
 // in flight so that their latency stays hidden.
-__device__ __forceinline__ void release_b(uint32_t bars, uint32_t seq, int lane) {
+__device__ __forceinline__ void release_b(uint32_t bars, uint32_t seq, int lane, int bstages) {
   fence_async_smem();
   __syncwarp();
-  if (lane == 0) mbar_arrive(bars + 8 * (kBF + seq % kBStages));
+  if (lane == 0) mbar_arrive(bars + 8 * (kBF + seq % bstages));
 }
 
 template <int PHASE>
@@ -380,8 +389,8 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       rb[q4] = j < v.ntok ? act_row<PHASE>(a, v, j) : nullptr;
     }
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int bs = b_seq % kBStages;
-      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / kBStages) & 1) ^ 1, abort_flag, a.s.err);
+      const int bs = b_seq % L.bstages;
+      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / L.bstages) & 1) ^ 1, abort_flag, a.s.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t b_tile = smem_u32(sm) + L.b_off + bs * L.b_bytes;
@@ -400,14 +409,14 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       cp_async_commit();
       if (b_seq > 0) {  // the previous chunk's copies: landed, fenced, released
         cp_async_wait<1>();
-        release_b(bars, b_seq - 1, lane);
+        release_b(bars, b_seq - 1, lane, L.bstages);
       }
       ++b_seq;
     }
   }
   // the last chunk (also on the way out after an abort: nothing may be left in flight)
   cp_async_wait<0>();
-  if (b_seq > 0) release_b(bars, b_seq - 1, lane);
+  if (b_seq > 0) release_b(bars, b_seq - 1, lane, L.bstages);
 }
 
 template <int PHASE>
@@ -415,7 +424,7 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
                            const ItemQueue &qu, volatile int *abort_flag) {
   if ((threadIdx.x & 31) != 0) return;
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  const uint32_t ring = smem_u32(sm);
+  const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
   const int S = L.slabs;
   RingPos pos;
   uint32_t b_seq = 0, a_seq = 0, item_seq = 0;
@@ -436,12 +445,12 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
       const uint32_t c = pos.c;
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
-      const int bs = b_seq % kBStages, ts = a_seq % kAStages;
+      const int bs = b_seq % L.bstages, ts = a_seq % kAStages;
       if (v.routed)
         ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / kAStages) & 1, abort_flag, a.s.err);
       else
         ok = wait_bar(wf_bar(bars, false, seq), (seq / kRing) & 1, abort_flag, a.s.err);
-      if (ok) ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / kBStages) & 1, abort_flag, a.s.err);
+      if (ok) ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / L.bstages) & 1, abort_flag, a.s.err);
       if (!ok) break;
       tc_fence_after();
       const uint32_t b0 = smem_u32(sm) + L.b_off + bs * L.b_bytes;
@@ -494,33 +503,14 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   const int r = 32 * quarter + lane;
   const bool rv = r < v.nr;
   const int S = L.slabs;
+  const LutLane lu = lut_lane(lut_slot, quarter, lane);
   LutRegs Lr;
-  uint32_t row_addr = 0;
   if constexpr (Q <= 4) {
     uint32_t P[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) P[i] = 0u;
-    if (rv) {
-      const uint32_t la = lut_slot + ((uint32_t)r << (Q + 1));
-      if constexpr (Q == 4) {
-        const uint4 x0 = lds128(la), x1 = lds128(la + 16);
-        P[0] = x0.x; P[1] = x0.y; P[2] = x0.z; P[3] = x0.w;
-        P[4] = x1.x; P[5] = x1.y; P[6] = x1.z; P[7] = x1.w;
-      } else if constexpr (Q == 3) {
-        const uint4 x0 = lds128(la);
-        P[0] = x0.x; P[1] = x0.y; P[2] = x0.z; P[3] = x0.w;
-      } else if constexpr (Q == 2) {
-        P[0] = lds32(la);
-        P[1] = lds32(la + 4);
-      } else {
-        P[0] = lds32(la);
-      }
-    }
+    lut_pairs_smem<Q>(lu, P);
     lut_regs(P, Lr);
-  } else {
-    row_addr = lut_slot + ((uint32_t)r << (Q + 1));
   }
-  const uint32_t ring = smem_u32(sm) + (uint32_t)(cg * v.nr + r) * 4;
+  const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off + (uint32_t)(cg * v.nr + r) * 4;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
   uint32_t v16[16];
   for (int kc = w.kc0; kc < w.kc1; ++kc) {
@@ -549,7 +539,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
       uint32_t Y[8];
       codes_byte<Q>(W, Y);
       flush_store(bars, pending_ts, lane);
-      dq_byte<Q>(Y, row_addr, v16);
+      dq_byte<Q>(Y, lu, v16);
     }
     if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
     tc_fence_after();
@@ -678,6 +668,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   __shared__ uint32_t tmem_slot;
   __shared__ int queue_slot[kQueue];
   const int warp = threadIdx.x >> 5;
+  {  // regions by absolute shared address (see TcLayout)
+    const uint32_t base = smem_u32(sm);
+    L.b_off = 0;
+    L.bar_off = L.bstages * L.b_bytes;
+    L.lut_off = (int)(kLutAddr - base);
+    L.ring_off = (int)(kRingAddr - base);
+    L.slabs = ((L.smem - L.ring_off) / kSlab) & ~1;
+    if (base >= kLutAddr || L.bar_off + kNumBars * 8 > L.lut_off || L.slabs < 2 * kDenseSlabs + 2) {
+      if (threadIdx.x == 0) atomicExch(a.s.err, 3);  // the map does not fit this launch
+      return;
+    }
+  }
   const uint32_t bars = smem_u32(sm + L.bar_off);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kTAF + i), kDq);
       mbar_init(bars + 8 * (kTAE + i), 1);
     }
-    for (int i = 0; i < kBStages; ++i) {
+    for (int i = 0; i < L.bstages; ++i) {
       mbar_init(bars + 8 * (kBF + i), 1);  // lane 0 of the activation producer
       mbar_init(bars + 8 * (kBE + i), 1);
     }
@@ -740,18 +742,14 @@ static TcLayout tc_layout(const FwdArgs &a) {
   TcLayout L{};
   L.npad_max = max(16, (min(a.T, kTokChunk) + 15) / 16 * 16);
   L.b_bytes = L.npad_max * kChunkCols * 2;
-  const int fixed = kBStages * L.b_bytes + 2 * kLutSlot + 512 + kNumBars * 8;
-  L.slabs = min(kMaxSlabs, (kSmemLimit - fixed) / kSlab) & ~1;
-  L.b_off = L.slabs * kSlab;
-  L.lut_off = L.b_off + kBStages * L.b_bytes;
-  L.bar_off = L.lut_off + 2 * kLutSlot + 512;
-  L.smem = L.bar_off + kNumBars * 8;
+  L.bstages = kBStages;
+  L.smem = kSmemLimit;
   return L;
 }
 
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
   const TcLayout L = tc_layout(a);
-  if (L.smem > kSmemLimit || L.slabs < 2 * kDenseSlabs) return (int)cudaErrorInvalidConfiguration;
+  if (L.bstages * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
   cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

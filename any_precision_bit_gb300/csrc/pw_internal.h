@@ -91,6 +91,22 @@ PW_HD void tile_pos(int d, int k, int N, int KC, long *word, int *bit) {
   *bit = 4 * i + j;
 }
 
+// Kernel-private LUT layout of one bitwidth b of a block: per 128-row tile (the last tile
+// zero-padded to 128 rows), 2^b codes of 256 bytes each; inside a code's 256 bytes, 32-bit
+// word (qp * 32 + L) (qp = 0, 1; L = 0..31) holds in its low half the centroid of row
+// 64 qp + L and in its high half that of row 64 qp + 32 + L.  A warp that owns the 32 rows
+// 32 m + L (a tensor-memory lane quarter m) thus reads one word per lane, every lane in its
+// own bank, and the code of an entry is byte 1 of its address relative to a 64 KB-aligned
+// table base.
+PW_HD long lut_tile_bytes(int b) { return 256L << b; }
+PW_HD long lut_dev_bytes(int N, int b) { return (long)((N + kCtaRows - 1) / kCtaRows) * lut_tile_bytes(b); }
+// element index (uint16) of (device row d, code c) in that layout
+PW_HD long lut_dev_index(int d, int c, int b) {
+  const int ct = d / kCtaRows, r = d % kCtaRows;
+  const int m = r / 32, L = r % 32;
+  return ct * (lut_tile_bytes(b) / 2) + ((long)c * 64 + (m >> 1) * 32 + L) * 2 + (m & 1);
+}
+
 // Operand tiles of the tensor-core MMAs are stored as 8x8 "core matrices" of fp16 (128
 // contiguous bytes, row i at byte 16 i); in a tile of R rows by 128 columns, core matrix
 // (row group rg, column group kc) sits at byte (rg * 16 + kc) * 128.

@@ -139,18 +139,29 @@ int launch_pack(const uint8_t *idx, int N, int K, int KC, int u, int I, int bmax
   return (int)cudaGetLastError();
 }
 
-__global__ void lut_permute_kernel(const uint16_t *in, int N, int entries, int u, int I, uint16_t *out) {
-  long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (long)N * entries) return;
-  const int d = (int)(i / entries), c = (int)(i % entries);
-  out[i] = in[(size_t)orig_row(d, u, I) * entries + c];
+// LUT_b from the caller's [N][2^b] (original rows) to the kernel-private tiled layout
+// (lut_dev_index; rows of the padded last tile are zero).  One thread per output entry.
+__global__ void lut_permute_kernel(const uint16_t *in, int N, int b, int u, int I, uint16_t *out, long total) {
+  const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const long tile = lut_tile_bytes(b) / 2;
+  const int ct = (int)(i / tile);
+  const long rem = i % tile;
+  const int half = (int)(rem & 1);
+  const long word = rem >> 1;
+  const int c = (int)(word / 64), w64 = (int)(word % 64);
+  const int m = 2 * (w64 / 32) + half, L = w64 % 32;
+  const int d = ct * kCtaRows + 32 * m + L;
+  out[i] = d < N ? in[(size_t)orig_row(d, u, I) * (1 << b) + c] : (uint16_t)0;
 }
 
 int launch_lut_permute(const uint16_t *lut_in, int N, int entries, int u, int I, uint16_t *lut_out,
                        void *stream) {
-  const long n = (long)N * entries;
+  int b = 0;
+  while ((1 << b) < entries) ++b;
+  const long n = lut_dev_bytes(N, b) / 2;
   lut_permute_kernel<<<(unsigned)((n + 255) / 256), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
-      lut_in, N, entries, u, I, lut_out);
+      lut_in, N, b, u, I, lut_out, n);
   return (int)cudaGetLastError();
 }
 
@@ -174,7 +185,7 @@ int launch_frag16(const uint16_t *w_in, int N, int K, int u, int I, uint16_t *w_
 
 // Debug read-back through the forward's dequantisation code (pw_dq.cuh): one CTA per
 // (CTA tile, chunk), one thread per (column group, row); the tile's LUT is staged in shared
-// memory as in the expert kernels.
+// memory at a 64 KB-aligned address as in the expert kernels.
 template <int Q>
 __device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, int u, int I, uint32_t lut_s,
                              uint8_t *idx_out, uint16_t *w_out) {
@@ -184,17 +195,12 @@ __device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, 
 #pragma unroll
   for (int p = 0; p < 8; ++p) W[p] = p < Q ? bd.plane[p][w0] : 0u;
   const int d = ct * kCtaRows + r;
+  const LutLane lu = lut_lane(lut_s, r / 32, r % 32);
   uint32_t v[16], codes[32];
   if constexpr (Q <= 4) {
-    uint32_t S[4];
+    uint32_t S[4], P[8];
     codes_nib<Q>(W, S);
-    uint32_t P[8];
-    const uint16_t *lr = bd.lut[Q] + (size_t)d * (1 << Q);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const uint32_t a0 = 2 * i < (1 << Q) ? lr[2 * i] : 0u, a1 = 2 * i + 1 < (1 << Q) ? lr[2 * i + 1] : 0u;
-      P[i] = a0 | (a1 << 16);
-    }
+    lut_pairs_smem<Q>(lu, P);
     LutRegs L;
     lut_regs(P, L);
     dq_nib<Q>(S, L, v);
@@ -203,7 +209,7 @@ __device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, 
   } else {
     uint32_t Y[8];
     codes_byte<Q>(W, Y);
-    dq_byte<Q>(Y, lut_s + ((uint32_t)r << (Q + 1)), v);
+    dq_byte<Q>(Y, lu, v);
 #pragma unroll
     for (int c = 0; c < 32; ++c) codes[c] = code_byte<Q>(Y, c);
   }
@@ -217,40 +223,42 @@ __device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, 
   }
 }
 
+constexpr int kUnpackSmem = 128 * 1024;  // a 64 KB-aligned 64 KB window inside
+
 __global__ void __launch_bounds__(512) unpack_kernel(const BlockDev *table, int block, int b, int u, int I,
                                                      uint8_t *idx_out, uint16_t *w_out) {
-  extern __shared__ __align__(512) uint8_t lut_smem[];
+  extern __shared__ __align__(1024) uint8_t lut_smem[];
   const BlockDev &bd = table[block];
   const int ct = blockIdx.x, kc = blockIdx.y;
   const int nr = tile_rows(ct, bd.N);
   const int cg = threadIdx.x / kCtaRows, r = threadIdx.x % kCtaRows;
-  if (b >= 5) {  // stage the tile's LUT rows as the expert kernels do
-    const int n16 = nr * (1 << b) / 8;
-    const uint4 *src = reinterpret_cast<const uint4 *>(bd.lut[b] + (size_t)ct * kCtaRows * (1 << b));
-    for (int i = threadIdx.x; i < n16; i += blockDim.x) reinterpret_cast<uint4 *>(lut_smem)[i] = src[i];
+  const uint32_t lut_s = (smem_u32(lut_smem) + 65535u) & ~65535u;
+  {  // stage the tile's LUT as the expert kernels do
+    const int n16 = (int)(lut_tile_bytes(b) / 16);
+    const uint4 *src = reinterpret_cast<const uint4 *>(bd.lut[b] + ct * (lut_tile_bytes(b) / 2));
+    uint4 *dst = reinterpret_cast<uint4 *>(lut_smem + (lut_s - smem_u32(lut_smem)));
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
   }
   __syncthreads();
   if (r >= nr) return;
-  const uint32_t ls = smem_u32(lut_smem);
   switch (b) {
-    case 1: unpack_group<1>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    case 2: unpack_group<2>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    case 3: unpack_group<3>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    case 4: unpack_group<4>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    case 5: unpack_group<5>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    case 6: unpack_group<6>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    case 7: unpack_group<7>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
-    default: unpack_group<8>(bd, ct, kc, cg, r, u, I, ls, idx_out, w_out); break;
+    case 1: unpack_group<1>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    case 2: unpack_group<2>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    case 3: unpack_group<3>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    case 4: unpack_group<4>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    case 5: unpack_group<5>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    case 6: unpack_group<6>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    case 7: unpack_group<7>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
+    default: unpack_group<8>(bd, ct, kc, cg, r, u, I, lut_s, idx_out, w_out); break;
   }
 }
 
 int launch_unpack(const BlockDev *table, int block, int b, int u, int I, int N, int KC, uint8_t *idx_out,
                   uint16_t *w_out, void *stream) {
-  const int smem = b >= 5 ? kCtaRows * (1 << b) * 2 : 0;
-  cudaFuncSetAttribute(unpack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCtaRows * 256 * 2);
+  cudaFuncSetAttribute(unpack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUnpackSmem);
   dim3 grid((N + kCtaRows - 1) / kCtaRows, KC);
-  unpack_kernel<<<grid, 4 * kCtaRows, smem, reinterpret_cast<cudaStream_t>(stream)>>>(table, block, b, u, I,
-                                                                                      idx_out, w_out);
+  unpack_kernel<<<grid, 4 * kCtaRows, kUnpackSmem, reinterpret_cast<cudaStream_t>(stream)>>>(table, block, b, u, I,
+                                                                                             idx_out, w_out);
   return (int)cudaGetLastError();
 }
 
