@@ -6,11 +6,11 @@
 // Input: the Q words W[p] (plane p) of one row and one 32-column group, in the nibble-major
 // bit order of the plane tiling (bit 4 i + j holds column 8 j + i).  Output: 16 registers
 // v[t], t = 0..15, each the fp16 centroids of columns 2t (low half) and 2t + 1 (high half).
-//   Q <= 4: a 4x4 bit transpose across the planes gives word j = the 4-bit codes of columns
+//   Q <= kRegLutMaxQ: a 4x4 bit transpose across the planes gives word j = the 4-bit codes of columns
 //           8j..8j+7 (column 8j + i in nibble i).  The row's LUT sits in registers as the
 //           low bytes and the high bytes of its centroids; byte permutes (prmt) look up four
 //           codes at a time and interleave the bytes into fp16 pairs.
-//   Q >= 5: an 8x8 bit transpose gives word s, byte e = the code (MSB-aligned) of column
+//   wider: an 8x8 bit transpose gives word s, byte e = the code (MSB-aligned) of column
 //           8 (s & 3) + 2e + (s >> 2).  The LUT is in shared memory in the tiled layout of
 //           lut_dev_index (pw_internal.h): the code is byte 1 of its entry's address, so one
 //           byte permute forms the address, every lane of a warp reads its own bank, and a
@@ -21,6 +21,11 @@
 #include "pw_device.cuh"
 
 namespace pw {
+
+// Widths up to this one look centroids up in registers (byte permutes); wider ones in the
+// shared-memory LUT.  At 4 bits the shared-memory path is the faster one: the register path
+// needs a second level of permutes to pick between two 8-entry halves.
+constexpr int kRegLutMaxQ = 3;
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;

@@ -66,7 +66,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr long kSpinLimit = 1L << 22;
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
-// Shared-memory map.  The host fills npad_max, b_bytes, bstages and smem (the dynamic size);
+// Shared-memory map.  The host fills npad_max, b_bytes and smem (the dynamic size);
 // the kernel places the regions by absolute shared address: the activation ring, the
 // mbarriers and the item queue at the start of the dynamic area, the two LUT slots at
 // [64 KB, 128 KB) (the tiled LUT layout needs a 64 KB-aligned table), and the slab ring from
@@ -74,7 +74,6 @@ constexpr int kSmemLimit = 227 * 1024 - 1024;
 struct TcLayout {
   int npad_max;    // B tile rows (tokens padded to 16)
   int b_bytes;     // one activation tile
-  int bstages;     // activation tiles in the ring (<= kBStages)
   int smem;        // dynamic shared memory of the launch
   // filled in by the kernel, offsets from the dynamic area
   int slabs;       // slab ring size (even)
@@ -389,8 +388,8 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       rb[q4] = j < v.ntok ? act_row<PHASE>(a, v, j) : nullptr;
     }
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int bs = b_seq % L.bstages;
-      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / L.bstages) & 1) ^ 1, abort_flag, a.s.err);
+      const int bs = b_seq % kBStages;
+      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / kBStages) & 1) ^ 1, abort_flag, a.s.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       const uint32_t b_tile = smem_u32(sm) + L.b_off + bs * L.b_bytes;
@@ -409,14 +408,14 @@ __device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       cp_async_commit();
       if (b_seq > 0) {  // the previous chunk's copies: landed, fenced, released
         cp_async_wait<1>();
-        release_b(bars, b_seq - 1, lane, L.bstages);
+        release_b(bars, b_seq - 1, lane, kBStages);
       }
       ++b_seq;
     }
   }
   // the last chunk (also on the way out after an abort: nothing may be left in flight)
   cp_async_wait<0>();
-  if (b_seq > 0) release_b(bars, b_seq - 1, lane, L.bstages);
+  if (b_seq > 0) release_b(bars, b_seq - 1, lane, kBStages);
 }
 
 template <int PHASE>
@@ -445,12 +444,12 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
       const uint32_t c = pos.c;
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
-      const int bs = b_seq % L.bstages, ts = a_seq % kAStages;
+      const int bs = b_seq % kBStages, ts = a_seq % kAStages;
       if (v.routed)
         ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / kAStages) & 1, abort_flag, a.s.err);
       else
         ok = wait_bar(wf_bar(bars, false, seq), (seq / kRing) & 1, abort_flag, a.s.err);
-      if (ok) ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / L.bstages) & 1, abort_flag, a.s.err);
+      if (ok) ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / kBStages) & 1, abort_flag, a.s.err);
       if (!ok) break;
       tc_fence_after();
       const uint32_t b0 = smem_u32(sm) + L.b_off + bs * L.b_bytes;
@@ -505,7 +504,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   const int S = L.slabs;
   const LutLane lu = lut_lane(lut_slot, quarter, lane);
   LutRegs Lr;
-  if constexpr (Q <= 4) {
+  if constexpr (Q <= kRegLutMaxQ) {
     uint32_t P[8];
     lut_pairs_smem<Q>(lu, P);
     lut_regs(P, Lr);
@@ -530,7 +529,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
     // tcgen05.st reads its source registers asynchronously: the previous chunk's store must
     // be complete (flush_store) before v16 is rewritten; the plane loads and the bit
     // transpose of this chunk overlap it
-    if constexpr (Q <= 4) {
+    if constexpr (Q <= kRegLutMaxQ) {
       uint32_t S4[4];
       codes_nib<Q>(W, S4);
       flush_store(bars, pending_ts, lane);
@@ -671,7 +670,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   {  // regions by absolute shared address (see TcLayout)
     const uint32_t base = smem_u32(sm);
     L.b_off = 0;
-    L.bar_off = L.bstages * L.b_bytes;
+    L.bar_off = kBStages * L.b_bytes;
     L.lut_off = (int)(kLutAddr - base);
     L.ring_off = (int)(kRingAddr - base);
     L.slabs = ((L.smem - L.ring_off) / kSlab) & ~1;
@@ -691,7 +690,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kTAF + i), kDq);
       mbar_init(bars + 8 * (kTAE + i), 1);
     }
-    for (int i = 0; i < L.bstages; ++i) {
+    for (int i = 0; i < kBStages; ++i) {
       mbar_init(bars + 8 * (kBF + i), 1);  // lane 0 of the activation producer
       mbar_init(bars + 8 * (kBE + i), 1);
     }
@@ -742,14 +741,13 @@ static TcLayout tc_layout(const FwdArgs &a) {
   TcLayout L{};
   L.npad_max = max(16, (min(a.T, kTokChunk) + 15) / 16 * 16);
   L.b_bytes = L.npad_max * kChunkCols * 2;
-  L.bstages = kBStages;
   L.smem = kSmemLimit;
   return L;
 }
 
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
   const TcLayout L = tc_layout(a);
-  if (L.bstages * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
+  if (kBStages * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
   cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -197,7 +197,7 @@ __device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, 
   const int d = ct * kCtaRows + r;
   const LutLane lu = lut_lane(lut_s, r / 32, r % 32);
   uint32_t v[16], codes[32];
-  if constexpr (Q <= 4) {
+  if constexpr (Q <= kRegLutMaxQ) {
     uint32_t S[4], P[8];
     codes_nib<Q>(W, S);
     lut_pairs_smem<Q>(lu, P);
