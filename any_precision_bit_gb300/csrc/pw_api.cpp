@@ -1,6 +1,7 @@
 // pw_api.cpp -- host runtime behind include/pw.h: context, weight page table, page pools,
 // packing, forward dispatch (with CUDA-graph replay of the layer stack) and the
 // asynchronous offload / reload protocol of PagedWeight Sec. 3.1 and Sec. 3.3.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -19,6 +20,34 @@ using namespace pw;
 namespace {
 
 thread_local std::string g_thread_err;
+
+// 2-D fp16 tensor map over a row-major [rows][cols] buffer: boxes of 64 columns (128 bytes)
+// by 128 rows with the 128-byte swizzle, out-of-range elements read as zero.  The encoder is
+// the driver's, looked up through the runtime (no link-time dependency on the driver library).
+bool encode_act_map(TmaDesc *out, void *base, long rows, long cols) {
+  using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Encode fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p) {
+      cudaGetLastError();
+      return false;
+    }
+    fn = reinterpret_cast<Encode>(p);
+  }
+  static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "tensor map size");
+  const cuuint64_t dim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t stride[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estride[2] = {1, 1};
+  return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dim, stride, box, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 // ------------------------------------------------------------------ page pools
 // Size-class free lists over large reservations.  Pages of one block type all have the
@@ -138,6 +167,8 @@ struct pw_ctx {
   void *stage = nullptr;  // device staging for packing / inspection
   size_t stage_bytes = 0;
   void *xdev = nullptr;   // device activations of pw_stack_forward_host
+  BMaps bmaps{};          // prefill tensor maps (valid when has_bmaps)
+  bool has_bmaps = false;
   std::vector<GraphEntry> graphs;
   std::string err;
   int sticky = 0;
@@ -374,9 +405,20 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.stat_count, sizeof(double) * d.L * d.E) &&
             salloc((void **)&c->s.stat_wsum, sizeof(double) * d.L * d.E) &&
             salloc(&c->xdev, sizeof(uint16_t) * Tm * d.H);
+  if (ok && Tm >= kPrefillMinT) ok = salloc((void **)&c->s.xs, sizeof(uint16_t) * TK * d.H);
   if (!ok) {
     fail(nullptr, PW_ERR_OOM, "scratch allocation failed (max_tokens=%d)", d.max_tokens);
     return bail(PW_ERR_OOM);
+  }
+  if (c->s.xs) {
+    const bool enc = encode_act_map(&c->bmaps.xs, c->s.xs, TK, d.H) && encode_act_map(&c->bmaps.xh, c->s.xh, Tm, d.H) &&
+                     encode_act_map(&c->bmaps.h_routed, c->s.h_routed, TK, d.I) &&
+                     (d.Is == 0 || encode_act_map(&c->bmaps.h_shared, c->s.h_shared, Tm, d.Is));
+    if (!enc) {
+      fail(nullptr, PW_ERR_CUDA, "tensor map encoding failed");
+      return bail(PW_ERR_CUDA);
+    }
+    c->has_bmaps = true;
   }
   cudaMemset(c->s.ticket, 0, sizeof(unsigned) * (1 + (Tm + 7) / 8));
   cudaMemset(c->s.err, 0, sizeof(int));
@@ -623,6 +665,7 @@ static pw_status forward_args(pw_ctx *c, int layer, const void *x, int T, void *
   a->ids_out = ids;
   a->w_out = w;
   a->sm_count = c->sm_count;
+  a->bmaps = c->has_bmaps ? &c->bmaps : nullptr;
   return PW_OK;
 }
 

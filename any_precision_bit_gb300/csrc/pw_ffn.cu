@@ -6,9 +6,12 @@
 // output goes through SiLU(gate)*up ("expert activation"), and the down projection follows.
 // The shared expert of the layer (Table 1) rides in the same launches.
 //
-// A work item is a 128-row tile of one block times up to 64 tokens: D[128][N] = W x X^T,
-// N = tokens padded to 16, accumulated in tensor memory.  One persistent CTA per SM, warp-
-// specialised:
+// A work item is a 128-row tile of one block times up to TOK tokens: D[128][N] = W x X^T,
+// N = tokens padded to 16, accumulated in tensor memory.  TOK = 64 at decode batch sizes; for
+// prefill-sized batches TOK = 128, so that each dequantised weight tile feeds twice the
+// tokens (the accumulators then fill half of tensor memory, and the activation tiles are
+// split along K into two 64-column stages to fit shared memory).  One persistent CTA per SM,
+// warp-specialised:
 //   * LUT producer (1 warp): per routed item the tile's LUT_q rows (one TMA bulk copy) into
 //     one of two LUT slots, so that the next item's table loads while this one runs (a q = 8
 //     table takes both);
@@ -19,9 +22,12 @@
 //     the q bit-plane slabs of a routed chunk (lane p copies plane p) or the eight 4 KB K-step
 //     pieces of a dense shared-expert tile (lane t copies piece t).  A chunk takes exactly the
 //     bytes it needs, so low bitwidths keep more chunks in flight;
-//   * activation producer (1 warp): the tokens' fp16 rows (16-byte cp.async gathers) into the
-//     B operand tile, a 3-deep ring; each lane fences its landed copies to the async proxy
-//     before the tile is released to the MMA thread;
+//   * activation producer (1 warp): the B operand tiles, a ring of 16 KB stages.  Decode
+//     tiling: the tokens' fp16 rows gathered with 16-byte cp.async copies, each lane fencing
+//     its landed copies to the async proxy before the tile is released to the MMA thread.
+//     Prefill tiling: one TMA box (128 rows x 64 columns, 128-byte swizzle) per stage from
+//     row-contiguous buffers (the layer input gathered into slot order beforehand, h, the
+//     shared expert's input and h);
 //   * dequantising warps (16, four per tensor-memory lane quarter): each thread owns one row
 //     and 32 columns of the chunk, turns its plane words into fp16 centroids (pw_dq.cuh) and
 //     writes them straight into tensor memory (tcgen05.st), a 4-deep ring of A buffers;
@@ -56,29 +62,56 @@ constexpr int kRing = 16;                   // chunks in flight (full/empty barr
 constexpr int kQueue = 8;                   // claimed work items published to the roles
 constexpr int kQueueReaders = kDq + kEpi + 3;  // warps that read the queue (all but the weight producer)
 constexpr int kAStages = 4;                 // tensor-memory A buffers
-constexpr int kBStages = 3;                 // activation tiles (at most)
+constexpr int kBStagesMax = 6;              // activation stages (at most)
+constexpr int kBLow = 3;                    // activation stages below the LUT slots
 constexpr int kDenseSlabs = 16;             // a dense 32 KB A tile: 8 pieces of 2 slabs
 constexpr int kLutSlot = 32 * 1024;         // LUT slot (q <= 7); q = 8 takes both slots
-constexpr int kAccCols = 64;                // tensor-memory columns per accumulator buffer
 constexpr int kACols = kChunkCols / 2;      // tensor-memory columns per A buffer (fp16 pairs)
-constexpr uint32_t kAColBase = 2 * kAccCols;
 constexpr uint32_t kTmemCols = 512;
+
+// The token tiling of a launch.  Tensor memory: two accumulator buffers of TOK fp32 columns,
+// then the kAStages A buffers (2 TOK + 4 * 64 <= 512 columns).  Activation stages: TOK rows
+// by kBK columns (16 KB at most), kBK / 16 MMA K-steps each.  Decode: core-matrix layout
+// written by cp.async, the producer one stage of copies ahead of its releases.  Prefill:
+// 128-byte swizzled layout written by TMA (kTma).
+template <int TOK>
+struct Tiling {
+  static_assert(TOK == 64 || TOK == 128, "token tile");
+  static constexpr bool kTma = TOK == 128;
+  static constexpr int kAccCols = TOK;
+  static constexpr uint32_t kAColBase = 2 * TOK;
+  static constexpr int kBK = TOK == 64 ? kChunkCols : kChunkCols / 2;
+  static constexpr int kBPieces = kChunkCols / kBK;  // activation stages per chunk
+  static constexpr int kBSteps = kBK / 16;           // MMA K-steps per activation stage
+  static constexpr int kBStages = TOK == 64 ? 3 : 6;
+  static constexpr int kBSlots = kBStages / kBPieces;  // per-chunk slots (one full/empty barrier pair each)
+  static constexpr int kBInFlight = 1;                 // cp.async slots issued ahead of the releases
+  static constexpr uint32_t kTmaBytes = TOK * kBK * 2;  // one TMA box
+  // descriptor start-address step (16-byte units) of one 16-column K-step inside a stage
+  static constexpr uint32_t kDescStep = kTma ? 2u : 16u;
+  static_assert(!kTma || kBK * 2 == 128, "a TMA box row is one 128-byte swizzle row");
+  static_assert(kTma || kBPieces == 1, "the cp.async path fills one stage per chunk");
+  static_assert(kBInFlight < kBSlots, "a slot must be released before its reuse is awaited");
+  static_assert(kAColBase + kAStages * kACols <= kTmemCols, "tensor memory");
+  static_assert(kBStages <= kBStagesMax, "activation stages");
+};
 constexpr long kSpinLimit = 1L << 22;
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
 // Shared-memory map.  The host fills npad_max, b_bytes and smem (the dynamic size);
-// the kernel places the regions by absolute shared address: the activation ring, the
-// mbarriers and the item queue at the start of the dynamic area, the two LUT slots at
-// [64 KB, 128 KB) (the tiled LUT layout needs a 64 KB-aligned table), and the slab ring from
-// 128 KB to the end.
+// the kernel places the regions by absolute shared address: the first kBLow activation
+// stages and the mbarriers at the start of the dynamic area, the two LUT slots at
+// [64 KB, 128 KB) (the tiled LUT layout needs a 64 KB-aligned table), then the other
+// activation stages (prefill tiling), and the slab ring to the end.
 struct TcLayout {
   int npad_max;    // B tile rows (tokens padded to 16)
-  int b_bytes;     // one activation tile
+  int b_bytes;     // one activation stage
   int smem;        // dynamic shared memory of the launch
   // filled in by the kernel, offsets from the dynamic area
   int slabs;       // slab ring size (even)
   int ring_off;    // slab ring
-  int b_off;       // activation ring
+  int b_off;       // activation stages 0 .. kBLow - 1
+  int b_hi;        // activation stages kBLow ..
   int lut_off;     // LUT slots
   int bar_off;     // mbarriers
 };
@@ -88,7 +121,7 @@ constexpr uint32_t kRingAddr = 128 * 1024;
 // mbarrier indices
 enum {
   kWFR = 0, kWFD = kWFR + kRing, kWE = kWFD + kRing, kTAF = kWE + kRing, kTAE = kTAF + kAStages, kBF = kTAE + kAStages,
-  kBE = kBF + kBStages, kLF = kBE + kBStages, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
+  kBE = kBF + kBStagesMax, kLF = kBE + kBStagesMax, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
   kIQF = kDrain + 1, kIQE = kIQF + kQueue, kNumBars = kIQE + kQueue
 };
 
@@ -145,6 +178,9 @@ __device__ __forceinline__ const uint16_t *act_row(const FwdArgs &a, const ItemV
 
 __device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const TcLayout &L) {
   return smem_u32(sm) + (uint32_t)L.lut_off;
+}
+__device__ __forceinline__ uint32_t b_stage(const uint8_t *sm, const TcLayout &L, int s) {
+  return smem_u32(sm) + (uint32_t)(s < kBLow ? L.b_off + s * L.b_bytes : L.b_hi + (s - kBLow) * L.b_bytes);
 }
 
 // LUT slot schedule, replayed identically by the weight producer and the dequantising warps:
@@ -367,60 +403,115 @@ __device__ __forceinline__ void release_b(uint32_t bars, uint32_t seq, int lane,
   if (lane == 0) mbar_arrive(bars + 8 * (kBF + seq % bstages));
 }
 
-template <int PHASE>
-__device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
-                            const ItemQueue &qu, volatile int *abort_flag) {
-  const int lane = threadIdx.x & 31;
+// Prefill tiling: lane 0 loads each stage with one TMA box of the item's consecutive rows.
+template <int PHASE, int TOK>
+__device__ void ab_producer_tma(const FwdArgs &a, const BMaps &bm, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                                const ItemQueue &qu, volatile int *abort_flag) {
+  using T_ = Tiling<TOK>;
+  if ((threadIdx.x & 31) != 0) return;
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  // lane L copies rows L % 16 + 16 k of the tile, 16-byte segments 8 (L / 16) .. 8 (L / 16) + 7
-  const int r0 = lane & 15, seg0 = (lane >> 4) * 8;
   uint32_t b_seq = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
+    const int it = queue_read(qu, k, 1u, abort_flag, a.s.err);
+    if (it < 0) break;
+    const WorkItem w = items[it];
+    const ItemView v = view_item<PHASE>(a, w);
+    const TmaDesc *map = PHASE == 1 ? (v.routed ? &bm.xs : &bm.xh) : (v.routed ? &bm.h_routed : &bm.h_shared);
+    for (int kc = w.kc0; kc < w.kc1; ++kc) {
+      const int bs = b_seq % T_::kBSlots;
+      ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / T_::kBSlots) & 1) ^ 1, abort_flag, a.s.err);
+      if (!ok) break;
+      mbar_arrive_expect_tx(bars + 8 * (kBF + bs), T_::kBPieces * T_::kTmaBytes);
+#pragma unroll
+      for (int piece = 0; piece < T_::kBPieces; ++piece)
+        tma_load_2d(b_stage(sm, L, bs * T_::kBPieces + piece), map, kc * kChunkCols + piece * T_::kBK, v.row0,
+                    bars + 8 * (kBF + bs));
+      ++b_seq;
+    }
+  }
+  // the last fills (the only ones whose barrier phase may still be open) land before exit
+  for (uint32_t i = b_seq > (uint32_t)T_::kBSlots ? b_seq - T_::kBSlots : 0u; i < b_seq; ++i)
+    drain_bar(bars + 8 * (kBF + i % T_::kBSlots), (i / T_::kBSlots) & 1);
+}
+
+template <int PHASE, int TOK>
+__device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                            const ItemQueue &qu, volatile int *abort_flag) {
+  using T_ = Tiling<TOK>;
+  constexpr int kRowSets = TOK / 16, kSegs = T_::kBK / 16;
+  const int lane = threadIdx.x & 31;
+  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  // lane L copies rows L % 16 + 16 k of the stage, 16-byte segments kSegs (L / 16) ..
+  const int r0 = lane & 15, seg0 = (lane >> 4) * kSegs;
+  uint32_t b_seq = 0, b_rel = 0;  // stages issued, stages released
+  bool ok = true;
+  for (uint32_t k = 0; ok; ++k) {
+    // Stages still in flight are released before this warp blocks on the item queue: the
+    // MMA thread needs them to finish the item, and the weight producer may be waiting for
+    // that before it publishes the next item.
+    const bool next_ready = __shfl_sync(0xffffffffu, mbar_try_wait(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1), 0);
+    if (b_rel < b_seq && !next_ready) {
+      cp_async_wait<0>();
+      for (; b_rel < b_seq; ++b_rel) release_b(bars, b_rel, lane, T_::kBSlots);
+    }
     const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
     if (it < 0) break;
     const WorkItem w = items[it];
     const ItemView v = view_item<PHASE>(a, w);
-    const uint16_t *rb[4];
+    const uint16_t *rb[kRowSets];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < kRowSets; ++q4) {
       const int j = r0 + 16 * q4;
       rb[q4] = j < v.ntok ? act_row<PHASE>(a, v, j) : nullptr;
     }
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int bs = b_seq % kBStages;
-      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / kBStages) & 1) ^ 1, abort_flag, a.s.err);
+      const int bs = b_seq % T_::kBSlots;
+      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / T_::kBSlots) & 1) ^ 1, abort_flag, a.s.err);
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const uint32_t b_tile = smem_u32(sm) + L.b_off + bs * L.b_bytes;
+      const uint32_t b_tile = b_stage(sm, L, bs);
+      const int col0 = kc * kChunkCols + seg0 * 8;  // first column of the lane
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < kRowSets; ++q4) {
         const int j = r0 + 16 * q4;
         if (16 * q4 >= v.npad) break;
-        const uint32_t dst = b_tile + core_offset128(j, seg0 * 8);
-        const uint16_t *src = rb[q4] ? rb[q4] + kc * kChunkCols + seg0 * 8 : nullptr;
+        const uint32_t dst = b_tile + core_offset(j, seg0 * 8, T_::kBK / 8);
+        const uint16_t *src = rb[q4] ? rb[q4] + col0 : nullptr;
 #pragma unroll
-        for (int sg = 0; sg < 8; ++sg) {
-          const bool valid = src != nullptr && kc * kChunkCols + (seg0 + sg) * 8 < v.Kc;
+        for (int sg = 0; sg < kSegs; ++sg) {
+          const bool valid = src != nullptr && col0 + sg * 8 < v.Kc;
           cp_async16(dst + sg * 128, valid ? src + sg * 8 : a.s.xh, valid ? 16u : 0u);
         }
       }
       cp_async_commit();
-      if (b_seq > 0) {  // the previous chunk's copies: landed, fenced, released
-        cp_async_wait<1>();
-        release_b(bars, b_seq - 1, lane, kBStages);
-      }
       ++b_seq;
+      if (b_seq - b_rel > (uint32_t)T_::kBInFlight) {  // the oldest slot: landed, fenced, released
+        cp_async_wait<T_::kBInFlight>();
+        release_b(bars, b_rel++, lane, T_::kBSlots);
+      }
     }
   }
-  // the last chunk (also on the way out after an abort: nothing may be left in flight)
+  // the last slots (also on the way out after an abort: nothing may be left in flight)
   cp_async_wait<0>();
-  if (b_seq > 0) release_b(bars, b_seq - 1, lane, kBStages);
+  for (; b_rel < b_seq; ++b_rel) release_b(bars, b_rel, lane, T_::kBSlots);
 }
 
-template <int PHASE>
+// Descriptor of K-step 0 of an activation stage: core-matrix layout (decode tiling) or
+// 128-byte swizzled rows (prefill tiling, 8-row atoms of 1 KB).  K-step t adds t kDescStep
+// to it (the start-address field, which does not overflow inside shared memory).
+template <int TOK>
+__device__ __forceinline__ uint64_t b_desc(uint32_t stage) {
+  if constexpr (Tiling<TOK>::kTma)
+    return smem_desc_sw128(stage, 1024);
+  else
+    return smem_desc(stage, 128, Tiling<TOK>::kBK * 16);
+}
+
+template <int PHASE, int TOK>
 __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                            const ItemQueue &qu, volatile int *abort_flag) {
+  using T_ = Tiling<TOK>;
   if ((threadIdx.x & 31) != 0) return;
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
@@ -438,38 +529,55 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
     ok = wait_bar(bars + 8 * (kAE + acs), ((item_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
     if (!ok) break;
     tc_fence_after();
-    const uint32_t d = tmem + acs * kAccCols;
+    const uint32_t d = tmem + acs * T_::kAccCols;
     bool first = true;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
       const uint32_t c = pos.c;
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
-      const int bs = b_seq % kBStages, ts = a_seq % kAStages;
+      const int ts = a_seq % kAStages;
       if (v.routed)
         ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / kAStages) & 1, abort_flag, a.s.err);
       else
         ok = wait_bar(wf_bar(bars, false, seq), (seq / kRing) & 1, abort_flag, a.s.err);
-      if (ok) ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / kBStages) & 1, abort_flag, a.s.err);
+      if (!ok) break;
+      const int bs = b_seq % T_::kBSlots;
+      ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / T_::kBSlots) & 1, abort_flag, a.s.err);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t b0 = smem_u32(sm) + L.b_off + bs * L.b_bytes;
+      // this thread shares its scheduler with dequantising warps: keep the per-MMA work to an
+      // add or two on values computed once per stage
+      const uint32_t acc0 = first ? 0u : 1u;
       if (v.routed) {
-        const uint32_t at = tmem + kAColBase + ts * kACols;
+        const uint32_t at = tmem + T_::kAColBase + ts * kACols;
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          tc_mma_f16_ta(d, at + 8 * t, smem_desc(b0 + 256 * t, 128, 16 * 128), idesc, (first && t == 0) ? 0u : 1u);
-        tc_commit(bars + 8 * (kTAE + ts));
-        ++a_seq;
+        for (int piece = 0; piece < T_::kBPieces; ++piece) {
+          const uint64_t bd = b_desc<TOK>(b_stage(sm, L, bs * T_::kBPieces + piece));
+#pragma unroll
+          for (int t = 0; t < T_::kBSteps; ++t)
+            tc_mma_f16_ta(d, at + 8 * (piece * T_::kBSteps + t), bd + t * T_::kDescStep, idesc,
+                          piece + t == 0 ? acc0 : 1u);
+        }
       } else {
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          tc_mma_f16(d, smem_desc(ring + ring_add(base, 2 * t, S) * kSlab, 128, 256),
-                     smem_desc(b0 + 256 * t, 128, 16 * 128), idesc, (first && t == 0) ? 0u : 1u);
+        for (int piece = 0; piece < T_::kBPieces; ++piece) {
+          const uint64_t bd = b_desc<TOK>(b_stage(sm, L, bs * T_::kBPieces + piece));
+#pragma unroll
+          for (int t = 0; t < T_::kBSteps; ++t) {
+            const int kt = piece * T_::kBSteps + t;
+            tc_mma_f16(d, smem_desc(ring + ring_add(base, 2 * kt, S) * kSlab, 128, 256), bd + t * T_::kDescStep, idesc,
+                       kt == 0 ? acc0 : 1u);
+          }
+        }
+      }
+      tc_commit(bars + 8 * (kBE + bs));
+      ++b_seq;
+      if (v.routed) {
+        tc_commit(bars + 8 * (kTAE + ts));
+        ++a_seq;
       }
       first = false;
-      tc_commit(bars + 8 * (kBE + bs));
       tc_commit(bars + 8 * (kWE + c % kRing));  // the chunk's slabs
-      ++b_seq;
     }
     if (!ok) break;
     tc_commit(bars + 8 * (kAF + acs));
@@ -494,7 +602,7 @@ __device__ __forceinline__ void flush_store(uint32_t bars, int &pending_ts, int 
 
 // One routed item for a dequantising thread: row r of the tile, columns [32 cg, 32 cg + 32)
 // of every chunk.
-template <int PHASE, int Q>
+template <int PHASE, int TOK, int Q>
 __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, const TcLayout &L,
                         uint32_t bars, uint32_t tmem, uint32_t lut_slot, int quarter, int cg, RingPos &pos,
                         uint32_t &a_seq, int &pending_ts, volatile int *abort_flag) {
@@ -542,7 +650,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
     }
     if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
     tc_fence_after();
-    tmem_st16(tmem + lane_base + kAColBase + ts * kACols + 16 * cg, v16);
+    tmem_st16(tmem + lane_base + Tiling<TOK>::kAColBase + ts * kACols + 16 * cg, v16);
     pending_ts = ts;
     ++a_seq;
   }
@@ -552,7 +660,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   return true;
 }
 
-template <int PHASE>
+template <int PHASE, int TOK>
 __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                             const ItemQueue &qu, volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -584,7 +692,8 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     switch (v.q) {
 #define PW_DQ_CASE(QQ)                                                                                       \
   case QQ:                                                                                                   \
-    ok = dq_item<PHASE, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts, abort_flag); \
+    ok = dq_item<PHASE, TOK, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts,     \
+                                 abort_flag);                                                                \
     break;
       PW_DQ_CASE(1)
       PW_DQ_CASE(2)
@@ -594,7 +703,8 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       PW_DQ_CASE(6)
       PW_DQ_CASE(7)
       default:
-        ok = dq_item<PHASE, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts, abort_flag);
+        ok = dq_item<PHASE, TOK, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts,
+                                    abort_flag);
         break;
 #undef PW_DQ_CASE
     }
@@ -608,7 +718,7 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
   }
 }
 
-template <int PHASE>
+template <int PHASE, int TOK>
 __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const ItemQueue &qu,
                          volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -626,7 +736,7 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
     const int row = 32 * quarter + lane;  // tile row = tensor-memory lane
     const int R = w.tile * kCtaRows + row;
     const bool empty = w.kc1 <= w.kc0;     // nothing accumulated (an empty split part)
-    const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * kAccCols;
+    const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * Tiling<TOK>::kAccCols;
     for (int c = 0; c < v.npad; c += 8) {
       uint32_t r8[8];
       tmem_ld8(taddr + c, r8);
@@ -660,8 +770,9 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
   }
 }
 
-template <int PHASE>
-__global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayout L) {
+template <int PHASE, int TOK>
+__global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayout L, const __grid_constant__ BMaps bm) {
+  using T_ = Tiling<TOK>;
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
@@ -669,12 +780,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   const int warp = threadIdx.x >> 5;
   {  // regions by absolute shared address (see TcLayout)
     const uint32_t base = smem_u32(sm);
+    constexpr int low = T_::kBStages < kBLow ? T_::kBStages : kBLow;
     L.b_off = 0;
-    L.bar_off = kBStages * L.b_bytes;
+    L.bar_off = low * L.b_bytes;
     L.lut_off = (int)(kLutAddr - base);
-    L.ring_off = (int)(kRingAddr - base);
-    L.slabs = ((L.smem - L.ring_off) / kSlab) & ~1;
-    if (base >= kLutAddr || L.bar_off + kNumBars * 8 > L.lut_off || L.slabs < 2 * kDenseSlabs + 2) {
+    L.b_hi = (int)(kRingAddr - base);
+    L.ring_off = L.b_hi + (T_::kBStages - low) * L.b_bytes;
+    L.slabs = L.smem > L.ring_off ? ((L.smem - L.ring_off) / kSlab) & ~1 : 0;
+    // a dense chunk (16 slabs, one of padding at most) must fit the ring
+    const bool misaligned = T_::kTma && ((base + L.b_off) & 1023u) != 0u;  // swizzle atoms are 1 KB-aligned
+    if (base >= kLutAddr || L.bar_off + kNumBars * 8 > L.lut_off || L.slabs < kDenseSlabs + 2 || misaligned) {
       if (threadIdx.x == 0) atomicExch(a.s.err, 3);  // the map does not fit this launch
       return;
     }
@@ -690,7 +805,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kTAF + i), kDq);
       mbar_init(bars + 8 * (kTAE + i), 1);
     }
-    for (int i = 0; i < kBStages; ++i) {
+    for (int i = 0; i < T_::kBSlots; ++i) {
       mbar_init(bars + 8 * (kBF + i), 1);  // lane 0 of the activation producer
       mbar_init(bars + 8 * (kBE + i), 1);
     }
@@ -718,15 +833,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   const uint32_t tmem = tmem_slot;
   const ItemQueue qu{queue_slot, bars};
   if (warp < kDq)
-    dequantiser<PHASE>(a, L, sm, bars, tmem, qu, &abort_flag);
+    dequantiser<PHASE, TOK>(a, L, sm, bars, tmem, qu, &abort_flag);
   else if (warp < kWarpP)
-    epilogue<PHASE>(a, bars, tmem, qu, &abort_flag);
+    epilogue<PHASE, TOK>(a, bars, tmem, qu, &abort_flag);
   else if (warp == kWarpP)
     weight_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
-  else if (warp == kWarpAB)
-    ab_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
+  else if (warp == kWarpAB) {
+    if constexpr (T_::kTma)
+      ab_producer_tma<PHASE, TOK>(a, bm, L, sm, bars, qu, &abort_flag);
+    else
+      ab_producer<PHASE, TOK>(a, L, sm, bars, qu, &abort_flag);
+  }
   else if (warp == kWarpMma)
-    mma_issuer<PHASE>(a, L, sm, bars, tmem, qu, &abort_flag);
+    mma_issuer<PHASE, TOK>(a, L, sm, bars, tmem, qu, &abort_flag);
   else
     lut_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
   tc_fence_before();
@@ -737,27 +856,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   }
 }
 
-static TcLayout tc_layout(const FwdArgs &a) {
+template <int TOK>
+static int launch_tiled(const FwdArgs &a, int phase, cudaStream_t st) {
+  using T_ = Tiling<TOK>;
   TcLayout L{};
-  L.npad_max = max(16, (min(a.T, kTokChunk) + 15) / 16 * 16);
-  L.b_bytes = L.npad_max * kChunkCols * 2;
+  L.npad_max = T_::kTma ? TOK : max(16, (min(a.T, TOK) + 15) / 16 * 16);  // a TMA box is always TOK rows
+  L.b_bytes = L.npad_max * T_::kBK * 2;
+  if (T_::kTma && !a.bmaps) return (int)cudaErrorInvalidValue;
+  const BMaps bm = a.bmaps ? *a.bmaps : BMaps{};
   L.smem = kSmemLimit;
-  return L;
+  const int low = T_::kBStages < kBLow ? T_::kBStages : kBLow;
+  if (low * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
+  const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
+  const int grid = min(max_items, a.sm_count);
+  if (phase == 1) {
+    cudaFuncSetAttribute(tc_ffn_kernel<1, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    tc_ffn_kernel<1, TOK><<<grid, kTcThreads, L.smem, st>>>(a, L, bm);
+  } else {
+    cudaFuncSetAttribute(tc_ffn_kernel<2, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    tc_ffn_kernel<2, TOK><<<grid, kTcThreads, L.smem, st>>>(a, L, bm);
+  }
+  return (int)cudaGetLastError();
 }
 
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
-  const TcLayout L = tc_layout(a);
-  if (kBStages * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
-  cudaFuncSetAttribute(tc_ffn_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  cudaFuncSetAttribute(tc_ffn_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
-  const int grid = min(max_items, a.sm_count);
-  if (phase == 1)
-    tc_ffn_kernel<1><<<grid, kTcThreads, L.smem, st>>>(a, L);
-  else
-    tc_ffn_kernel<2><<<grid, kTcThreads, L.smem, st>>>(a, L);
-  return (int)cudaGetLastError();
+  return tok_chunk_for(a.T) == kTokChunkPrefill ? launch_tiled<kTokChunkPrefill>(a, phase, st)
+                                                 : launch_tiled<kTokChunk>(a, phase, st);
 }
 
 }  // namespace pw

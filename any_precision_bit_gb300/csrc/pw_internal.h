@@ -25,7 +25,13 @@ namespace pw {
 constexpr int kMaxPlanes = 8;
 constexpr int kChunkCols = 128;   // columns per plane chunk (one pipeline stage)
 constexpr int kCtaRows = 128;     // rows per CTA tile (tensor-memory lanes of one MMA)
-constexpr int kTokChunk = 64;     // tokens per work item in the decode kernels
+constexpr int kTokChunk = 64;     // tokens per work item at decode batch sizes
+constexpr int kTokChunkPrefill = 128;  // tokens per work item for prefill-sized batches
+constexpr int kPrefillMinT = 512;      // batches of at least this many tokens use the prefill tiling
+
+// Tokens per work item for a launch of T tokens: the prefill tiling halves how often each
+// weight tile is dequantised when experts see hundreds of tokens.
+PW_HD int tok_chunk_for(int T) { return T >= kPrefillMinT ? kTokChunkPrefill : kTokChunk; }
 
 // One row of the device weight page table (PagedWeight Sec. 3.1).  The kernels read q and
 // the pointers of the block they run; commits rewrite the whole row between launches.
@@ -36,13 +42,13 @@ struct BlockDev {
   int N, K, KC;                       // rows, columns, 128-column chunks
 };
 
-// A unit of work of the decode expert kernels.
+// A unit of work of the expert kernels.
 struct WorkItem {
   int kind;    // 0 routed expert, 1 shared expert
   int expert;  // routed expert id (kind 0)
   int tile;    // CTA row tile (kCtaRows rows)
   int tok0;    // first slot (routed: into the expert-sorted pair list; shared: token)
-  int ntok;    // tokens in this item (<= kTokChunk)
+  int ntok;    // tokens in this item (<= tok_chunk_for(T))
   int kc0, kc1;  // 128-column stages [kc0, kc1) of the item along K
   int part;    // shared down projection: the partial-sum buffer this item writes
 };
@@ -135,6 +141,23 @@ PW_HD long shared_tile_index(int d, int k, int K) {
 // value as int.
 namespace pw {
 
+// An encoded TMA tensor descriptor (the driver's 128-byte, 64-byte-aligned CUtensorMap),
+// opaque here; the host runtime encodes it.
+struct alignas(64) TmaDesc {
+  unsigned char bytes[128];
+};
+
+// Tensor maps of the activation tiles of the prefill tiling: fp16, boxes of 64 columns by 128
+// rows, 128-byte swizzle (the K-major operand layout the MMAs read), rows past the end read
+// as zeros.  Rows are the scratch buffers' full capacity (max_tokens), so the maps are fixed
+// for the context.
+struct BMaps {
+  TmaDesc xs;        // [Tm*K][H] layer input gathered into expert-sorted slot order (routed gate_up)
+  TmaDesc xh;        // [Tm][H] layer input (shared gate_up)
+  TmaDesc h_routed;  // [Tm*K][I] (routed down)
+  TmaDesc h_shared;  // [Tm][Is] (shared down)
+};
+
 struct Scratch {
   float *logits;       // [Tm][E]
   int *ids;            // [Tm][K]
@@ -149,6 +172,7 @@ struct Scratch {
   int *n_items;        // [2]
   unsigned *ticket;    // [1 + ceil(Tm/8)] router last-CTA counters: all token groups, then per group
   uint16_t *xh;        // fp16 [Tm][H]: the layer input as the experts read it (normalised under PW_PRENORM)
+  uint16_t *xs;        // fp16 [Tm*K][H]: xh rows in expert-sorted slot order (prefill tiling; null if Tm is smaller)
   uint16_t *h_routed;  // fp16 [Tm*K][I]
   uint16_t *h_shared;  // fp16 [Tm][Is]
   float *o_routed;     // [Tm*K][H]
@@ -178,6 +202,7 @@ struct FwdArgs {
   int *ids_out;           // optional
   float *w_out;           // optional
   int sm_count;
+  const BMaps *bmaps;     // host copy of the prefill tensor maps (null when the context has none)
 };
 
 // ev: null, or five timing events recorded before, between and after the four kernels

@@ -70,6 +70,18 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
   }
 }
 
+// Prefill tiling: the layer input's rows in expert-sorted slot order (xs[slot] = xh[token of
+// slot]), so that every routed gate_up work item reads consecutive rows, one TMA box per
+// activation stage.  16-byte vectors, grid-stride.
+__global__ void gather_kernel(FwdArgs a) {
+  const int vec = a.H / 8;
+  const long n = (long)a.T * a.K * vec;
+  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+    const int s = (int)(i / vec), v = (int)(i % vec);
+    const int t = a.s.slot_tok[s];
+    reinterpret_cast<uint4 *>(a.s.xs + (size_t)s * a.H)[v] = reinterpret_cast<const uint4 *>(a.s.xh + (size_t)t * a.H)[v];
+  }
+}
 
 // ------------------------------------------------------------------ launch
 // Timing events: under stream capture an ordinary record only orders graph nodes, so the
@@ -88,6 +100,10 @@ int launch_forward(const FwdArgs &a, void *stream_, void *const *ev_) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   if (ev) record(ev[0], st);
   if (int e = launch_route(a, stream_)) return e;
+  if (tok_chunk_for(a.T) == kTokChunkPrefill) {
+    if (!a.s.xs) return (int)cudaErrorInvalidValue;
+    gather_kernel<<<a.sm_count * 4, 256, 0, st>>>(a);
+  }
   if (ev) record(ev[1], st);
   if (int e = launch_ffn(a, 1, stream_)) return e;
   if (ev) record(ev[2], st);

@@ -329,7 +329,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   __syncthreads();
   const int tiles1 = (2 * a.I + kCtaRows - 1) / kCtaRows;
   const int tiles2 = (a.H + kCtaRows - 1) / kCtaRows;
-  const int tchunks = (T + kTokChunk - 1) / kTokChunk;
+  const int tc = tok_chunk_for(T);
+  const int tchunks = (T + tc - 1) / tc;
   const int nsplit = shared_down_splits(a.I, a.Is);
   const int sh1 = a.Is > 0 ? ((2 * a.Is + kCtaRows - 1) / kCtaRows) * tchunks : 0;
   const int sh2 = a.Is > 0 ? tiles2 * tchunks * nsplit : 0;
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
         s_wc[w][tid] = cnt;
         cnt += c;
       }
-    const int ch = (cnt + kTokChunk - 1) / kTokChunk;
+    const int ch = (cnt + tc - 1) / tc;
     int x0 = cnt, x1 = ch * tiles1, x2 = ch * tiles2;  // inclusive scans over the experts
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -402,32 +403,32 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   for (int i = tid; i < sh1; i += kRtThreads) {
     const int tile = i / tchunks, c = i % tchunks;
     store_item(a.s.items1 + i,
-               WorkItem{1, 0, tile, c * kTokChunk, min(kTokChunk, T - c * kTokChunk), 0, kc_gu, 0});
+               WorkItem{1, 0, tile, c * tc, min(tc, T - c * tc), 0, kc_gu, 0});
   }
   {
     const int total = (a.Is / 16 + 7) / 8, per = (total + nsplit - 1) / nsplit;
     for (int i = tid; i < sh2; i += kRtThreads) {
       const int tile = i / (tchunks * nsplit), rem = i % (tchunks * nsplit);
       const int c = rem / nsplit, part = rem % nsplit;
-      store_item(a.s.items2 + i, WorkItem{1, 0, tile, c * kTokChunk, min(kTokChunk, T - c * kTokChunk),
-                                          part * per, min(total, (part + 1) * per), part});
+      store_item(a.s.items2 + i,
+                 WorkItem{1, 0, tile, c * tc, min(tc, T - c * tc), part * per, min(total, (part + 1) * per), part});
     }
   }
   __syncthreads();  // every slot weight is in place
-  // per expert (one warp each): its (token chunk, row tile) work items and its routing
-  // statistics, the slot weights summed in a fixed order
+  // per expert (one warp each): its (row tile, token chunk) work items and its routing
+  // statistics, the slot weights summed in a fixed order.  The token chunks of a row tile are
+  // consecutive items, so that CTAs claiming them together share the tile's planes in L2.
   for (int ee = warp; ee < E; ee += kRtWarps) {
     const int cnt = s_cnt[ee], o0 = s_off[ee];
+    const int ch = (cnt + tc - 1) / tc;
     const int n1 = s_itm1[ee + 1] - s_itm1[ee], n2 = s_itm2[ee + 1] - s_itm2[ee];
     for (int i = lane; i < n1; i += 32) {
-      const int c = i / tiles1;
-      store_item(a.s.items1 + s_itm1[ee] + i,
-                 WorkItem{0, ee, i - c * tiles1, c * kTokChunk, min(kTokChunk, cnt - c * kTokChunk), 0, kc_gu, 0});
+      const int c = i % ch;
+      store_item(a.s.items1 + s_itm1[ee] + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_gu, 0});
     }
     for (int i = lane; i < n2; i += 32) {
-      const int c = i / tiles2;
-      store_item(a.s.items2 + s_itm2[ee] + i,
-                 WorkItem{0, ee, i - c * tiles2, c * kTokChunk, min(kTokChunk, cnt - c * kTokChunk), 0, kc_d, 0});
+      const int c = i % ch;
+      store_item(a.s.items2 + s_itm2[ee] + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_d, 0});
     }
     float wsum = 0.f;
     for (int sl = lane; sl < cnt; sl += 32) wsum += rs.pairs ? psw[o0 + sl] : __ldcg(psw + o0 + sl);

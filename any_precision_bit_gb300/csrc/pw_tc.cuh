@@ -24,6 +24,16 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte swizzled layout (the
+// layout a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes): rows of 128 bytes (64 fp16) in
+// 8-row atoms of 1 KB whose 16-byte chunks are permuted by the row within the atom, atoms
+// `sbo_bytes` apart.  The atom must be 1 KB-aligned; the K-step k (16 columns) of the row
+// starts 32 k bytes in.  Leading byte offset unused (1), version 1, layout type 2.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
 // Instruction descriptor of kind::f16 with fp16 A and B (K-major), fp32 accumulation.
 __host__ __device__ __forceinline__ uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
