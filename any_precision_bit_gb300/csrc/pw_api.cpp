@@ -1090,21 +1090,31 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
   if (!c || !obs || !off || !out) return fail(c, PW_ERR_INVALID, "null argument");
   if (off->n_bits != c->n_bits) return fail(c, PW_ERR_INVALID, "offline table has %d bitwidths, context %d", off->n_bits, c->n_bits);
   if (!obs->phi) return fail(c, PW_ERR_INVALID, "obs->phi is required");
-  const int n = (int)c->blocks.size(), nb = c->n_bits, L = c->d.L, E = c->d.E;
+  const int nb = c->n_bits, L = c->d.L, E = c->d.E;
+  // A block whose pages are still in transfer (or whose landed reload awaits pw_commit)
+  // cannot take another step yet: the problem holds the idle blocks only.
+  std::vector<int> ids;
+  for (int i = 0; i < (int)c->blocks.size(); ++i) {
+    if (!c->blocks[i].packed) return fail(c, PW_ERR_STATE, "block %d is not packed", i);
+    if (pw_status st = observe(c, i)) return st;
+    if (!c->blocks[i].pend.kind) ids.push_back(i);
+  }
+  const int n = (int)ids.size();
   std::vector<int> q(n), q0(n), ut(n), ly(n), ex(n);
-  std::vector<double> M((size_t)n * nb);
-  for (int i = 0; i < n; ++i) {
-    const HostBlock &b = c->blocks[i];
-    if (!b.packed) return fail(c, PW_ERR_STATE, "block %d is not packed", i);
-    q[i] = b.pend.kind == 2 ? b.pend.to : b.q;  // a landed-but-uncommitted reload counts as raised
-    q0[i] = b.q_init;
-    ut[i] = b.u;
-    ly[i] = b.layer;
-    ex[i] = b.expert;
-    for (int j = 0; j < nb; ++j) M[(size_t)i * nb + j] = (double)block_M(c, b, c->bits[j]);
+  std::vector<double> M((size_t)n * nb), phi((size_t)n * 3);
+  for (int k = 0; k < n; ++k) {
+    const HostBlock &b = c->blocks[ids[k]];
+    q[k] = b.q;
+    q0[k] = b.q_init;
+    ut[k] = b.u;
+    ly[k] = b.layer;
+    ex[k] = b.expert;
+    for (int j = 0; j < nb; ++j) M[(size_t)k * nb + j] = (double)block_M(c, b, c->bits[j]);
+    for (int j = 0; j < 3; ++j) phi[(size_t)k * 3 + j] = obs->phi[(size_t)ids[k] * 3 + j];
   }
   std::vector<double> mass;
   pw_obs o = *obs;
+  o.phi = phi.data();
   if (!o.mass) {  // Eq. 1 from the online routing statistics
     CU(c, cudaStreamSynchronize(c->compute));
     mass.resize((size_t)L * E);
@@ -1119,7 +1129,10 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
   pw_plan_problem prob{n, nb, L, E, c->bits, q.data(), q0.data(), ut.data(), ly.data(), ex.data(), M.data()};
   pw_status st = pw_plan_host(&prob, &o, off, out);
   if (st != PW_OK) return fail(c, st, "planner rejected its inputs (or the plan did not fit in out->capacity)");
-  for (int k = 0; k < out->n; ++k) c->blocks[out->entries[k].block].d = out->entries[k].to_bits;
+  for (int k = 0; k < out->n; ++k) {
+    out->entries[k].block = ids[out->entries[k].block];
+    c->blocks[out->entries[k].block].d = out->entries[k].to_bits;
+  }
   return PW_OK;
 }
 

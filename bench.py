@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--paging", action="store_true",
+                    help="dynamic paging run: a free-KV-block trace drives the planner, offload and reload every step")
     return ap.parse_args()
 
 
@@ -237,6 +239,64 @@ def run_reference(args, shape, L, T):
     print(json.dumps(line), flush=True)
 
 
+def run_paging(args, pw, torch, ctx, shape, L, T, stream, x0, xw, clocks_cls):
+    """PagedWeight Sec. 3.2-3.3 in the loop: per decode step the planner (Eqs. 3-8) reads the
+    trace's free KV blocks, its plan is applied with offload / reload on the side stream,
+    landed reloads are committed, then the stack runs.  Timed end to end on the host (the
+    planner and the page I/O calls are part of the step) and on the device."""
+    steps = 200
+    trace = syn.kv_free_block_trace(steps)
+    n_blocks = L * shape.E * 2
+    off = syn.gen_planner_offline_np(n_blocks, list(shape.bits), 4, args.seed)
+    off["n_stages"] = 3
+    B_KV = 2.0 * 1024 * 1024
+    start = pw.pw_memory(ctx).resident_bytes
+    moved = {"offload": 0.0, "reload": 0.0}
+    applied = 0
+    kinds = {0: 0, 1: 0, 2: 0}
+    resident = []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    clocks = clocks_cls(int(os.environ.get("LOCAL_RANK", "0")))
+    clocks.start()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for step in range(steps):
+            obs = dict(T_blk=16, F_blk=int(trace[step]), B_KV=B_KV, R=8, mass=None,
+                       phi=syn.gen_phi_np(n_blocks, args.seed, step))
+            plan = pw.pw_plan_step(ctx, n_blocks, obs, off)
+            kinds[plan["kind"]] += 1
+            applied += len(plan["entries"])
+            for block, fb, tb, delta in plan["entries"]:
+                if tb < fb:
+                    pw.pw_offload(ctx, block, tb)
+                    moved["offload"] += delta
+                else:
+                    pw.pw_reload(ctx, block, tb)
+                    moved["reload"] += delta
+            pw.pw_commit(ctx)
+            xw.copy_(x0)
+            pw.pw_stack_forward(ctx, xw, T, stream)
+            resident.append(pw.pw_memory(ctx).resident_bytes)
+        ev1.record(stream)
+    stream.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    dev_ms = ev0.elapsed_time(ev1)
+    pw.pw_sync_io(ctx)
+    return {
+        "steps": steps, "trace": "F_blk(t) = round(32 + 32 cos(2 pi t / 200)), T_blk = 16, R = 8, B_KV = 2 MiB",
+        "host_ms_per_step": wall * 1e3 / steps, "device_ms_per_step": dev_ms / steps,
+        "tokens_per_s": T * L * steps / wall, "plans": {"none": kinds[0], "offload": kinds[1], "reload": kinds[2]},
+        "offloaded_bytes": moved["offload"], "reloaded_bytes": moved["reload"],
+        "resident_bytes": {"start": start, "min": min(resident), "end": resident[-1]}, "clocks": clk,
+        # the stack's kernels, plus one page-table commit kernel per applied bitwidth change
+        "gpu_launches": (5 if T >= PREFILL_MIN_T else 4) * L * steps + applied,
+    }
+
+
 def run_ours(args, shape, L, T):
     import torch
     import any_precision_bit_gb300 as pw
@@ -268,6 +328,29 @@ def run_ours(args, shape, L, T):
         for _ in range(max(args.warmup, 3)):
             step()
     stream.synchronize()
+    if args.paging:
+        static_ms = None
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(20):
+                step()
+            ev1.record(stream)
+        stream.synchronize()
+        static_ms = ev0.elapsed_time(ev1) / 20
+        res = run_paging(args, pw, torch, ctx, shape, L, T, stream, x0, xw, Clocks)
+        line = {"metric": METRIC, "value": res["tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+                "steps": res["steps"], "warmup": max(args.warmup, 3), "ms_per_step": res["host_ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+                "config": dict(workload_config(shape, T, L), workload=f"{shape.name}-shaped MoE stack decode with "
+                               f"dynamic paging: {L} layers, T={T}, 200 steps"),
+                "static_ms_per_step": static_ms, "paging": res, "clocks": res["clocks"],
+                "gpu_launches": res["gpu_launches"]}
+        pw.pw_destroy(ctx)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     for l in range(L):
         pw.pw_routing_stats(ctx, l, shape.E, reset=True)
     if dist:
@@ -336,7 +419,7 @@ def run_ours(args, shape, L, T):
         "routed_gbs": (tot["gu"] + tot["dn"]) / (ms * 1e-3) / 1e9,
         "hbm_frac": tot["total"] / (ms * 1e-3) / 1e9 / peak,
         "bytes_per_step": tot["total"], "roofline": roofline, "clocks": clk,
-        "gpu_launches": 4 * L * args.steps, "setup_s": round(t_setup, 1),
+        "gpu_launches": (5 if T >= PREFILL_MIN_T else 4) * L * args.steps, "setup_s": round(t_setup, 1),
     }
     if flops is not None:
         tot_fl = (flops[1] + flops[2]) * L

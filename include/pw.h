@@ -302,8 +302,10 @@ pw_status pw_plan_host(const pw_plan_problem *prob, const pw_obs *obs,
                        const pw_offline *off, pw_plan *out);
 
 /* PlanStep on the context's page table (q_i, M_i^b) and, when obs->mass is NULL, its
- * online routing statistics (Eq. 1).  Writes the desired bitwidth d_i of every planned
- * block.  Applying the plan is the caller's pw_offload / pw_reload. */
+ * online routing statistics (Eq. 1).  Blocks with a page transfer in flight, or a landed
+ * reload not yet committed, take no step (they are left out of the problem), so every
+ * entry of the plan can be applied at once.  Writes the desired bitwidth d_i of every
+ * planned block.  Applying the plan is the caller's pw_offload / pw_reload. */
 pw_status pw_plan_step(pw_ctx *ctx, const pw_obs *obs, const pw_offline *off, pw_plan *out);
 
 /* ---------------------------------------------------------------- inspection */

@@ -1,0 +1,248 @@
+"""The dynamic paging run (PagedWeight Sec. 3.2 and Sec. 3.3, Fig. 4) on the device: a
+synthetic free-KV-block trace F_blk(t) = round(32 + 32 cos(2 pi t / 200)) drives the greedy
+planner (Eqs. 3-8, Algorithm 1) for 200 decode steps of 64 tokens; every plan is applied with
+pw_offload / pw_reload on the side stream and pw_commit between steps, retired device pages
+are poisoned with 0xFF, and at EVERY step every layer's output is compared with the float64
+oracle run at that step's committed bitwidths.
+
+The layers have the structure of the Qwen1.5-MoE-shaped stack (60 routed experts, top-4,
+hot/cold bitwidths under a Zipf(1.1) router prior, a dense shared expert, bits 3..8) at
+reduced widths, so that the oracle can check all 200 steps; the KV block size is scaled
+with the weight bytes so that the pressure phase of the trace pushes blocks to their floors
+and the recovery phase restores them.  A second test runs the trace on full-size
+Qwen-shaped layers and checks the oracle at a handful of steps."""
+import numpy as np
+import pytest
+
+import synthetic as syn
+from oracle import ap
+from oracle import moe as omoe
+from oracle import planner as opl
+
+from gpu_helpers import assert_close, bf16_to_f64, make_ctx, lut_concat
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+pw = pytest.importorskip("any_precision_bit_gb300")
+
+MINI = syn.LayerShape("qwen_mini", H=256, E=60, I=128, K=4, Is=512, L=2, bmax=8, bits=(3, 4, 5, 6, 7, 8),
+                      sigma_lut=0.02, zipf_a=1.1, q_rule="hot_cold")
+STEPS, T, T_BLK, R = 200, 64, 16, 8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_ready():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from any_precision_bit_gb300 import _build
+    _build.build()
+
+
+class Stack:
+    """Seeded layers of `shape`, packed into a context with poisoned retired pages."""
+
+    def __init__(self, shape, L, seed=0):
+        self.shape, self.L, self.seed = shape, L, seed
+        self.ctx = make_ctx(pw, shape, L=L, max_tokens=T, flags=pw.PW_FLAG_POISON)
+        self.layers = []
+        for l in range(L):
+            Wr, bias, ranks = syn.gen_router_np(shape, seed, l)
+            q = syn.gen_q_assignment(shape, seed, l, ranks)
+            experts = {}
+            for e in range(shape.E):
+                gi, gl = syn.gen_block_np(shape, seed, l, e, 0)
+                di, dl = syn.gen_block_np(shape, seed, l, e, 1)
+                experts[e] = (gi, gl, di, dl)
+                pw.pw_pack(self.ctx, l, e, 0, gi, lut_concat(gl, shape.bits), int(q[e, 0]))
+                pw.pw_pack(self.ctx, l, e, 1, di, lut_concat(dl, shape.bits), int(q[e, 1]))
+            shared = syn.gen_shared_np(shape, seed, l)
+            pw.pw_set_router(self.ctx, l, Wr, bias)
+            pw.pw_set_shared(self.ctx, l, shared[0], shared[1])
+            self.layers.append(dict(Wr=Wr, bias=bias, q0=q, experts=experts, shared=shared))
+        self.n_blocks = L * shape.E * 2
+        self._w = {}
+
+    def committed_q(self, l):
+        E = self.shape.E
+        return np.array([[pw.pw_query(self.ctx, syn.block_id(l, e, u, E)).q for u in (0, 1)] for e in range(E)],
+                        dtype=np.int32)
+
+    def tokens(self, step, l):
+        """Step-dependent tokens whose sorted logits are separated by >= 1e-3 among ranks
+        1..K+1, so that the top-K decision does not depend on the rounding of fp32 logits."""
+        sh, lay = self.shape, self.layers[l]
+        seed = self.seed * 100003 + 7 + step
+        x = syn.gen_tokens_np(sh, seed, l, T)
+
+        def ok(row):
+            s = np.sort(omoe.router_logits(row[None], lay["Wr"], lay["bias"], True)[0])[::-1][: sh.K + 1]
+            return np.all(-np.diff(s) >= 1e-3)
+        for t in range(T):
+            a = 0
+            while not ok(x[t]):
+                a += 1
+                x[t] = syn.gen_token_np(sh, seed, l, t, a)
+        return x
+
+    def oracle(self, l, x, q):
+        """The float64 layer at bitwidths q on the rows of x; the dense weight of each
+        (block, q) is the oracle's own block_weight, memoised across steps."""
+        lay, sh = self.layers[l], self.shape
+        n = x.shape[0]
+        ids, w, _ = omoe.route(x, lay["Wr"], lay["bias"], sh.K, prenorm=True)
+        xf = omoe.rmsnorm(bf16_to_f64(x))
+        y = np.zeros((n, sh.H))
+        o = np.zeros((n, sh.K, sh.H))
+        for e in np.unique(ids):
+            e = int(e)
+            W = []
+            for u in (0, 1):
+                key = (l, e, u, int(q[e, u]))
+                if key not in self._w:
+                    self._w[key] = omoe.block_weight(lay["experts"][e][2 * u], lay["experts"][e][2 * u + 1], sh.bmax,
+                                                     int(q[e, u]))
+                W.append(self._w[key])
+            rows, slots = np.nonzero(ids == e)
+            o[rows, slots] = omoe.expert_ffn(xf[rows], W[0], W[1])
+        for k in range(sh.K):
+            y += w[:, k:k + 1] * o[:, k, :]
+        if ("shared", l) not in self._w:
+            self._w[("shared", l)] = (bf16_to_f64(lay["shared"][0]), bf16_to_f64(lay["shared"][1]))
+        y += omoe.expert_ffn(xf, *self._w[("shared", l)])
+        return y
+
+    def forward(self, l, x):
+        xd = torch.from_numpy(x.view(np.int16)).cuda()
+        yd = torch.zeros_like(xd)
+        torch.cuda.synchronize()
+        pw.pw_moe_forward(self.ctx, l, xd, T, yd, None, None, pw.PW_PRENORM, pw.pw_get_stream(self.ctx))
+        torch.cuda.synchronize()
+        return bf16_to_f64(yd.cpu().numpy().view(np.uint16))
+
+    def resident_bytes_eq3(self):
+        tot = 0
+        for l in range(self.L):
+            q = self.committed_q(l)
+            for e in range(self.shape.E):
+                for u in (0, 1):
+                    N, K = syn.block_shape(self.shape, u)
+                    tot += ap.block_bytes(N, K, self.shape.bits, int(q[e, u]))
+        return tot
+
+
+def oracle_plan(st, off, obs):
+    """The oracle planner (Algorithm 1 restated) on the blocks that can take a step now: no
+    page in transfer and no landed reload awaiting its commit.  Routing mass (Eq. 1) from the
+    context's accumulated routing-weight sums."""
+    sh, E = st.shape, st.shape.E
+    idle, q, q0, ut, ly, ex, M = [], [], [], [], [], [], []
+    for l in range(st.L):
+        for e in range(E):
+            for u in (0, 1):
+                b = syn.block_id(l, e, u, E)
+                info = pw.pw_query(st.ctx, b)
+                busy = info.pending_q != 0 or any(info.state[p] in (pw.PW_PAGE_TO_CPU, pw.PW_PAGE_TO_GPU)
+                                                  for p in range(sh.bmax))
+                if busy:
+                    continue
+                N, K = syn.block_shape(sh, u)
+                idle.append(b)
+                q.append(info.q)
+                q0.append(int(st.layers[l]["q0"][e, u]))
+                ut.append(u)
+                ly.append(l)
+                ex.append(e)
+                M.append([ap.block_bytes(N, K, sh.bits, bb) for bb in sh.bits])
+    mass = np.array([pw.pw_routing_stats(st.ctx, l, E)[1] for l in range(st.L)], dtype=np.float64)
+    for l in range(st.L):  # normalised per layer, summed in expert order
+        tot = 0.0
+        for e in range(E):
+            tot += float(mass[l, e])
+        mass[l] = mass[l] / tot if tot > 0 else 1.0 / E
+    idx = np.array(idle, dtype=np.int64)
+    sub = dict(off, s=np.asarray(off["s"])[idx])
+    blocks = opl.Blocks(list(sh.bits), q, ut, ly, ex, np.array(M, dtype=np.float64), sub["s"])
+    phi = np.asarray(obs["phi"])[idx]
+    _, chosen, D = opl.plan_step(blocks, mass, phi, sub, off["n_stages"], obs["T_blk"], obs["F_blk"], obs["B_KV"])
+    if D > 0:
+        stage, plan, total = chosen
+        return 1, stage, D, [(idle[i], a, b, d) for i, (a, b, d) in plan.items()]
+    plan, total = opl.reload_plan(blocks, q0, mass, phi, sub, obs["T_blk"], obs["F_blk"], obs["B_KV"], obs["R"])
+    return (2 if total > 0 else 0), -1, D, [(idle[i], a, b, d) for i, (a, b, d) in plan.items()]
+
+
+def run_trace(st, off, B_KV, check_steps, check_layers, check_tokens=None, check_plans=False):
+    trace = syn.kv_free_block_trace(STEPS)
+    log = []
+    for step in range(STEPS):
+        obs = dict(T_blk=T_BLK, F_blk=int(trace[step]), B_KV=B_KV, R=R, mass=None,
+                   phi=syn.gen_phi_np(st.n_blocks, st.seed, step))
+        if check_plans:
+            pw.pw_set_fault(st.ctx, 3, 1)  # hold: no transfer is observed landing until the plan is compared
+            want = oracle_plan(st, off, obs)
+        plan = pw.pw_plan_step(st.ctx, st.n_blocks, obs, off)
+        if check_plans:
+            pw.pw_set_fault(st.ctx, 3, 0)
+            assert (plan["kind"], plan["stage"], plan["D"]) == want[:3], f"step {step}"
+            assert plan["entries"] == want[3], f"step {step}"
+        for block, fb, tb, _ in plan["entries"]:
+            if tb < fb:
+                pw.pw_offload(st.ctx, block, tb)
+            else:
+                pw.pw_reload(st.ctx, block, tb)
+        pw.pw_commit(st.ctx)  # reloads that have landed raise q now, between launches
+        for l in range(st.L):
+            x = st.tokens(step, l)
+            y = st.forward(l, x)
+            if step in check_steps and l in check_layers:
+                q = st.committed_q(l)
+                rows = np.arange(T) if check_tokens is None else (np.arange(check_tokens) + 5 * step) % T
+                assert_close(y[rows], st.oracle(l, x[rows], q), f"step {step} layer {l}")
+        log.append((step, plan["kind"], len(plan["entries"]), pw.pw_memory(st.ctx).resident_bytes))
+    return log
+
+
+def offline_inputs(st):
+    off = syn.gen_planner_offline_np(st.n_blocks, list(st.shape.bits), 4, st.seed)
+    off["n_stages"] = 3
+    return off
+
+
+def test_paging_run_every_step_matches_oracle():
+    st = Stack(MINI, L=MINI.L)
+    try:
+        start = st.resident_bytes_eq3()
+        assert pw.pw_memory(st.ctx).resident_bytes == start
+        # KV block size: the whole pressure phase asks for about half the resident bytes
+        trace = syn.kv_free_block_trace(STEPS)
+        demand = sum(max(0, T_BLK - int(f) + 1) for f in trace)
+        B_KV = 0.5 * start / demand
+        log = run_trace(st, offline_inputs(st), B_KV, check_steps=set(range(STEPS)), check_layers=range(st.L),
+                        check_plans=True)
+        pw.pw_sync_io(st.ctx)
+        pw.pw_commit(st.ctx)
+        kinds = [k for _, k, _, _ in log]
+        resident = [r for _, _, _, r in log]
+        assert 1 in kinds and 2 in kinds          # both offload and reload plans were applied
+        assert min(resident) < 0.75 * start       # the pressure phase freed weight pages
+        assert resident[-1] > min(resident)       # and the recovery phase brought some back
+        assert pw.pw_memory(st.ctx).resident_bytes == st.resident_bytes_eq3()
+        for l in range(st.L):                     # never above the packed bitwidths
+            assert np.all(st.committed_q(l) <= st.layers[l]["q0"])
+    finally:
+        pw.pw_destroy(st.ctx)
+
+
+def test_paging_run_full_size_spot_checks():
+    shape = syn.SHAPES["qwen"]
+    st = Stack(shape, L=2)
+    try:
+        B_KV = 2.0 * 1024 * 1024 * 2 / shape.L  # 2 MiB per KV block, scaled to 2 of the 24 layers
+        log = run_trace(st, offline_inputs(st), B_KV, check_steps={0, 100, 199}, check_layers={0}, check_tokens=3)
+        assert any(k == 1 for _, k, _, _ in log)
+        pw.pw_sync_io(st.ctx)
+        pw.pw_commit(st.ctx)
+        assert pw.pw_memory(st.ctx).resident_bytes == st.resident_bytes_eq3()
+    finally:
+        pw.pw_destroy(st.ctx)
