@@ -22,9 +22,9 @@ namespace {
 thread_local std::string g_thread_err;
 
 // 2-D fp16 tensor map over a row-major [rows][cols] buffer: boxes of 64 columns (128 bytes)
-// by 128 rows with the 128-byte swizzle, out-of-range elements read as zero.  The encoder is
+// by box_rows rows with the 128-byte swizzle, out-of-range elements read as zero.  The encoder is
 // the driver's, looked up through the runtime (no link-time dependency on the driver library).
-bool encode_act_map(TmaDesc *out, void *base, long rows, long cols) {
+bool encode_act_map(TmaDesc *out, void *base, long rows, long cols, unsigned box_rows) {
   using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                               const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -42,7 +42,7 @@ bool encode_act_map(TmaDesc *out, void *base, long rows, long cols) {
   static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "tensor map size");
   const cuuint64_t dim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t stride[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, box_rows};
   const cuuint32_t estride[2] = {1, 1};
   return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dim, stride, box, estride,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -167,7 +167,7 @@ struct pw_ctx {
   void *stage = nullptr;  // device staging for packing / inspection
   size_t stage_bytes = 0;
   void *xdev = nullptr;   // device activations of pw_stack_forward_host
-  BMaps bmaps{};          // prefill tensor maps (valid when has_bmaps)
+  BMaps bmaps{};          // activation tensor maps of the expert kernels (valid when has_bmaps)
   bool has_bmaps = false;
   std::vector<GraphEntry> graphs;
   std::string err;
@@ -405,15 +405,20 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.stat_count, sizeof(double) * d.L * d.E) &&
             salloc((void **)&c->s.stat_wsum, sizeof(double) * d.L * d.E) &&
             salloc(&c->xdev, sizeof(uint16_t) * Tm * d.H);
-  if (ok && Tm >= kPrefillMinT) ok = salloc((void **)&c->s.xs, sizeof(uint16_t) * TK * d.H);
+  if (ok) ok = salloc((void **)&c->s.xs, sizeof(uint16_t) * TK * d.H);
   if (!ok) {
     fail(nullptr, PW_ERR_OOM, "scratch allocation failed (max_tokens=%d)", d.max_tokens);
     return bail(PW_ERR_OOM);
   }
-  if (c->s.xs) {
-    const bool enc = encode_act_map(&c->bmaps.xs, c->s.xs, TK, d.H) && encode_act_map(&c->bmaps.xh, c->s.xh, Tm, d.H) &&
-                     encode_act_map(&c->bmaps.h_routed, c->s.h_routed, TK, d.I) &&
-                     (d.Is == 0 || encode_act_map(&c->bmaps.h_shared, c->s.h_shared, Tm, d.Is));
+  {
+    bool enc = true;
+    for (int k = 0; k < 2; ++k) {
+      ActMaps &m = k ? c->bmaps.rows128 : c->bmaps.rows16;
+      const unsigned br = k ? 128u : 16u;
+      enc = enc && encode_act_map(&m.xs, c->s.xs, TK, d.H, br) && encode_act_map(&m.xh, c->s.xh, Tm, d.H, br) &&
+            encode_act_map(&m.h_routed, c->s.h_routed, TK, d.I, br) &&
+            (d.Is == 0 || encode_act_map(&m.h_shared, c->s.h_shared, Tm, d.Is, br));
+    }
     if (!enc) {
       fail(nullptr, PW_ERR_CUDA, "tensor map encoding failed");
       return bail(PW_ERR_CUDA);

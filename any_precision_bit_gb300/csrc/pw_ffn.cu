@@ -22,12 +22,12 @@
 //     the q bit-plane slabs of a routed chunk (lane p copies plane p) or the eight 4 KB K-step
 //     pieces of a dense shared-expert tile (lane t copies piece t).  A chunk takes exactly the
 //     bytes it needs, so low bitwidths keep more chunks in flight;
-//   * activation producer (1 warp): the B operand tiles, a ring of 16 KB stages.  Decode
-//     tiling: the tokens' fp16 rows gathered with 16-byte cp.async copies, each lane fencing
-//     its landed copies to the async proxy before the tile is released to the MMA thread.
-//     Prefill tiling: one TMA box (128 rows x 64 columns, 128-byte swizzle) per stage from
-//     row-contiguous buffers (the layer input gathered into slot order beforehand, h, the
-//     shared expert's input and h);
+//   * activation producer (1 warp): the B operand tiles, three per-chunk slots of two stages
+//     (64 columns each, 128-byte swizzle), loaded by TMA from row-contiguous buffers (the
+//     layer input gathered into slot order beforehand, h, the shared expert's input and h):
+//     decode, one 16-row box per lane, as many as the item has tokens padded to 16; prefill,
+//     one 128-row box per stage.  TMA keeps every slot's copies in flight at once (16-byte
+//     cp.async gathers stall on one round trip per tile);
 //   * dequantising warps (16, four per tensor-memory lane quarter): each thread owns one row
 //     and 32 columns of the chunk, turns its plane words into fp16 centroids (pw_dq.cuh) and
 //     writes them straight into tensor memory (tcgen05.st), a 4-deep ring of A buffers;
@@ -63,7 +63,6 @@ constexpr int kQueue = 8;                   // claimed work items published to t
 constexpr int kQueueReaders = kDq + kEpi + 3;  // warps that read the queue (all but the weight producer)
 constexpr int kAStages = 4;                 // tensor-memory A buffers
 constexpr int kBStagesMax = 6;              // activation stages (at most)
-constexpr int kBLow = 3;                    // activation stages below the LUT slots
 constexpr int kDenseSlabs = 16;             // a dense 32 KB A tile: 8 pieces of 2 slabs
 constexpr int kLutSlot = 32 * 1024;         // LUT slot (q <= 7); q = 8 takes both slots
 constexpr int kACols = kChunkCols / 2;      // tensor-memory columns per A buffer (fp16 pairs)
@@ -71,27 +70,22 @@ constexpr uint32_t kTmemCols = 512;
 
 // The token tiling of a launch.  Tensor memory: two accumulator buffers of TOK fp32 columns,
 // then the kAStages A buffers (2 TOK + 4 * 64 <= 512 columns).  Activation stages: TOK rows
-// by kBK columns (16 KB at most), kBK / 16 MMA K-steps each.  Decode: core-matrix layout
-// written by cp.async, the producer one stage of copies ahead of its releases.  Prefill:
-// 128-byte swizzled layout written by TMA (kTma).
+// by 64 columns in the 128-byte swizzled K-major layout (8 KB or 16 KB), four MMA K-steps
+// each; two stages make a chunk's slot.  kBLowStages of them sit below the LUT slots, the
+// rest after them.
 template <int TOK>
 struct Tiling {
   static_assert(TOK == 64 || TOK == 128, "token tile");
-  static constexpr bool kTma = TOK == 128;
   static constexpr int kAccCols = TOK;
   static constexpr uint32_t kAColBase = 2 * TOK;
-  static constexpr int kBK = TOK == 64 ? kChunkCols : kChunkCols / 2;
-  static constexpr int kBPieces = kChunkCols / kBK;  // activation stages per chunk
-  static constexpr int kBSteps = kBK / 16;           // MMA K-steps per activation stage
-  static constexpr int kBStages = TOK == 64 ? 3 : 6;
+  static constexpr int kBK = 64;                     // columns per stage: one 128-byte swizzle row
+  static constexpr int kBPieces = kChunkCols / kBK;  // stages per chunk
+  static constexpr int kBSteps = kBK / 16;           // MMA K-steps per stage
+  static constexpr int kBStages = 6;
   static constexpr int kBSlots = kBStages / kBPieces;  // per-chunk slots (one full/empty barrier pair each)
-  static constexpr int kBInFlight = 1;                 // cp.async slots issued ahead of the releases
-  static constexpr uint32_t kTmaBytes = TOK * kBK * 2;  // one TMA box
-  // descriptor start-address step (16-byte units) of one 16-column K-step inside a stage
-  static constexpr uint32_t kDescStep = kTma ? 2u : 16u;
-  static_assert(!kTma || kBK * 2 == 128, "a TMA box row is one 128-byte swizzle row");
-  static_assert(kTma || kBPieces == 1, "the cp.async path fills one stage per chunk");
-  static_assert(kBInFlight < kBSlots, "a slot must be released before its reuse is awaited");
+  static constexpr int kBLowStages = TOK == 64 ? 6 : 3;
+  static constexpr uint32_t kDescStep = 2u;  // descriptor start-address step (16 B units) of one K-step (32 B)
+  static constexpr int kBoxRows = TOK == 64 ? 16 : 128;  // rows of one TMA box
   static_assert(kAColBase + kAStages * kACols <= kTmemCols, "tensor memory");
   static_assert(kBStages <= kBStagesMax, "activation stages");
 };
@@ -99,8 +93,8 @@ constexpr long kSpinLimit = 1L << 22;
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
 // Shared-memory map.  The host fills npad_max, b_bytes and smem (the dynamic size);
-// the kernel places the regions by absolute shared address: the first kBLow activation
-// stages and the mbarriers at the start of the dynamic area, the two LUT slots at
+// the kernel places the regions by absolute shared address: the first kBLowStages
+// activation stages and the mbarriers at the start of the dynamic area, the two LUT slots at
 // [64 KB, 128 KB) (the tiled LUT layout needs a 64 KB-aligned table), then the other
 // activation stages (prefill tiling), and the slab ring to the end.
 struct TcLayout {
@@ -110,8 +104,8 @@ struct TcLayout {
   // filled in by the kernel, offsets from the dynamic area
   int slabs;       // slab ring size (even)
   int ring_off;    // slab ring
-  int b_off;       // activation stages 0 .. kBLow - 1
-  int b_hi;        // activation stages kBLow ..
+  int b_off;       // activation stages 0 .. kBLowStages - 1
+  int b_hi;        // activation stages kBLowStages ..
   int lut_off;     // LUT slots
   int bar_off;     // mbarriers
 };
@@ -135,7 +129,8 @@ struct ItemView {
   int ntok, npad;
   int row0;      // first activation row: routed slot (expert-sorted), shared token
   const BlockDev *bd;
-  const uint16_t *W;  // shared weights
+  const uint16_t *W;    // shared weights
+  const uint16_t *lut;  // routed: LUT_q of the block (tiled layout)
 };
 
 template <int PHASE>
@@ -152,6 +147,7 @@ __device__ __forceinline__ ItemView view_item(const FwdArgs &a, const WorkItem &
     v.Kc = v.bd->K;
     v.row0 = a.s.offsets[w.expert] + w.tok0;
     v.W = nullptr;
+    v.lut = v.bd->lut[v.q];
   } else {
     v.routed = false;
     v.bd = nullptr;
@@ -161,26 +157,19 @@ __device__ __forceinline__ ItemView view_item(const FwdArgs &a, const WorkItem &
     v.KC = kpad_cols(v.Kc) / kChunkCols;
     v.row0 = w.tok0;
     v.W = (PHASE == 1) ? a.lay.wgu : a.lay.wd;
+    v.lut = nullptr;
   }
   v.nr = tile_rows(w.tile, v.N);
   return v;
 }
 
-// Activation row j of an item, fp16.
-template <int PHASE>
-__device__ __forceinline__ const uint16_t *act_row(const FwdArgs &a, const ItemView &v, int j) {
-  if (PHASE == 1) {
-    const int t = v.routed ? a.s.slot_tok[v.row0 + j] : v.row0 + j;
-    return a.s.xh + (size_t)t * a.H;
-  }
-  return v.routed ? a.s.h_routed + (size_t)(v.row0 + j) * a.I : a.s.h_shared + (size_t)(v.row0 + j) * a.Is;
-}
-
 __device__ __forceinline__ uint32_t lut_base(const uint8_t *sm, const TcLayout &L) {
   return smem_u32(sm) + (uint32_t)L.lut_off;
 }
+template <int TOK>
 __device__ __forceinline__ uint32_t b_stage(const uint8_t *sm, const TcLayout &L, int s) {
-  return smem_u32(sm) + (uint32_t)(s < kBLow ? L.b_off + s * L.b_bytes : L.b_hi + (s - kBLow) * L.b_bytes);
+  constexpr int low = Tiling<TOK>::kBLowStages;
+  return smem_u32(sm) + (uint32_t)(s < low ? L.b_off + s * L.b_bytes : L.b_hi + (s - low) * L.b_bytes);
 }
 
 // LUT slot schedule, replayed identically by the weight producer and the dequantising warps:
@@ -228,10 +217,15 @@ __device__ __forceinline__ uint32_t ring_add(uint32_t a, uint32_t b, int S) {
 }
 
 // Bounded wait on an mbarrier phase; false on expiry or when another warp gave up.
+// Waiting warps back off (and look at the abort flag) every 16 polls, so that they take
+// fewer issue slots from the warps they wait for.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
   for (long i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if ((i & 15) == 15) {
+      if (*abort_flag) return false;
+      __nanosleep(64);
+    }
   }
   *abort_flag = 1;
   atomicExch(err, 1);
@@ -245,20 +239,33 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
 
 // Work items are claimed one at a time (atomic counter) by the weight producer and published,
 // in order, in a shared-memory queue that every other role reads.  Entry k of a role's
-// sequence: the item index, or -1 once the items are exhausted.
+// sequence holds the item index (-1 once the items are exhausted), the item, and the facts
+// about it that every role needs; the producer reads them from global memory once, so that
+// no other role waits on that latency.
+struct QEntry {
+  int it;
+  WorkItem w;
+  ItemView v;
+};
 struct ItemQueue {
-  volatile int *slot;  // [kQueue]
+  QEntry *slot;  // [kQueue]
   uint32_t bars;
 };
 // Reader side, one call per warp and entry (lane 0 releases the entry after the warp read it).
-// `lanes`: the lanes of the warp that run the role (all, or lane 0 alone).
-__device__ __forceinline__ int queue_read(const ItemQueue &qu, uint32_t k, unsigned lanes, volatile int *abort_flag,
-                                          int *err) {
-  if (!wait_bar(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1, abort_flag, err)) return -1;
-  const int it = qu.slot[k % kQueue];
+// `lanes`: the lanes of the warp that run the role (all, or lane 0 alone).  False once the
+// items are exhausted (or on a timeout).
+__device__ __forceinline__ bool queue_read(const ItemQueue &qu, uint32_t k, unsigned lanes, volatile int *abort_flag,
+                                           int *err, WorkItem &w, ItemView &v) {
+  if (!wait_bar(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1, abort_flag, err)) return false;
+  const QEntry &e = qu.slot[k % kQueue];
+  const int it = e.it;
+  if (it >= 0) {
+    w = e.w;
+    v = e.v;
+  }
   __syncwarp(lanes);
   if ((threadIdx.x & 31) == 0) mbar_arrive(qu.bars + 8 * (kIQE + k % kQueue));
-  return it;
+  return it >= 0;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -298,19 +305,25 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
     // claim the next work item only now that this one is needed, and publish it to the other
     // roles; entry k % kQueue is free once every reader has read its previous use
     int it = -1;
+    QEntry &e = qu.slot[k % kQueue];
     if (lane == 0) {
       ok = wait_bar(qu.bars + 8 * (kIQE + k % kQueue), ((k / kQueue) & 1) ^ 1, abort_flag, a.s.err);
       if (ok) {
         it = atomicAdd(a.s.work + (PHASE - 1), 1);
         if (it >= n_items) it = -1;
-        qu.slot[k % kQueue] = it;
+        e.it = it;
+        if (it >= 0) {
+          e.w = items[it];
+          e.v = view_item<PHASE>(a, e.w);
+        }
         mbar_arrive(qu.bars + 8 * (kIQF + k % kQueue));
       }
     }
+    __syncwarp();
     it = __shfl_sync(0xffffffffu, it, 0);
     if (it < 0) break;
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
+    const WorkItem w = e.w;
+    const ItemView v = e.v;
     // lane p < q copies plane p of every chunk; lane t < 8 copies K-step piece t of a dense tile
     const uint32_t bytes = (uint32_t)v.nr * 16;
     const uint32_t tx = v.routed ? bytes * v.q : (uint32_t)(kCtaRows * kChunkCols * 2);
@@ -367,16 +380,14 @@ template <int PHASE>
 __device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, const ItemQueue &qu,
                              volatile int *abort_flag) {
   if ((threadIdx.x & 31) != 0) return;
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t lut0 = lut_base(sm, L);
   LutSched ls;
   for (uint32_t k = 0;; ++k) {
-    const int it = queue_read(qu, k, 1u, abort_flag, a.s.err);
-    if (it < 0) break;
-    const WorkItem w = items[it];
-    if (w.kind != 0) continue;
-    const BlockDev *bd = &a.table[(a.layer * a.E + w.expert) * 2 + (PHASE - 1)];
-    const int q = bd->q;
+    WorkItem w;
+    ItemView v;
+    if (!queue_read(qu, k, 1u, abort_flag, a.s.err, w, v)) break;
+    if (!v.routed) continue;
+    const int q = v.q;
     bool both;
     const int slot = ls.next(q, both);
     bool ok = wait_bar(bars + 8 * (kLE + slot), (ls.uses[slot] & 1) ^ 1, abort_flag, a.s.err);
@@ -386,144 +397,73 @@ __device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, u
     if (both) ++ls.uses[1];
     const uint32_t lbytes = (uint32_t)lut_tile_bytes(q);
     mbar_arrive_expect_tx(bars + 8 * (kLF + slot), lbytes);
-    bulk_g2s(lut0 + slot * kLutSlot, bd->lut[q] + (size_t)w.tile * (lbytes / 2), lbytes, bars + 8 * (kLF + slot));
+    bulk_g2s(lut0 + slot * kLutSlot, v.lut + (size_t)w.tile * (lbytes / 2), lbytes, bars + 8 * (kLF + slot));
     ++ls.fills[slot];
   }
   for (int s = 0; s < 2; ++s)
     if (ls.fills[s] > 0) drain_bar(bars + 8 * (kLF + s), (ls.fills[s] - 1) & 1);
 }
 
-// The activation tiles are written with cp.async, a generic-proxy write; the MMAs read them
-// through the async proxy.  So each lane waits for its own copies of a chunk, fences them to
-// the async proxy, and only then does lane 0 release the tile, one chunk behind the copies
-// in flight so that their latency stays hidden.
-__device__ __forceinline__ void release_b(uint32_t bars, uint32_t seq, int lane, int bstages) {
-  fence_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bars + 8 * (kBF + seq % bstages));
-}
-
-// Prefill tiling: lane 0 loads each stage with one TMA box of the item's consecutive rows.
+// The activation producer: per chunk, slot b_seq % kBSlots is refilled once the MMAs of its
+// previous chunk are done; lane i loads box i (stage i / boxes, rows kBoxRows (i % boxes)
+// onward) of the item's consecutive rows, all completing on the slot's barrier.
 template <int PHASE, int TOK>
-__device__ void ab_producer_tma(const FwdArgs &a, const BMaps &bm, const TcLayout &L, uint8_t *sm, uint32_t bars,
-                                const ItemQueue &qu, volatile int *abort_flag) {
+__device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L, uint8_t *sm, uint32_t bars,
+                            const ItemQueue &qu, volatile int *abort_flag) {
   using T_ = Tiling<TOK>;
-  if ((threadIdx.x & 31) != 0) return;
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
+  const int lane = threadIdx.x & 31;
   uint32_t b_seq = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
-    const int it = queue_read(qu, k, 1u, abort_flag, a.s.err);
-    if (it < 0) break;
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
-    const TmaDesc *map = PHASE == 1 ? (v.routed ? &bm.xs : &bm.xh) : (v.routed ? &bm.h_routed : &bm.h_shared);
+    WorkItem w;
+    ItemView v;
+    if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
+    const ActMaps &mm = T_::kBoxRows == 16 ? bm.rows16 : bm.rows128;
+    const TmaDesc *map = PHASE == 1 ? (v.routed ? &mm.xs : &mm.xh) : (v.routed ? &mm.h_routed : &mm.h_shared);
+    const int rows = (v.npad + T_::kBoxRows - 1) / T_::kBoxRows * T_::kBoxRows;  // rows loaded per stage
+    const int boxes = rows / T_::kBoxRows;  // per stage
+    const bool loads = lane < T_::kBPieces * boxes;
+    const int piece = loads ? lane / boxes : 0, rb = loads ? lane % boxes : 0;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
       const int bs = b_seq % T_::kBSlots;
-      ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / T_::kBSlots) & 1) ^ 1, abort_flag, a.s.err);
+      if (lane == 0) {
+        ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / T_::kBSlots) & 1) ^ 1, abort_flag, a.s.err);
+        if (ok) mbar_arrive_expect_tx(bars + 8 * (kBF + bs), (uint32_t)(T_::kBPieces * rows * T_::kBK * 2));
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      mbar_arrive_expect_tx(bars + 8 * (kBF + bs), T_::kBPieces * T_::kTmaBytes);
-#pragma unroll
-      for (int piece = 0; piece < T_::kBPieces; ++piece)
-        tma_load_2d(b_stage(sm, L, bs * T_::kBPieces + piece), map, kc * kChunkCols + piece * T_::kBK, v.row0,
-                    bars + 8 * (kBF + bs));
+      if (loads)
+        tma_load_2d(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece) + rb * T_::kBoxRows * T_::kBK * 2, map,
+                    kc * kChunkCols + piece * T_::kBK, v.row0 + rb * T_::kBoxRows, bars + 8 * (kBF + bs));
       ++b_seq;
     }
   }
   // the last fills (the only ones whose barrier phase may still be open) land before exit
-  for (uint32_t i = b_seq > (uint32_t)T_::kBSlots ? b_seq - T_::kBSlots : 0u; i < b_seq; ++i)
-    drain_bar(bars + 8 * (kBF + i % T_::kBSlots), (i / T_::kBSlots) & 1);
+  __syncwarp();
+  if (lane == 0)
+    for (uint32_t i = b_seq > (uint32_t)T_::kBSlots ? b_seq - T_::kBSlots : 0u; i < b_seq; ++i)
+      drain_bar(bars + 8 * (kBF + i % T_::kBSlots), (i / T_::kBSlots) & 1);
 }
 
-template <int PHASE, int TOK>
-__device__ void ab_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars,
-                            const ItemQueue &qu, volatile int *abort_flag) {
-  using T_ = Tiling<TOK>;
-  constexpr int kRowSets = TOK / 16, kSegs = T_::kBK / 16;
-  const int lane = threadIdx.x & 31;
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
-  // lane L copies rows L % 16 + 16 k of the stage, 16-byte segments kSegs (L / 16) ..
-  const int r0 = lane & 15, seg0 = (lane >> 4) * kSegs;
-  uint32_t b_seq = 0, b_rel = 0;  // stages issued, stages released
-  bool ok = true;
-  for (uint32_t k = 0; ok; ++k) {
-    // Stages still in flight are released before this warp blocks on the item queue: the
-    // MMA thread needs them to finish the item, and the weight producer may be waiting for
-    // that before it publishes the next item.
-    const bool next_ready = __shfl_sync(0xffffffffu, mbar_try_wait(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1), 0);
-    if (b_rel < b_seq && !next_ready) {
-      cp_async_wait<0>();
-      for (; b_rel < b_seq; ++b_rel) release_b(bars, b_rel, lane, T_::kBSlots);
-    }
-    const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
-    if (it < 0) break;
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
-    const uint16_t *rb[kRowSets];
-#pragma unroll
-    for (int q4 = 0; q4 < kRowSets; ++q4) {
-      const int j = r0 + 16 * q4;
-      rb[q4] = j < v.ntok ? act_row<PHASE>(a, v, j) : nullptr;
-    }
-    for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const int bs = b_seq % T_::kBSlots;
-      if (lane == 0) ok = wait_bar(bars + 8 * (kBE + bs), ((b_seq / T_::kBSlots) & 1) ^ 1, abort_flag, a.s.err);
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-      const uint32_t b_tile = b_stage(sm, L, bs);
-      const int col0 = kc * kChunkCols + seg0 * 8;  // first column of the lane
-#pragma unroll
-      for (int q4 = 0; q4 < kRowSets; ++q4) {
-        const int j = r0 + 16 * q4;
-        if (16 * q4 >= v.npad) break;
-        const uint32_t dst = b_tile + core_offset(j, seg0 * 8, T_::kBK / 8);
-        const uint16_t *src = rb[q4] ? rb[q4] + col0 : nullptr;
-#pragma unroll
-        for (int sg = 0; sg < kSegs; ++sg) {
-          const bool valid = src != nullptr && col0 + sg * 8 < v.Kc;
-          cp_async16(dst + sg * 128, valid ? src + sg * 8 : a.s.xh, valid ? 16u : 0u);
-        }
-      }
-      cp_async_commit();
-      ++b_seq;
-      if (b_seq - b_rel > (uint32_t)T_::kBInFlight) {  // the oldest slot: landed, fenced, released
-        cp_async_wait<T_::kBInFlight>();
-        release_b(bars, b_rel++, lane, T_::kBSlots);
-      }
-    }
-  }
-  // the last slots (also on the way out after an abort: nothing may be left in flight)
-  cp_async_wait<0>();
-  for (; b_rel < b_seq; ++b_rel) release_b(bars, b_rel, lane, T_::kBSlots);
-}
-
-// Descriptor of K-step 0 of an activation stage: core-matrix layout (decode tiling) or
-// 128-byte swizzled rows (prefill tiling, 8-row atoms of 1 KB).  K-step t adds t kDescStep
-// to it (the start-address field, which does not overflow inside shared memory).
-template <int TOK>
-__device__ __forceinline__ uint64_t b_desc(uint32_t stage) {
-  if constexpr (Tiling<TOK>::kTma)
-    return smem_desc_sw128(stage, 1024);
-  else
-    return smem_desc(stage, 128, Tiling<TOK>::kBK * 16);
-}
+// Descriptor of K-step 0 of an activation stage: 128-byte swizzled rows in 8-row atoms of
+// 1 KB.  K-step t adds t kDescStep to it (the start-address field, which does not overflow
+// inside shared memory).
+__device__ __forceinline__ uint64_t b_desc(uint32_t stage) { return smem_desc_sw128(stage, 1024); }
 
 template <int PHASE, int TOK>
 __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                            const ItemQueue &qu, volatile int *abort_flag) {
   using T_ = Tiling<TOK>;
   if ((threadIdx.x & 31) != 0) return;
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
   const int S = L.slabs;
   RingPos pos;
   uint32_t b_seq = 0, a_seq = 0, item_seq = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
-    const int it = queue_read(qu, k, 1u, abort_flag, a.s.err);
-    if (it < 0) break;
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
+    WorkItem w;
+    ItemView v;
+    if (!queue_read(qu, k, 1u, abort_flag, a.s.err, w, v)) break;
     const uint32_t idesc = idesc_f16_f32(128, v.npad);
     const int acs = item_seq % 2;
     ok = wait_bar(bars + 8 * (kAE + acs), ((item_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
@@ -552,7 +492,7 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
         const uint32_t at = tmem + T_::kAColBase + ts * kACols;
 #pragma unroll
         for (int piece = 0; piece < T_::kBPieces; ++piece) {
-          const uint64_t bd = b_desc<TOK>(b_stage(sm, L, bs * T_::kBPieces + piece));
+          const uint64_t bd = b_desc(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece));
 #pragma unroll
           for (int t = 0; t < T_::kBSteps; ++t)
             tc_mma_f16_ta(d, at + 8 * (piece * T_::kBSteps + t), bd + t * T_::kDescStep, idesc,
@@ -561,7 +501,7 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
       } else {
 #pragma unroll
         for (int piece = 0; piece < T_::kBPieces; ++piece) {
-          const uint64_t bd = b_desc<TOK>(b_stage(sm, L, bs * T_::kBPieces + piece));
+          const uint64_t bd = b_desc(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece));
 #pragma unroll
           for (int t = 0; t < T_::kBSteps; ++t) {
             const int kt = piece * T_::kBSteps + t;
@@ -665,17 +605,15 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
                             const ItemQueue &qu, volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3, cg = warp >> 2;
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t lut0 = lut_base(sm, L);
   RingPos pos;
   uint32_t a_seq = 0;
   int pending_ts = -1;
   LutSched ls;
   for (uint32_t k = 0;; ++k) {
-    const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
-    if (it < 0) break;
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
+    WorkItem w;
+    ItemView v;
+    if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
     if (!v.routed) {  // dense chunks: only the ring position moves
       for (int kc = w.kc0; kc < w.kc1; ++kc) {
         uint32_t n, seq;
@@ -723,13 +661,11 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
                          volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   uint32_t item_seq = 0;
   for (uint32_t k = 0;; ++k) {
-    const int it = queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err);
-    if (it < 0) break;
-    const WorkItem w = items[it];
-    const ItemView v = view_item<PHASE>(a, w);
+    WorkItem w;
+    ItemView v;
+    if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
     const int acs = item_seq % 2;
     if (!wait_bar(bars + 8 * (kAF + acs), (item_seq / 2) & 1, abort_flag, a.s.err)) return;
     tc_fence_after();
@@ -776,11 +712,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ int abort_flag;
   __shared__ uint32_t tmem_slot;
-  __shared__ int queue_slot[kQueue];
+  __shared__ QEntry queue_slot[kQueue];
   const int warp = threadIdx.x >> 5;
   {  // regions by absolute shared address (see TcLayout)
     const uint32_t base = smem_u32(sm);
-    constexpr int low = T_::kBStages < kBLow ? T_::kBStages : kBLow;
+    constexpr int low = T_::kBLowStages;
     L.b_off = 0;
     L.bar_off = low * L.b_bytes;
     L.lut_off = (int)(kLutAddr - base);
@@ -788,7 +724,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
     L.ring_off = L.b_hi + (T_::kBStages - low) * L.b_bytes;
     L.slabs = L.smem > L.ring_off ? ((L.smem - L.ring_off) / kSlab) & ~1 : 0;
     // a dense chunk (16 slabs, one of padding at most) must fit the ring
-    const bool misaligned = T_::kTma && ((base + L.b_off) & 1023u) != 0u;  // swizzle atoms are 1 KB-aligned
+    const bool misaligned = ((base + L.b_off) & 1023u) != 0u;  // swizzle atoms are 1 KB-aligned
     if (base >= kLutAddr || L.bar_off + kNumBars * 8 > L.lut_off || L.slabs < kDenseSlabs + 2 || misaligned) {
       if (threadIdx.x == 0) atomicExch(a.s.err, 3);  // the map does not fit this launch
       return;
@@ -838,12 +774,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
     epilogue<PHASE, TOK>(a, bars, tmem, qu, &abort_flag);
   else if (warp == kWarpP)
     weight_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
-  else if (warp == kWarpAB) {
-    if constexpr (T_::kTma)
-      ab_producer_tma<PHASE, TOK>(a, bm, L, sm, bars, qu, &abort_flag);
-    else
-      ab_producer<PHASE, TOK>(a, L, sm, bars, qu, &abort_flag);
-  }
+  else if (warp == kWarpAB)
+    ab_producer<PHASE, TOK>(a, bm, L, sm, bars, qu, &abort_flag);
   else if (warp == kWarpMma)
     mma_issuer<PHASE, TOK>(a, L, sm, bars, tmem, qu, &abort_flag);
   else
@@ -860,13 +792,12 @@ template <int TOK>
 static int launch_tiled(const FwdArgs &a, int phase, cudaStream_t st) {
   using T_ = Tiling<TOK>;
   TcLayout L{};
-  L.npad_max = T_::kTma ? TOK : max(16, (min(a.T, TOK) + 15) / 16 * 16);  // a TMA box is always TOK rows
+  L.npad_max = TOK;
   L.b_bytes = L.npad_max * T_::kBK * 2;
-  if (T_::kTma && !a.bmaps) return (int)cudaErrorInvalidValue;
-  const BMaps bm = a.bmaps ? *a.bmaps : BMaps{};
+  if (!a.bmaps) return (int)cudaErrorInvalidValue;
+  const BMaps bm = *a.bmaps;
   L.smem = kSmemLimit;
-  const int low = T_::kBStages < kBLow ? T_::kBStages : kBLow;
-  if (low * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
+  if (T_::kBLowStages * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
   const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
   const int grid = min(max_items, a.sm_count);
   if (phase == 1) {

@@ -147,15 +147,19 @@ struct alignas(64) TmaDesc {
   unsigned char bytes[128];
 };
 
-// Tensor maps of the activation tiles of the prefill tiling: fp16, boxes of 64 columns by 128
-// rows, 128-byte swizzle (the K-major operand layout the MMAs read), rows past the end read
-// as zeros.  Rows are the scratch buffers' full capacity (max_tokens), so the maps are fixed
-// for the context.
-struct BMaps {
+// Tensor maps of the expert kernels' activation tiles: fp16, boxes of 64 columns by 16 rows
+// (decode tiling: as many boxes as an item has tokens) or by 128 rows (prefill tiling: one
+// box per stage), 128-byte swizzle (the K-major operand layout the MMAs read), rows past the
+// end read as zeros.  Rows are the scratch buffers' full capacity (max_tokens), so the maps
+// are fixed for the context.
+struct ActMaps {
   TmaDesc xs;        // [Tm*K][H] layer input gathered into expert-sorted slot order (routed gate_up)
   TmaDesc xh;        // [Tm][H] layer input (shared gate_up)
   TmaDesc h_routed;  // [Tm*K][I] (routed down)
   TmaDesc h_shared;  // [Tm][Is] (shared down)
+};
+struct BMaps {
+  ActMaps rows16, rows128;
 };
 
 struct Scratch {
@@ -172,7 +176,7 @@ struct Scratch {
   int *n_items;        // [2]
   unsigned *ticket;    // [1 + ceil(Tm/8)] router last-CTA counters: all token groups, then per group
   uint16_t *xh;        // fp16 [Tm][H]: the layer input as the experts read it (normalised under PW_PRENORM)
-  uint16_t *xs;        // fp16 [Tm*K][H]: xh rows in expert-sorted slot order (prefill tiling; null if Tm is smaller)
+  uint16_t *xs;        // fp16 [Tm*K][H]: xh rows in expert-sorted slot order
   uint16_t *h_routed;  // fp16 [Tm*K][I]
   uint16_t *h_shared;  // fp16 [Tm][Is]
   float *o_routed;     // [Tm*K][H]
@@ -202,7 +206,7 @@ struct FwdArgs {
   int *ids_out;           // optional
   float *w_out;           // optional
   int sm_count;
-  const BMaps *bmaps;     // host copy of the prefill tensor maps (null when the context has none)
+  const BMaps *bmaps;     // host copy of the activation tensor maps
 };
 
 // ev: null, or five timing events recorded before, between and after the four kernels

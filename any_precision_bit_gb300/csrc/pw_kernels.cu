@@ -70,9 +70,9 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
   }
 }
 
-// Prefill tiling: the layer input's rows in expert-sorted slot order (xs[slot] = xh[token of
-// slot]), so that every routed gate_up work item reads consecutive rows, one TMA box per
-// activation stage.  16-byte vectors, grid-stride.
+// The layer input's rows in expert-sorted slot order (xs[slot] = xh[token of slot]), so that
+// every routed gate_up work item reads consecutive rows with TMA boxes.  16-byte vectors,
+// grid-stride.
 __global__ void gather_kernel(FwdArgs a) {
   const int vec = a.H / 8;
   const long n = (long)a.T * a.K * vec;
@@ -100,9 +100,12 @@ int launch_forward(const FwdArgs &a, void *stream_, void *const *ev_) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   if (ev) record(ev[0], st);
   if (int e = launch_route(a, stream_)) return e;
-  if (tok_chunk_for(a.T) == kTokChunkPrefill) {
-    if (!a.s.xs) return (int)cudaErrorInvalidValue;
-    gather_kernel<<<a.sm_count * 4, 256, 0, st>>>(a);
+  if (!a.s.xs) return (int)cudaErrorInvalidValue;
+  {
+    const long vecs = (long)a.T * a.K * (a.H / 8);
+    const long want = (vecs + 255) / 256, cap = (long)a.sm_count * 4;
+    const int blocks = (int)(want < cap ? want : cap);
+    gather_kernel<<<blocks, 256, 0, st>>>(a);
   }
   if (ev) record(ev[1], st);
   if (int e = launch_ffn(a, 1, stream_)) return e;

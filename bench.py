@@ -419,6 +419,10 @@ def run_ours(args, shape, L, T):
         "routed_gbs": (tot["gu"] + tot["dn"]) / (ms * 1e-3) / 1e9,
         "hbm_frac": tot["total"] / (ms * 1e-3) / 1e9 / peak,
         "bytes_per_step": tot["total"], "roofline": roofline, "clocks": clk,
+        # algorithmic bytes of each layer's two expert kernels (gate_up with the shared gate_up and
+        # the input rows; down with the shared down), for comparison with per-launch DRAM counters
+        "expert_kernel_bytes_per_layer": [[b["gu"] + b["sh_gu"] + T * shape.H * 2, b["dn"] + b["sh_dn"]]
+                                          for b in bytes_l] if L <= 4 else None,
         "gpu_launches": (5 if T >= PREFILL_MIN_T else 4) * L * args.steps, "setup_s": round(t_setup, 1),
     }
     if flops is not None:
