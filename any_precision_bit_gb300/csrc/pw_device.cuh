@@ -127,6 +127,30 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Programmatic dependent launch.  pdl_wait: block until the grids this one depends on have
+// completed and their memory is visible (returns at once for a launch without a
+// programmatic dependency).  pdl_trigger: let the next grid of the stream be scheduled now;
+// it still waits in its own pdl_wait for this one to complete.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled before the
+// previous kernel of the stream has completed, and waits for it in pdl_wait.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 // TMA load of one box of a 2-D tensor map (`tmap`: the map's generic address, in kernel
 // parameter space) at element coordinates (x = column, y = row) into shared memory,
 // completing on the mbarrier.  x times the element size must be a multiple of 16 bytes.

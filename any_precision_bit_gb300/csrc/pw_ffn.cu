@@ -61,7 +61,7 @@ constexpr int kSlab = kCtaRows * 16;        // 2 KB: one plane of a 128-row tile
 constexpr int kRing = 16;                   // chunks in flight (full/empty barrier pairs)
 constexpr int kQueue = 8;                   // claimed work items published to the roles
 constexpr int kQueueReaders = kDq + kEpi + 3;  // warps that read the queue (all but the weight producer)
-constexpr int kAStages = 4;                 // tensor-memory A buffers
+constexpr int kAStagesMax = 6;              // tensor-memory A buffers (at most)
 constexpr int kBStagesMax = 6;              // activation stages (at most)
 constexpr int kDenseSlabs = 16;             // a dense 32 KB A tile: 8 pieces of 2 slabs
 constexpr int kLutSlot = 32 * 1024;         // LUT slot (q <= 7); q = 8 takes both slots
@@ -69,7 +69,7 @@ constexpr int kACols = kChunkCols / 2;      // tensor-memory columns per A buffe
 constexpr uint32_t kTmemCols = 512;
 
 // The token tiling of a launch.  Tensor memory: two accumulator buffers of TOK fp32 columns,
-// then the kAStages A buffers (2 TOK + 4 * 64 <= 512 columns).  Activation stages: TOK rows
+// then the kAStages A buffers (2 TOK + kAStages * 64 <= 512 columns).  Activation stages: TOK rows
 // by 64 columns in the 128-byte swizzled K-major layout (8 KB or 16 KB), four MMA K-steps
 // each; two stages make a chunk's slot.  kBLowStages of them sit below the LUT slots, the
 // rest after them.
@@ -86,7 +86,8 @@ struct Tiling {
   static constexpr int kBLowStages = TOK == 64 ? 6 : 3;
   static constexpr uint32_t kDescStep = 2u;  // descriptor start-address step (16 B units) of one K-step (32 B)
   static constexpr int kBoxRows = TOK == 64 ? 16 : 128;  // rows of one TMA box
-  static_assert(kAColBase + kAStages * kACols <= kTmemCols, "tensor memory");
+  static constexpr int kAStages = TOK == 64 ? 4 : 4;
+  static_assert(kAStages <= kAStagesMax && kAColBase + kAStages * kACols <= kTmemCols, "tensor memory");
   static_assert(kBStages <= kBStagesMax, "activation stages");
 };
 constexpr long kSpinLimit = 1L << 22;
@@ -114,7 +115,7 @@ constexpr uint32_t kRingAddr = 128 * 1024;
 
 // mbarrier indices
 enum {
-  kWFR = 0, kWFD = kWFR + kRing, kWE = kWFD + kRing, kTAF = kWE + kRing, kTAE = kTAF + kAStages, kBF = kTAE + kAStages,
+  kWFR = 0, kWFD = kWFR + kRing, kWE = kWFD + kRing, kTAF = kWE + kRing, kTAE = kTAF + kAStagesMax, kBF = kTAE + kAStagesMax,
   kBE = kBF + kBStagesMax, kLF = kBE + kBStagesMax, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
   kIQF = kDrain + 1, kIQE = kIQF + kQueue, kNumBars = kIQE + kQueue
 };
@@ -475,9 +476,9 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
       const uint32_t c = pos.c;
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
-      const int ts = a_seq % kAStages;
+      const int ts = a_seq % T_::kAStages;
       if (v.routed)
-        ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / kAStages) & 1, abort_flag, a.s.err);
+        ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / T_::kAStages) & 1, abort_flag, a.s.err);
       else
         ok = wait_bar(wf_bar(bars, false, seq), (seq / kRing) & 1, abort_flag, a.s.err);
       if (!ok) break;
@@ -528,16 +529,15 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
   drain_bar(bars + 8 * kDrain, 0);
 }
 
-// Dequantising thread's pending tensor-memory store: completed, made visible and signalled to
-// the MMA thread during the next chunk, so that its latency hides behind that chunk's plane
-// loads and bit transpose.
-__device__ __forceinline__ void flush_store(uint32_t bars, int &pending_ts, int lane) {
-  if (pending_ts < 0) return;
+// A dequantising warp's tensor-memory store of A buffer ts: completed (tcgen05.st reads its
+// source registers asynchronously, so they may be rewritten only after this), made visible
+// and signalled to the MMA thread at once.  Deferring the signal to the next chunk, to hide
+// the store's latency, delays the MMAs by a chunk and was measured slower.
+__device__ __forceinline__ void signal_store(uint32_t bars, int ts, int lane) {
   tmem_wait_st();
   tc_fence_before();
   __syncwarp();
-  if (lane == 0) mbar_arrive(bars + 8 * (kTAF + pending_ts));
-  pending_ts = -1;
+  if (lane == 0) mbar_arrive(bars + 8 * (kTAF + ts));
 }
 
 // One routed item for a dequantising thread: row r of the tile, columns [32 cg, 32 cg + 32)
@@ -545,7 +545,7 @@ __device__ __forceinline__ void flush_store(uint32_t bars, int &pending_ts, int 
 template <int PHASE, int TOK, int Q>
 __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, const TcLayout &L,
                         uint32_t bars, uint32_t tmem, uint32_t lut_slot, int quarter, int cg, RingPos &pos,
-                        uint32_t &a_seq, int &pending_ts, volatile int *abort_flag) {
+                        uint32_t &a_seq, volatile int *abort_flag) {
   const int lane = threadIdx.x & 31;
   const int r = 32 * quarter + lane;
   const bool rv = r < v.nr;
@@ -563,7 +563,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   for (int kc = w.kc0; kc < w.kc1; ++kc) {
     uint32_t n, seq;
     uint32_t sl = pos.take(true, Q, S, n, seq);
-    const int ts = a_seq % kAStages;
+    const int ts = a_seq % Tiling<TOK>::kAStages;
     if (!wait_bar(wf_bar(bars, true, seq), (seq / kRing) & 1, abort_flag, a.s.err)) return false;
     uint32_t W[8];
 #pragma unroll
@@ -574,29 +574,21 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
         sl = (sl + 1 == (uint32_t)S) ? 0u : sl + 1;
       }
     }
-    // tcgen05.st reads its source registers asynchronously: the previous chunk's store must
-    // be complete (flush_store) before v16 is rewritten; the plane loads and the bit
-    // transpose of this chunk overlap it
     if constexpr (Q <= kRegLutMaxQ) {
       uint32_t S4[4];
       codes_nib<Q>(W, S4);
-      flush_store(bars, pending_ts, lane);
       dq_nib<Q>(S4, Lr, v16);
     } else {
       uint32_t Y[8];
       codes_byte<Q>(W, Y);
-      flush_store(bars, pending_ts, lane);
       dq_byte<Q>(Y, lu, v16);
     }
-    if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
+    if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / Tiling<TOK>::kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
     tc_fence_after();
     tmem_st16(tmem + lane_base + Tiling<TOK>::kAColBase + ts * kACols + 16 * cg, v16);
-    pending_ts = ts;
+    signal_store(bars, ts, lane);
     ++a_seq;
   }
-  // the item's last store is signalled now: what follows may need the MMA thread to have
-  // released slabs, which it does only after this chunk's MMAs
-  flush_store(bars, pending_ts, lane);
   return true;
 }
 
@@ -608,7 +600,6 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
   const uint32_t lut0 = lut_base(sm, L);
   RingPos pos;
   uint32_t a_seq = 0;
-  int pending_ts = -1;
   LutSched ls;
   for (uint32_t k = 0;; ++k) {
     WorkItem w;
@@ -630,8 +621,7 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     switch (v.q) {
 #define PW_DQ_CASE(QQ)                                                                                       \
   case QQ:                                                                                                   \
-    ok = dq_item<PHASE, TOK, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts,     \
-                                 abort_flag);                                                                \
+    ok = dq_item<PHASE, TOK, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, abort_flag);   \
     break;
       PW_DQ_CASE(1)
       PW_DQ_CASE(2)
@@ -641,8 +631,7 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       PW_DQ_CASE(6)
       PW_DQ_CASE(7)
       default:
-        ok = dq_item<PHASE, TOK, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, pending_ts,
-                                    abort_flag);
+        ok = dq_item<PHASE, TOK, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, abort_flag);
         break;
 #undef PW_DQ_CASE
     }
@@ -737,7 +726,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kWFD + i), 1);
       mbar_init(bars + 8 * (kWE + i), 1);
     }
-    for (int i = 0; i < kAStages; ++i) {
+    for (int i = 0; i < T_::kAStages; ++i) {
       mbar_init(bars + 8 * (kTAF + i), kDq);
       mbar_init(bars + 8 * (kTAE + i), 1);
     }
@@ -766,6 +755,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // set up before the previous kernel of the stream has finished; its outputs (work items,
+  // activations) are read only after this
+  pdl_trigger();
+  pdl_wait();
   const uint32_t tmem = tmem_slot;
   const ItemQueue qu{queue_slot, bars};
   if (warp < kDq)
@@ -802,12 +795,10 @@ static int launch_tiled(const FwdArgs &a, int phase, cudaStream_t st) {
   const int grid = min(max_items, a.sm_count);
   if (phase == 1) {
     cudaFuncSetAttribute(tc_ffn_kernel<1, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    tc_ffn_kernel<1, TOK><<<grid, kTcThreads, L.smem, st>>>(a, L, bm);
-  } else {
-    cudaFuncSetAttribute(tc_ffn_kernel<2, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    tc_ffn_kernel<2, TOK><<<grid, kTcThreads, L.smem, st>>>(a, L, bm);
+    return (int)launch_pdl(tc_ffn_kernel<1, TOK>, dim3(grid), dim3(kTcThreads), (size_t)L.smem, st, a, L, bm);
   }
-  return (int)cudaGetLastError();
+  cudaFuncSetAttribute(tc_ffn_kernel<2, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  return (int)launch_pdl(tc_ffn_kernel<2, TOK>, dim3(grid), dim3(kTcThreads), (size_t)L.smem, st, a, L, bm);
 }
 
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {

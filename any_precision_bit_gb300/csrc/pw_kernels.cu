@@ -23,6 +23,8 @@ namespace pw {
 
 // ------------------------------------------------------------------ combine
 __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.x;
   const int h_begin = blockIdx.y * 1024, h_end = min(a.H, h_begin + 1024);
   const int H = a.H, K = a.K;
@@ -74,6 +76,8 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
 // every routed gate_up work item reads consecutive rows with TMA boxes.  16-byte vectors,
 // grid-stride.
 __global__ void gather_kernel(FwdArgs a) {
+  pdl_trigger();
+  pdl_wait();
   const int vec = a.H / 8;
   const long n = (long)a.T * a.K * vec;
   for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
@@ -105,14 +109,14 @@ int launch_forward(const FwdArgs &a, void *stream_, void *const *ev_) {
     const long vecs = (long)a.T * a.K * (a.H / 8);
     const long want = (vecs + 255) / 256, cap = (long)a.sm_count * 4;
     const int blocks = (int)(want < cap ? want : cap);
-    gather_kernel<<<blocks, 256, 0, st>>>(a);
+    if (cudaError_t e = launch_pdl(gather_kernel, dim3(blocks), dim3(256), 0, st, a)) return (int)e;
   }
   if (ev) record(ev[1], st);
   if (int e = launch_ffn(a, 1, stream_)) return e;
   if (ev) record(ev[2], st);
   if (int e = launch_ffn(a, 2, stream_)) return e;
   if (ev) record(ev[3], st);
-  combine_kernel<<<dim3(a.T, (a.H + 1023) / 1024), 256, 0, st>>>(a);
+  if (cudaError_t e = launch_pdl(combine_kernel, dim3(a.T, (a.H + 1023) / 1024), dim3(256), 0, st, a)) return (int)e;
   if (ev) record(ev[4], st);
   return (int)cudaGetLastError();
 }

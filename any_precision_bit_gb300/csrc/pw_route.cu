@@ -178,6 +178,10 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
     fence_mbar_init();
   }
   __syncthreads();
+  // the previous kernel of the stream (the last layer's combine) wrote x and still reads the
+  // routing scratch this kernel rewrites
+  pdl_trigger();
+  pdl_wait();
 
   // ---- logits: token rows once, router rows chunk by chunk (bulk copies on one mbarrier)
   float acc[kRtTok];
@@ -312,6 +316,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   __shared__ int s_off[257];
   __shared__ int s_itm1[257];
   __shared__ int s_itm2[257];
+  __shared__ int s_q[2][256];  // bitwidths, then item counts by rank, then first items by expert
   __shared__ int s_wsum[3][kRtWarps];
   __shared__ float s_fsum[256];
   for (int i = tid; i < kRtWarps * 256; i += kRtThreads) (&s_wc[0][0])[i] = 0;
@@ -344,7 +349,30 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
         cnt += c;
       }
     const int ch = (cnt + tc - 1) / tc;
-    int x0 = cnt, x1 = ch * tiles1, x2 = ch * tiles2;  // inclusive scans over the experts
+    // The routed work items of the experts are laid out by decreasing committed bitwidth
+    // (ties by expert id), separately for the two projections: an item's time grows with its
+    // bitwidth, and items are claimed in list order, so the longest go first and the tail of
+    // the launch is made of the shortest.
+    const BlockDev *tab = a.table + (size_t)a.layer * E * 2;
+    const int q1 = tid < E ? tab[2 * tid].q : 0, q2 = tid < E ? tab[2 * tid + 1].q : 0;
+    if (tid < E) {
+      s_q[0][tid] = q1;
+      s_q[1][tid] = q2;
+    }
+    __syncthreads();
+    int r1 = 0, r2 = 0;  // ranks in the two orders
+    if (tid < E)
+      for (int e = 0; e < E; ++e) {
+        r1 += s_q[0][e] > q1 || (s_q[0][e] == q1 && e < tid);
+        r2 += s_q[1][e] > q2 || (s_q[1][e] == q2 && e < tid);
+      }
+    __syncthreads();
+    if (tid < E) {  // item counts in rank order (the q table is no longer needed)
+      s_q[0][r1] = ch * tiles1;
+      s_q[1][r2] = ch * tiles2;
+    }
+    __syncthreads();
+    int x0 = cnt, x1 = tid < E ? s_q[0][tid] : 0, x2 = tid < E ? s_q[1][tid] : 0;  // inclusive scans
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y0 = __shfl_up_sync(0xffffffffu, x0, o);
@@ -367,16 +395,21 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
       x1 += s_wsum[1][w];
       x2 += s_wsum[2][w];
     }
-    if (tid < E) {
+    if (tid < E) {  // exclusive scans in rank order, by rank
       s_cnt[tid] = cnt;
       s_off[tid] = x0 - cnt;
-      s_itm1[tid] = sh1 + x1 - ch * tiles1;
-      s_itm2[tid] = sh2 + x2 - ch * tiles2;
+      s_itm1[tid] = sh1 + x1 - s_q[0][tid];
+      s_itm2[tid] = sh2 + x2 - s_q[1][tid];
     }
     if (tid == kRtThreads - 1) {
       s_off[E] = x0;
       s_itm1[E] = sh1 + x1;
       s_itm2[E] = sh2 + x2;
+    }
+    __syncthreads();
+    if (tid < E) {  // first item of each expert
+      s_q[0][tid] = s_itm1[r1];
+      s_q[1][tid] = s_itm2[r2];
     }
   }
   __syncthreads();
@@ -421,14 +454,14 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   for (int ee = warp; ee < E; ee += kRtWarps) {
     const int cnt = s_cnt[ee], o0 = s_off[ee];
     const int ch = (cnt + tc - 1) / tc;
-    const int n1 = s_itm1[ee + 1] - s_itm1[ee], n2 = s_itm2[ee + 1] - s_itm2[ee];
+    const int n1 = ch * tiles1, n2 = ch * tiles2, f1 = s_q[0][ee], f2 = s_q[1][ee];
     for (int i = lane; i < n1; i += 32) {
       const int c = i % ch;
-      store_item(a.s.items1 + s_itm1[ee] + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_gu, 0});
+      store_item(a.s.items1 + f1 + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_gu, 0});
     }
     for (int i = lane; i < n2; i += 32) {
       const int c = i % ch;
-      store_item(a.s.items2 + s_itm2[ee] + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_d, 0});
+      store_item(a.s.items2 + f2 + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_d, 0});
     }
     float wsum = 0.f;
     for (int sl = lane; sl < cnt; sl += 32) wsum += rs.pairs ? psw[o0 + sl] : __ldcg(psw + o0 + sl);
@@ -457,8 +490,7 @@ int launch_route(const FwdArgs &a, void *stream_) {
   if (rs.bytes > kRtMaxSmem) return (int)cudaErrorInvalidValue;
   cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtMaxSmem);
   dim3 rg((a.T + kRtTok - 1) / kRtTok, (a.E + kRtExp - 1) / kRtExp);
-  route_kernel<<<rg, kRtThreads, rs.bytes, st>>>(a);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(route_kernel, rg, dim3(kRtThreads), (size_t)rs.bytes, st, a);
 }
 
 }  // namespace pw

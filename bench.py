@@ -293,7 +293,7 @@ def run_paging(args, pw, torch, ctx, shape, L, T, stream, x0, xw, clocks_cls):
         "offloaded_bytes": moved["offload"], "reloaded_bytes": moved["reload"],
         "resident_bytes": {"start": start, "min": min(resident), "end": resident[-1]}, "clocks": clk,
         # the stack's kernels, plus one page-table commit kernel per applied bitwidth change
-        "gpu_launches": (5 if T >= PREFILL_MIN_T else 4) * L * steps + applied,
+        "gpu_launches": 5 * L * steps + applied,
     }
 
 
@@ -318,7 +318,6 @@ def run_ours(args, shape, L, T):
     x0 = torch.from_numpy(syn.gen_tokens_np(shape, args.seed, 0, T).view(np.int16)).cuda()
     xw = torch.empty_like(x0)
     torch.cuda.synchronize()
-    pw.pw_set_profiling(ctx, 1)
 
     def step():
         xw.copy_(x0)
@@ -373,8 +372,17 @@ def run_ours(args, shape, L, T):
         t = torch.tensor([ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    # kernel durations of the last timed step, per layer
+    # Kernel durations, per layer: a second timed pass with CUDA events recorded between the
+    # kernels on the launching stream.  The events serialise the kernels (the step above lets
+    # each kernel start while its predecessor drains, through programmatic dependent launch),
+    # so the step time is taken without them.
+    pw.pw_set_profiling(ctx, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, min(args.steps, 10))):
+            step()
+    stream.synchronize()
     kern = np.array([pw.pw_profile_read(ctx, l) for l in range(L)], dtype=np.float64)  # [L][4] ms
+    pw.pw_set_profiling(ctx, 0)
     bytes_l = []
     for l in range(L):
         cnt, _ = pw.pw_routing_stats(ctx, l, shape.E)
@@ -384,7 +392,8 @@ def run_ours(args, shape, L, T):
     peak, peak_kind = peaks()
     # dominant kernel: the one with the largest share of the step
     share = kern.sum(axis=0) / kern.sum()
-    names = ["route_kernel", "ffn_kernel<1> (gate_up + SiLU*up)", "ffn_kernel<2> (down)", "combine_kernel"]
+    names = ["route_kernel + gather_kernel", "tc_ffn_kernel<1> (gate_up + SiLU*up)", "tc_ffn_kernel<2> (down)",
+             "combine_kernel"]
     dom = int(np.argmax(share))
     dom_bytes = {1: tot["gu"] + tot["sh_gu"] + T * shape.H * 2 * L,
                  2: tot["dn"] + tot["sh_dn"],
@@ -423,7 +432,7 @@ def run_ours(args, shape, L, T):
         # the input rows; down with the shared down), for comparison with per-launch DRAM counters
         "expert_kernel_bytes_per_layer": [[b["gu"] + b["sh_gu"] + T * shape.H * 2, b["dn"] + b["sh_dn"]]
                                           for b in bytes_l] if L <= 4 else None,
-        "gpu_launches": (5 if T >= PREFILL_MIN_T else 4) * L * args.steps, "setup_s": round(t_setup, 1),
+        "gpu_launches": 5 * L * args.steps, "setup_s": round(t_setup, 1),
     }
     if flops is not None:
         tot_fl = (flops[1] + flops[2]) * L
