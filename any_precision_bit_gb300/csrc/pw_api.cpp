@@ -1131,8 +1131,15 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
     }
     o.mass = mass.data();
   }
+  // the offline sensitivities are per block too: the idle blocks' rows
+  if (!off->s) return fail(c, PW_ERR_INVALID, "off->s is required");
+  std::vector<double> s_sub((size_t)n * nb);
+  for (int k = 0; k < n; ++k)
+    for (int j = 0; j < nb; ++j) s_sub[(size_t)k * nb + j] = off->s[(size_t)ids[k] * nb + j];
+  pw_offline off_sub = *off;
+  off_sub.s = s_sub.data();
   pw_plan_problem prob{n, nb, L, E, c->bits, q.data(), q0.data(), ut.data(), ly.data(), ex.data(), M.data()};
-  pw_status st = pw_plan_host(&prob, &o, off, out);
+  pw_status st = pw_plan_host(&prob, &o, &off_sub, out);
   if (st != PW_OK) return fail(c, st, "planner rejected its inputs (or the plan did not fit in out->capacity)");
   for (int k = 0; k < out->n; ++k) {
     out->entries[k].block = ids[out->entries[k].block];

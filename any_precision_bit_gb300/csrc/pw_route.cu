@@ -316,7 +316,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   __shared__ int s_off[257];
   __shared__ int s_itm1[257];
   __shared__ int s_itm2[257];
-  __shared__ int s_q[2][256];  // bitwidths, then item counts by rank, then first items by expert
+  __shared__ int s_q[2][256];  // bitwidths, then item counts by rank
+  __shared__ int s_rk[2][256];  // expert of each rank
   __shared__ int s_wsum[3][kRtWarps];
   __shared__ float s_fsum[256];
   for (int i = tid; i < kRtWarps * 256; i += kRtThreads) (&s_wc[0][0])[i] = 0;
@@ -370,6 +371,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
     if (tid < E) {  // item counts in rank order (the q table is no longer needed)
       s_q[0][r1] = ch * tiles1;
       s_q[1][r2] = ch * tiles2;
+      s_rk[0][r1] = tid;
+      s_rk[1][r2] = tid;
     }
     __syncthreads();
     int x0 = cnt, x1 = tid < E ? s_q[0][tid] : 0, x2 = tid < E ? s_q[1][tid] : 0;  // inclusive scans
@@ -405,11 +408,6 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
       s_off[E] = x0;
       s_itm1[E] = sh1 + x1;
       s_itm2[E] = sh2 + x2;
-    }
-    __syncthreads();
-    if (tid < E) {  // first item of each expert
-      s_q[0][tid] = s_itm1[r1];
-      s_q[1][tid] = s_itm2[r2];
     }
   }
   __syncthreads();
@@ -447,22 +445,31 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
                  WorkItem{1, 0, tile, c * tc, min(tc, T - c * tc), part * per, min(total, (part + 1) * per), part});
     }
   }
+  // routed work items, one thread each: item i of a projection belongs to the expert whose
+  // rank's range [first[r], first[r + 1]) holds it; within an expert, (row tile, token
+  // chunk) with the token chunks of a row tile consecutive, so that CTAs claiming them
+  // together share the tile's planes in L2
+  for (int u = 0; u < 2; ++u) {
+    const int *first = u ? s_itm2 : s_itm1;
+    WorkItem *dst = u ? a.s.items2 : a.s.items1;
+    for (int i = (u ? sh2 : sh1) + tid; i < first[E]; i += kRtThreads) {
+      int lo = 0, hi = E - 1;  // the largest rank r with first[r] <= i
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (first[mid] <= i)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      const int ee = s_rk[u][lo], cnt = s_cnt[ee], ch = (cnt + tc - 1) / tc, loc = i - first[lo];
+      const int c = loc % ch;
+      store_item(dst + i, WorkItem{0, ee, loc / ch, c * tc, min(tc, cnt - c * tc), 0, u ? kc_d : kc_gu, 0});
+    }
+  }
   __syncthreads();  // every slot weight is in place
-  // per expert (one warp each): its (row tile, token chunk) work items and its routing
-  // statistics, the slot weights summed in a fixed order.  The token chunks of a row tile are
-  // consecutive items, so that CTAs claiming them together share the tile's planes in L2.
+  // per expert (one warp each): its routing statistics, the slot weights summed in a fixed order
   for (int ee = warp; ee < E; ee += kRtWarps) {
     const int cnt = s_cnt[ee], o0 = s_off[ee];
-    const int ch = (cnt + tc - 1) / tc;
-    const int n1 = ch * tiles1, n2 = ch * tiles2, f1 = s_q[0][ee], f2 = s_q[1][ee];
-    for (int i = lane; i < n1; i += 32) {
-      const int c = i % ch;
-      store_item(a.s.items1 + f1 + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_gu, 0});
-    }
-    for (int i = lane; i < n2; i += 32) {
-      const int c = i % ch;
-      store_item(a.s.items2 + f2 + i, WorkItem{0, ee, i / ch, c * tc, min(tc, cnt - c * tc), 0, kc_d, 0});
-    }
     float wsum = 0.f;
     for (int sl = lane; sl < cnt; sl += 32) wsum += rs.pairs ? psw[o0 + sl] : __ldcg(psw + o0 + sl);
 #pragma unroll

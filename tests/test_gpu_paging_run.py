@@ -246,3 +246,31 @@ def test_paging_run_full_size_spot_checks():
         assert pw.pw_memory(st.ctx).resident_bytes == st.resident_bytes_eq3()
     finally:
         pw.pw_destroy(st.ctx)
+
+
+def test_planner_leaves_blocks_in_transit_out():
+    """Blocks whose pages are in transfer take no planner step, and the other blocks keep
+    their own offline sensitivities (the problem is re-indexed over the idle blocks)."""
+    st = Stack(MINI, L=1)
+    try:
+        off = offline_inputs(st)
+        for step in range(3):  # routing statistics for Eq. 1
+            st.forward(0, st.tokens(step, 0))
+        pw.pw_set_fault(st.ctx, 3, 1)  # transfers stay in flight while held
+        E = MINI.E
+        moved = [syn.block_id(0, e, 0, E) for e in (0, 5, 11, 17)]
+        for b in moved:
+            pw.pw_offload(st.ctx, b, 3)
+        start = pw.pw_memory(st.ctx).resident_bytes
+        obs = dict(T_blk=T_BLK, F_blk=0, B_KV=0.25 * start, R=R, mass=None, phi=syn.gen_phi_np(st.n_blocks, 0, 7))
+        want = oracle_plan(st, off, obs)
+        plan = pw.pw_plan_step(st.ctx, st.n_blocks, obs, off)
+        assert (plan["kind"], plan["stage"], plan["D"]) == want[:3]
+        assert plan["entries"] == want[3]
+        assert plan["kind"] == 1 and plan["entries"]
+        assert not set(moved) & {blk for blk, _, _, _ in plan["entries"]}
+        pw.pw_set_fault(st.ctx, 3, 0)
+        pw.pw_sync_io(st.ctx)
+        pw.pw_commit(st.ctx)
+    finally:
+        pw.pw_destroy(st.ctx)
