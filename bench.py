@@ -52,6 +52,12 @@ def parse():
 
 PREFILL_MIN_T = 512  # batches of at least this many tokens run the prefill tiling (tensor-bound)
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of one launch) per
+# algorithmic byte of that launch, for the expert kernels: (phase, prefill tiling) -> ratio.
+# Taken on the two-layer Qwen-shaped decode run and the one-layer Mixtral-shaped prefill run
+# of this kernel version; to be measured again whenever the kernel changes.
+TRAFFIC_PER_ALGORITHMIC_BYTE = {(1, False): 1.040, (2, False): 1.052, (1, True): 1.321, (2, True): 2.889}
+
 
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -401,8 +407,10 @@ def run_ours(args, shape, L, T):
                  3: T * shape.H * 2 * L}[dom]
     dom_ms = kern[:, dom].sum()
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    ratio = TRAFFIC_PER_ALGORITHMIC_BYTE.get((dom, T >= PREFILL_MIN_T)) if dom in (1, 2) else None
     roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": ratio * dom_bytes / L if ratio else None,
                 "algorithmic_bytes_per_launch": dom_bytes / L, "avg_launch_ms": dom_ms / L,
                 "kernel_share": {n: float(s) for n, s in zip(names, share)}}
     flops = None
