@@ -11,7 +11,9 @@ Readings where the pages are silent:
 * top-K keeps the K largest p, ties to the lower expert id, listed by descending p;
 * expert activation is SiLU(gate) * up with gate rows [0, I) and up rows [I, 2I) of the
   gate_up block; silu(g) = g / (1 + exp(-g));
-* the shared expert is a dense FFN of the same form added to every token, ungated;
+* the shared expert is a dense FFN of the same form added to every token, ungated by
+  default; with ``shared_gate`` (a vector w_g of length H) its output is scaled per token by
+  sigmoid(x . w_g), the gated shared expert of the Qwen1.5-MoE model in the pages' Table 1;
 * with ``prenorm`` the layer reads RMSNorm(x) = x / sqrt(mean(x^2) + 1e-6) with unit
   gain, as the pre-norm transformers of the pages' model table (Table 1) feed their MoE
   blocks; the caller adds the output to the un-normalised x.
@@ -90,13 +92,18 @@ def expert_ffn(xe: np.ndarray, Wgu: np.ndarray, Wd: np.ndarray) -> np.ndarray:
     return h @ Wd.T
 
 
+def sigmoid(g: np.ndarray) -> np.ndarray:
+    return 1.0 / (1.0 + np.exp(-g))
+
+
 def moe_layer(x_bits: np.ndarray, Wr, bias, experts, q: np.ndarray, K: int, bmax: int,
-              shared=None, renorm: bool = False, tokens=None, prenorm: bool = False):
+              shared=None, renorm: bool = False, tokens=None, prenorm: bool = False, shared_gate=None):
     """Forward of one MoE layer in float64.
 
     experts: dict e -> (gu_idx, gu_luts, d_idx, d_luts); only routed experts are needed.
     q: int [E][2] committed bitwidths (gate_up, down).
     shared: None or (wgu_bits [2Is][H], wd_bits [H][Is]) bf16.
+    shared_gate: None or float [H]: the shared output is scaled by sigmoid(x . shared_gate).
     tokens: optional subset of token rows to evaluate (rows are independent).
     Returns (y float64 [T'][H], ids [T'][K], weights [T'][K]).
     """
@@ -119,5 +126,8 @@ def moe_layer(x_bits: np.ndarray, Wr, bias, experts, q: np.ndarray, K: int, bmax
     for k in range(K):  # routing-weighted accumulation in k order
         y += w[:, k:k + 1] * o[:, k, :]
     if shared is not None:
-        y += expert_ffn(x, bf16_to_f64(shared[0]), bf16_to_f64(shared[1]))
+        ys = expert_ffn(x, bf16_to_f64(shared[0]), bf16_to_f64(shared[1]))
+        if shared_gate is not None:
+            ys = sigmoid(x @ np.asarray(shared_gate, dtype=np.float64))[:, None] * ys
+        y += ys
     return y, ids, w

@@ -62,7 +62,7 @@ def test_router_bias_and_renorm():
     assert np.array_equal(ids, ids2) and np.all(w2 < w + 1e-15)
 
 
-def _brute_layer(x_bits, Wr, bias, experts, q, K, bmax, shared):
+def _brute_layer(x_bits, Wr, bias, experts, q, K, bmax, shared, gate=None):
     """Per-output-element loops in a different order from the oracle: each weight is read
     from its code with Python integer bit operations, each dot product summed by hand."""
     T, H = x_bits.shape
@@ -109,8 +109,12 @@ def _brute_layer(x_bits, Wr, bias, experts, q, K, bmax, shared):
                 g = sum(wgu[n, h] * x[t, h] for h in range(H))
                 u = sum(wgu[Is + n, h] * x[t, h] for h in range(H))
                 hs.append(g / (1.0 + math.exp(-g)) * u)
+            scale = 1.0
+            if gate is not None:
+                z = sum(x[t, h] * float(gate[h]) for h in range(H))
+                scale = 1.0 / (1.0 + math.exp(-z))
             for m in range(H):
-                out[t, m] += sum(wd[m, n] * hs[n] for n in range(Is))
+                out[t, m] += scale * sum(wd[m, n] * hs[n] for n in range(Is))
     return out
 
 
@@ -171,3 +175,34 @@ def test_rmsnorm_and_prenorm_layer():
     assert np.array_equal(ids1, ids2)
     # eps = 1e-6 against mean(x^2) ~ 1 perturbs the scale by ~eps/2
     assert np.allclose(y1, y2, rtol=1e-5, atol=1e-9)
+
+
+def test_gated_shared_expert():
+    """Sigmoid-gated shared expert: brute force with a random gate, and the closed forms
+    sigmoid(0) = 1/2 (the shared output exactly halved) and a saturated gate (ungated)."""
+    shape = syn.LayerShape("gate", H=16, E=4, I=8, K=2, Is=8, L=1, bmax=6, bits=(3, 4, 5, 6), sigma_lut=0.2,
+                           zipf_a=1.0, q_rule="uniform")
+    seed = 12
+    Wr, bias, _ = syn.gen_router_np(shape, seed, 0)
+    x = syn.gen_tokens_np(shape, seed, 0, 3)
+    experts = {}
+    for e in range(shape.E):
+        gi, gl = syn.gen_block_np(shape, seed, 0, e, 0)
+        di, dl = syn.gen_block_np(shape, seed, 0, e, 1)
+        experts[e] = (gi, gl, di, dl)
+    q = syn.gen_q_assignment(shape, seed, 0)
+    shared = syn.gen_shared_np(shape, seed, 0)
+    gate = np.random.default_rng(3).normal(0.0, 0.5, size=shape.H)
+    y, _, _ = moe.moe_layer(x, Wr, bias, experts, q, shape.K, shape.bmax, shared=shared, shared_gate=gate)
+    ref = _brute_layer(x, Wr, bias, experts, q, shape.K, shape.bmax, shared, gate)
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-14)
+    y_none, _, _ = moe.moe_layer(x, Wr, bias, experts, q, shape.K, shape.bmax)
+    y_full, _, _ = moe.moe_layer(x, Wr, bias, experts, q, shape.K, shape.bmax, shared=shared)
+    y_half, _, _ = moe.moe_layer(x, Wr, bias, experts, q, shape.K, shape.bmax, shared=shared,
+                                 shared_gate=np.zeros(shape.H))
+    assert np.allclose(y_half - y_none, 0.5 * (y_full - y_none), rtol=1e-12, atol=1e-15)
+    xf = moe.bf16_to_f64(x)
+    sat = 60.0 * np.linalg.lstsq(xf, np.ones(xf.shape[0]), rcond=None)[0]  # x . sat = 60 for every token
+    assert np.allclose(xf @ sat, 60.0)
+    y_sat, _, _ = moe.moe_layer(x, Wr, bias, experts, q, shape.K, shape.bmax, shared=shared, shared_gate=sat)
+    assert np.allclose(y_sat, y_full, rtol=1e-12, atol=1e-14)
