@@ -86,6 +86,7 @@ _SIGS = {
     "pw_pack": [_P, _I, _I, _I, _P, _P, _I],
     "pw_set_router": [_P, _I, _P, _P],
     "pw_set_shared": [_P, _I, _P, _P],
+    "pw_set_shared_gate": [_P, _I, _P],
     "pw_moe_forward": [_P, _I, _P, _I, _P, _P, _P, _I, _P],
     "pw_check": [_P],
     "pw_stack_forward": [_P, _P, _I, _P],
@@ -203,6 +204,12 @@ def pw_set_router(ctx, layer, Wr, bias=None):
 
 def pw_set_shared(ctx, layer, wgu, wd):
     _check(lib().pw_set_shared(ctx, layer, _ptr(wgu), _ptr(wd)), ctx)
+
+
+def pw_set_shared_gate(ctx, layer, wsg=None):
+    if wsg is not None and not hasattr(wsg, "data_ptr"):
+        wsg = np.ascontiguousarray(wsg, dtype=np.float32)
+    _check(lib().pw_set_shared_gate(ctx, layer, _ptr(wsg)), ctx)
 
 
 def pw_moe_forward(ctx, layer, x, T, y, ids=None, w=None, flags=0, stream=None):

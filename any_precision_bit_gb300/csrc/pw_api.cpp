@@ -399,7 +399,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.h_shared, sizeof(uint16_t) * Tm * std::max(d.Is, 1)) &&
             salloc((void **)&c->s.o_routed, sizeof(float) * TK * d.H) &&
             salloc((void **)&c->s.o_shared, sizeof(float) * nsplit * Tm * d.H) &&
-            salloc((void **)&c->s.inv_rms, sizeof(float) * Tm) &&
+            salloc((void **)&c->s.inv_rms, sizeof(float) * Tm) && salloc((void **)&c->s.sgate, sizeof(float) * Tm) &&
             salloc((void **)&c->s.xh, sizeof(uint16_t) * Tm * d.H) &&
             salloc((void **)&c->s.err, sizeof(int)) && salloc((void **)&c->s.work, sizeof(int) * 2) &&
             salloc((void **)&c->s.stat_count, sizeof(double) * d.L * d.E) &&
@@ -451,6 +451,7 @@ void pw_destroy(pw_ctx *c) {
     cudaFree(const_cast<float *>(l.bias));
     cudaFree(const_cast<uint16_t *>(l.wgu));
     cudaFree(const_cast<uint16_t *>(l.wd));
+    cudaFree(const_cast<float *>(l.wsg));
   }
   for (void *p : c->scratch_allocs) cudaFree(p);
   if (c->stage) cudaFree(c->stage);
@@ -638,6 +639,28 @@ pw_status pw_set_shared(pw_ctx *c, int layer, const uint16_t *wgu, const uint16_
   CU(c, cudaStreamSynchronize(c->compute));
   if (bad) return fail(c, PW_ERR_INVALID, "%d shared-expert weights exceed the fp16 range (|w| > 65504)", bad);
   c->shared_set[layer] = 1;
+  return PW_OK;
+}
+
+pw_status pw_set_shared_gate(pw_ctx *c, int layer, const float *wsg) {
+  if (!c) return fail(nullptr, PW_ERR_INVALID, "null context");
+  if (layer < 0 || layer >= c->d.L) return fail(c, PW_ERR_INVALID, "layer out of range");
+  if (c->d.Is == 0) return fail(c, PW_ERR_INVALID, "this context has no shared expert (Is = 0)");
+  cudaSetDevice(c->d.device);
+  LayerDev &l = c->layers[layer];
+  CU(c, cudaStreamSynchronize(c->compute));  // no launch in flight reads the old gate
+  if (!wsg) {
+    cudaFree(const_cast<float *>(l.wsg));
+    l.wsg = nullptr;
+    drop_graphs(c);  // captured launches hold the old layer description
+    return PW_OK;
+  }
+  if (!l.wsg) {
+    CU(c, cudaMalloc((void **)&l.wsg, sizeof(float) * c->d.H));
+    drop_graphs(c);
+  }
+  CU(c, cudaMemcpyAsync(const_cast<float *>(l.wsg), wsg, sizeof(float) * c->d.H, cudaMemcpyDefault, c->compute));
+  CU(c, cudaStreamSynchronize(c->compute));
   return PW_OK;
 }
 

@@ -182,6 +182,7 @@ struct Scratch {
   float *o_routed;     // [Tm*K][H]
   float *o_shared;     // [splits][T][H] partial sums of the shared down projection
   float *inv_rms;      // [Tm] per-token 1/rms of the layer input (PW_PRENORM)
+  float *sgate;        // [Tm] per-token shared-expert gate sigmoid(x . w_sg) (layers with a gate)
   double *stat_count;  // [L][E]
   double *stat_wsum;   // [L][E]
   int *err;            // [1] bounded-wait timeouts in the expert kernels (0 = none)
@@ -194,6 +195,7 @@ struct LayerDev {
   const float *bias;       // [E] or null
   const uint16_t *wgu;     // shared gate_up, fp16, frag16 layout (dev rows interleaved)
   const uint16_t *wd;      // shared down, fp16, frag16 layout
+  const float *wsg;        // [H] shared-expert gate, or null (ungated)
 };
 
 struct FwdArgs {

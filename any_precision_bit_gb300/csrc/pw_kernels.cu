@@ -55,10 +55,11 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
         sh.z += sv.z;
         sh.w += sv.w;
       }
-      acc.x += sh.x;
-      acc.y += sh.y;
-      acc.z += sh.z;
-      acc.w += sh.w;
+      const float g = a.lay.wsg ? a.s.sgate[t] : 1.f;  // the shared-expert gate, when the layer has one
+      acc.x = fmaf(g, sh.x, acc.x);
+      acc.y = fmaf(g, sh.y, acc.y);
+      acc.z = fmaf(g, sh.z, acc.z);
+      acc.w = fmaf(g, sh.w, acc.w);
     }
     uint2 *yp = reinterpret_cast<uint2 *>(a.y + (size_t)t * H + h);
     if (a.flags & 1) {

@@ -207,17 +207,28 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
       // unit-gain RMSNorm of the layer input (PW_PRENORM): one warp per staged token
       if (warp < nt) {
         float ss = 0.f;
+        const float *wsg = blockIdx.y == 0 ? a.lay.wsg : nullptr;  // shared-expert gate
+        float gz = 0.f;
         for (int h = lane * 2; h < H; h += 64) {
           const uint32_t v = *reinterpret_cast<const uint32_t *>(xs + warp * H + h);
           const float a0 = bf16f(v & 0xFFFF), a1 = bf16f(v >> 16);
           ss = fmaf(a0, a0, fmaf(a1, a1, ss));
+          if (wsg) {
+            const float2 g = *reinterpret_cast<const float2 *>(wsg + h);
+            gz = fmaf(a0, g.x, fmaf(a1, g.y, gz));
+          }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        for (int o = 16; o > 0; o >>= 1) {
+          ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          gz += __shfl_xor_sync(0xffffffffu, gz, o);
+        }
         const float inv = (a.flags & 2) ? rsqrtf(ss / (float)H + 1e-6f) : 1.0f;
         if (lane == 0) {
           s_inv[warp] = inv;
           if (blockIdx.y == 0) a.s.inv_rms[t0 + warp] = inv;
+          // the gate reads the layer input as the experts do (normalised under PW_PRENORM)
+          if (wsg) a.s.sgate[t0 + warp] = 1.f / (1.f + expf(-gz * inv));
         }
       }
       if (blockIdx.y == 0) {  // the experts' fp16 input rows

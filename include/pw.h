@@ -118,6 +118,14 @@ pw_status pw_set_router(pw_ctx *ctx, int layer, const float *Wr, const float *bi
  * error below 2^-25); PW_ERR_INVALID if a weight exceeds 65504 in magnitude. */
 pw_status pw_set_shared(pw_ctx *ctx, int layer, const uint16_t *wgu, const uint16_t *wd);
 
+/* Gate the shared expert of `layer`: its output for token t is scaled by
+ * sigmoid(x_t . wsg), x_t the layer input as the experts read it (RMS-normalised under
+ * PW_PRENORM), computed in fp32 by the router.  This is the shared-expert gate of the
+ * Qwen1.5-MoE model in Table 1; the pages describe no gating, so layers are ungated until
+ * this is called.  wsg: fp32 [H], host or device, copied; NULL removes the gate.  Waits for
+ * the context's stream.  PW_ERR_INVALID if the context has no shared expert. */
+pw_status pw_set_shared_gate(pw_ctx *ctx, int layer, const float *wsg);
+
 /* ---------------------------------------------------------------- forward */
 
 /* One fused MoE layer (Sec. 3.3 "fused mixed-precision MoE kernel"): router logits in

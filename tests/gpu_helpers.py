@@ -89,10 +89,10 @@ class LayerData:
         if self.shared is not None:
             pw.pw_set_shared(ctx, layer_slot, self.shared[0], self.shared[1])
 
-    def oracle(self, q=None, tokens=None, renorm=False):
+    def oracle(self, q=None, tokens=None, renorm=False, shared_gate=None):
         return omoe.moe_layer(self.x, self.Wr, self.bias, self.experts, self.q if q is None else q,
                               self.shape.K, self.shape.bmax, shared=self.shared, renorm=renorm, tokens=tokens,
-                              prenorm=self.prenorm)
+                              prenorm=self.prenorm, shared_gate=shared_gate)
 
 
 def bf16_to_f64(a):

@@ -189,6 +189,30 @@ def test_prenorm_layer(name, T):
         pw.pw_destroy(ctx)
 
 
+@pytest.mark.parametrize("name,T,prenorm", [("qwen", 16, False), ("qwen", 64, True)])
+def test_gated_shared_expert(name, T, prenorm):
+    """The shared expert scaled per token by sigmoid(x . w_sg); removing the gate restores the
+    ungated layer."""
+    shape = syn.SHAPES[name]
+    data = LayerData(shape, 8, 0, T, prenorm=prenorm)
+    wsg = np.random.default_rng(8).normal(0.0, 2.0 / np.sqrt(shape.H), size=shape.H)
+    ctx = make_ctx(pw, shape, L=1, max_tokens=T)
+    try:
+        data.load(pw, ctx)
+        flags = pw.PW_PRENORM if prenorm else 0
+        pw.pw_set_shared_gate(ctx, 0, wsg.astype(np.float32))
+        y, _, _ = run_layer(ctx, data, T, flags=flags)
+        y_ref, _, _ = data.oracle(shared_gate=wsg.astype(np.float32).astype(np.float64))
+        assert_close(y, y_ref, f"gated {name} T={T}")
+        y_plain_ref, _, _ = data.oracle()
+        assert not np.allclose(y_ref, y_plain_ref, rtol=1e-2)  # the gate matters at this scale
+        pw.pw_set_shared_gate(ctx, 0, None)
+        y2, _, _ = run_layer(ctx, data, T, flags=flags)
+        assert_close(y2, y_plain_ref, f"ungated again {name} T={T}")
+    finally:
+        pw.pw_destroy(ctx)
+
+
 def test_routing_statistics_match_eq1_inputs():
     shape = syn.SHAPES["tiny"]
     T = shape.decode_T[0]
