@@ -41,6 +41,30 @@ def routing_mass(ids: np.ndarray, weights: np.ndarray, E: int) -> np.ndarray:
     return num / float(np.sum(weights, dtype=np.float64))
 
 
+def routed_input_features(x: np.ndarray, ids: np.ndarray, weights: np.ndarray, E: int) -> np.ndarray:
+    """Eq. 5's phi for every expert e (shared by its two linear blocks): over the tokens t
+    routed to e with weight r_t, with n_t = ||x_t||_2 the norm of the expert's input row,
+    (sum r n / sum r, sqrt(sum r n^2 / sum r), max n); zeros for an expert no token reached.
+    x: float [T][H] (the input as the experts read it)."""
+    phi = np.zeros((E, 3), dtype=np.float64)
+    s0 = np.zeros(E)
+    s1 = np.zeros(E)
+    s2 = np.zeros(E)
+    mx = np.zeros(E)
+    for t in range(ids.shape[0]):
+        n = math.sqrt(sum(float(v) * float(v) for v in x[t]))
+        for k in range(ids.shape[1]):
+            e, r = int(ids[t, k]), float(weights[t, k])
+            s0[e] += r
+            s1[e] += r * n
+            s2[e] += r * n * n
+            mx[e] = max(mx[e], n)
+    for e in range(E):
+        if s0[e] > 0:
+            phi[e] = (s1[e] / s0[e], math.sqrt(s2[e] / s0[e]), mx[e])
+    return phi
+
+
 def sensitivity(h: np.ndarray, W: np.ndarray, Wb: np.ndarray) -> float:
     """Eq. 2: s^b = sum_j h_j (W_j - W^b_j)^2."""
     h = np.asarray(h, dtype=np.float64)

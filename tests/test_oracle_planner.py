@@ -117,3 +117,9 @@ def test_reload_restores_most_damaging_first():
     none, _ = pl.reload_plan(blocks, [5, 5], np.array([[0.5, 0.5]]), np.zeros((2, 3)), off,
                              T_blk=16, F_blk=20, B_KV=1.0, R=8)
     assert none == {}
+
+
+def test_eq5_features_hand_example():
+    g = load_golden("eq5_features.json")
+    phi = pl.routed_input_features(np.array(g["x"]), np.array(g["ids"]), np.array(g["weights"]), g["E"])
+    assert np.allclose(phi, np.array(g["phi"]), rtol=1e-14, atol=0)
