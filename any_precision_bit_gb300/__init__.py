@@ -87,6 +87,7 @@ _SIGS = {
     "pw_set_router": [_P, _I, _P, _P],
     "pw_set_shared": [_P, _I, _P, _P],
     "pw_set_shared_gate": [_P, _I, _P],
+    "pw_routing_features": [_P, _I, _P, _I],
     "pw_moe_forward": [_P, _I, _P, _I, _P, _P, _P, _I, _P],
     "pw_check": [_P],
     "pw_stack_forward": [_P, _P, _I, _P],
@@ -235,6 +236,12 @@ def pw_routing_stats(ctx, layer, E, reset=False):
     return cnt, ws
 
 
+def pw_routing_features(ctx, layer, E, reset=False):
+    phi = np.zeros((E, 3), dtype=np.float64)
+    _check(lib().pw_routing_features(ctx, layer, _ptr(phi), int(reset)), ctx)
+    return phi
+
+
 def pw_set_bits(ctx, block, q):
     _check(lib().pw_set_bits(ctx, block, q), ctx)
 
@@ -377,7 +384,7 @@ def pw_plan_step(ctx, n_blocks, obs: dict, off: dict):
         return a.ctypes.data
     o = pw_obs(T_blk=int(obs["T_blk"]), F_blk=int(obs["F_blk"]), B_KV=float(obs["B_KV"]), R=int(obs.get("R", 0)),
                mass=arr(obs["mass"], np.float64) if obs.get("mass") is not None else None,
-               phi=arr(obs["phi"], np.float64))
+               phi=arr(obs["phi"], np.float64) if obs.get("phi") is not None else None)
     f = _offline_struct(off, keep)
     entries = (pw_plan_entry * n_blocks)()
     plan = pw_plan(entries=C.cast(entries, C.POINTER(pw_plan_entry)), capacity=n_blocks)

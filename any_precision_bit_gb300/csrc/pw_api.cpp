@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -400,6 +401,8 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.o_routed, sizeof(float) * TK * d.H) &&
             salloc((void **)&c->s.o_shared, sizeof(float) * nsplit * Tm * d.H) &&
             salloc((void **)&c->s.inv_rms, sizeof(float) * Tm) && salloc((void **)&c->s.sgate, sizeof(float) * Tm) &&
+            salloc((void **)&c->s.xnorm, sizeof(float) * Tm) &&
+            salloc((void **)&c->s.stat_phi, sizeof(double) * 4 * d.L * d.E) &&
             salloc((void **)&c->s.xh, sizeof(uint16_t) * Tm * d.H) &&
             salloc((void **)&c->s.err, sizeof(int)) && salloc((void **)&c->s.work, sizeof(int) * 2) &&
             salloc((void **)&c->s.stat_count, sizeof(double) * d.L * d.E) &&
@@ -430,6 +433,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
   cudaMemset(c->s.work, 0, sizeof(int) * 2);
   cudaMemset(c->s.stat_count, 0, sizeof(double) * d.L * d.E);
   cudaMemset(c->s.stat_wsum, 0, sizeof(double) * d.L * d.E);
+  cudaMemset(c->s.stat_phi, 0, sizeof(double) * 4 * d.L * d.E);
   if (cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     fail(nullptr, PW_ERR_CUDA, "context initialisation failed");
@@ -784,6 +788,36 @@ pw_status pw_routing_stats(pw_ctx *c, int layer, double *count, double *weight_s
   return check_sticky(c);
 }
 
+// Eq. 5 features of `layer`'s experts from the device sums: phi[e] = (sum r n / sum r,
+// sqrt(sum r n^2 / sum r), max n), zeros where no token was routed.
+static pw_status read_features(pw_ctx *c, int layer, double *phi, int reset) {
+  const int E = c->d.E;
+  std::vector<double> raw((size_t)4 * E);
+  const size_t off = (size_t)layer * E * 4;
+  CU(c, cudaMemcpy(raw.data(), c->s.stat_phi + off, sizeof(double) * 4 * E, cudaMemcpyDeviceToHost));
+  for (int e = 0; e < E; ++e) {
+    const double *r = &raw[(size_t)e * 4];
+    double *o = phi + (size_t)e * 3;
+    if (r[0] > 0) {
+      o[0] = r[1] / r[0];
+      o[1] = std::sqrt(r[2] / r[0]);
+      o[2] = r[3];
+    } else {
+      o[0] = o[1] = o[2] = 0.0;
+    }
+  }
+  if (reset) CU(c, cudaMemset(c->s.stat_phi + off, 0, sizeof(double) * 4 * E));
+  return PW_OK;
+}
+
+pw_status pw_routing_features(pw_ctx *c, int layer, double *phi, int reset) {
+  if (!c || !phi) return fail(c, PW_ERR_INVALID, "null argument");
+  if (layer < 0 || layer >= c->d.L) return fail(c, PW_ERR_INVALID, "layer out of range");
+  CU(c, cudaStreamSynchronize(c->compute));
+  if (pw_status st = read_features(c, layer, phi, reset)) return st;
+  return check_sticky(c);
+}
+
 // ================================================================== page table
 pw_status pw_set_bits(pw_ctx *c, int block, int q) {
   if (!c) return fail(nullptr, PW_ERR_INVALID, "null context");
@@ -1117,7 +1151,19 @@ pw_status pw_dequant(pw_ctx *c, int block, int b, uint16_t *host_out) {
 pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_plan *out) {
   if (!c || !obs || !off || !out) return fail(c, PW_ERR_INVALID, "null argument");
   if (off->n_bits != c->n_bits) return fail(c, PW_ERR_INVALID, "offline table has %d bitwidths, context %d", off->n_bits, c->n_bits);
-  if (!obs->phi) return fail(c, PW_ERR_INVALID, "obs->phi is required");
+  std::vector<double> dev_phi;  // obs->phi == NULL: the device's routed-input features (Eq. 5)
+  if (!obs->phi) {
+    CU(c, cudaStreamSynchronize(c->compute));
+    std::vector<double> lay((size_t)c->d.E * 3);
+    dev_phi.resize(c->blocks.size() * 3);
+    for (int l = 0; l < c->d.L; ++l) {
+      if (pw_status st = read_features(c, l, lay.data(), 0)) return st;
+      for (size_t i = 0; i < c->blocks.size(); ++i)
+        if (c->blocks[i].layer == l)
+          for (int j = 0; j < 3; ++j) dev_phi[i * 3 + j] = lay[(size_t)c->blocks[i].expert * 3 + j];
+    }
+  }
+  const double *obs_phi = obs->phi ? obs->phi : dev_phi.data();
   const int nb = c->n_bits, L = c->d.L, E = c->d.E;
   // A block whose pages are still in transfer (or whose landed reload awaits pw_commit)
   // cannot take another step yet: the problem holds the idle blocks only.
@@ -1138,7 +1184,7 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
     ly[k] = b.layer;
     ex[k] = b.expert;
     for (int j = 0; j < nb; ++j) M[(size_t)k * nb + j] = (double)block_M(c, b, c->bits[j]);
-    for (int j = 0; j < 3; ++j) phi[(size_t)k * 3 + j] = obs->phi[(size_t)ids[k] * 3 + j];
+    for (int j = 0; j < 3; ++j) phi[(size_t)k * 3 + j] = obs_phi[(size_t)ids[k] * 3 + j];
   }
   std::vector<double> mass;
   pw_obs o = *obs;

@@ -183,8 +183,10 @@ struct Scratch {
   float *o_shared;     // [splits][T][H] partial sums of the shared down projection
   float *inv_rms;      // [Tm] per-token 1/rms of the layer input (PW_PRENORM)
   float *sgate;        // [Tm] per-token shared-expert gate sigmoid(x . w_sg) (layers with a gate)
+  float *xnorm;        // [Tm] per-token L2 norm of the layer input as the experts read it
   double *stat_count;  // [L][E]
   double *stat_wsum;   // [L][E]
+  double *stat_phi;    // [L][E][4] routed-input sums for Eq. 5: sum r, sum r n, sum r n^2, max n
   int *err;            // [1] bounded-wait timeouts in the expert kernels (0 = none)
   int *work;           // [2] next unclaimed work item of the two expert kernels (reset by the router)
   int max_items1, max_items2;

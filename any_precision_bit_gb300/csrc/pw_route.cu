@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
           if (blockIdx.y == 0) a.s.inv_rms[t0 + warp] = inv;
           // the gate reads the layer input as the experts do (normalised under PW_PRENORM)
           if (wsg) a.s.sgate[t0 + warp] = 1.f / (1.f + expf(-gz * inv));
+          if (blockIdx.y == 0) a.s.xnorm[t0 + warp] = sqrtf(ss) * inv;
         }
       }
       if (blockIdx.y == 0) {  // the experts' fp16 input rows
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   __shared__ int s_rk[2][256];  // expert of each rank
   __shared__ int s_wsum[3][kRtWarps];
   __shared__ float s_fsum[256];
+  __shared__ float s_phi[3][256];  // per expert: sum r n, sum r n^2, max n
   for (int i = tid; i < kRtWarps * 256; i += kRtThreads) (&s_wc[0][0])[i] = 0;
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
@@ -478,20 +480,45 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
     }
   }
   __syncthreads();  // every slot weight is in place
-  // per expert (one warp each): its routing statistics, the slot weights summed in a fixed order
+  // per expert (one warp each): its routing statistics and the sums behind Eq. 5's routed-
+  // input features, over its slots in a fixed order (n = the token's input norm)
   for (int ee = warp; ee < E; ee += kRtWarps) {
     const int cnt = s_cnt[ee], o0 = s_off[ee];
-    float wsum = 0.f;
-    for (int sl = lane; sl < cnt; sl += 32) wsum += rs.pairs ? psw[o0 + sl] : __ldcg(psw + o0 + sl);
+    float wsum = 0.f, s1 = 0.f, s2 = 0.f, mx = 0.f;
+    for (int sl = lane; sl < cnt; sl += 32) {
+      const float r = rs.pairs ? psw[o0 + sl] : __ldcg(psw + o0 + sl);
+      const float n = __ldcg(a.s.xnorm + a.s.slot_tok[o0 + sl]);
+      wsum += r;
+      s1 = fmaf(r, n, s1);
+      s2 = fmaf(r * n, n, s2);
+      mx = fmaxf(mx, n);
+    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-    if (lane == 0) s_fsum[ee] = wsum;
+    for (int o = 16; o > 0; o >>= 1) {
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (lane == 0) {
+      s_fsum[ee] = wsum;
+      s_phi[0][ee] = s1;
+      s_phi[1][ee] = s2;
+      s_phi[2][ee] = mx;
+    }
   }
   __syncthreads();
   // the running statistics: one thread per expert, every read-modify-write in flight at once
   for (int ee = tid; ee < E; ee += kRtThreads) {
     a.s.stat_count[(size_t)a.layer * E + ee] += (double)s_cnt[ee];
     a.s.stat_wsum[(size_t)a.layer * E + ee] += (double)s_fsum[ee];
+    if (a.s.stat_phi && s_cnt[ee] > 0) {
+      double *ph = a.s.stat_phi + ((size_t)a.layer * E + ee) * 4;
+      ph[0] += (double)s_fsum[ee];
+      ph[1] += (double)s_phi[0][ee];
+      ph[2] += (double)s_phi[1][ee];
+      ph[3] = fmax(ph[3], (double)s_phi[2][ee]);
+    }
   }
   if (tid == 0) {
     *a.s.ticket = 0u;

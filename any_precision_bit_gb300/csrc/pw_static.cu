@@ -64,6 +64,8 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
       sizeof(double) * a.E,         // stat_count (discarded)
       sizeof(double) * a.E,         // stat_wsum (discarded)
       sizeof(uint16_t) * T * a.H,   // xh: the fp16 expert input the router also writes
+      sizeof(float) * T,            // xnorm: per-token input norms
+      sizeof(float) * T,            // sgate: per-token shared-expert gates (gated layers)
   };
   size_t need = 0;
   for (size_t s : sizes) need += align256(s);
@@ -112,6 +114,8 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   s.stat_count = reinterpret_cast<double *>(take(sizes[13]));
   s.stat_wsum = reinterpret_cast<double *>(take(sizes[14]));
   s.xh = reinterpret_cast<uint16_t *>(take(sizes[15]));
+  s.xnorm = reinterpret_cast<float *>(take(sizes[16]));
+  s.sgate = reinterpret_cast<float *>(take(sizes[17]));
   s.max_items1 = (int)n1;
   s.max_items2 = (int)n2;
   a.s = s;

@@ -165,6 +165,14 @@ pw_status pw_stack_forward_host(pw_ctx *ctx, const void *x_host, int T, void *y_
 pw_status pw_routing_stats(pw_ctx *ctx, int layer, double *count, double *weight_sum,
                            int reset);
 
+/* Routed-input features phi of Eq. 5 (Sec. 3.2 "Prompt residual"), per expert of `layer`,
+ * over every forward call since the last reset: with n_t the L2 norm of token t's input as
+ * the experts read it (RMS-normalised under PW_PRENORM) and r the routing weight of each
+ * (token, k) selection of the expert, phi[e] = (sum r n / sum r, sqrt(sum r n^2 / sum r),
+ * max n); zeros for an expert no token reached.  Both linear blocks of an expert share its
+ * phi.  Output host double [E][3].  Waits for the compute stream. */
+pw_status pw_routing_features(pw_ctx *ctx, int layer, double *phi, int reset);
+
 /* Tracing: while on, every forward records five CUDA timing events per layer, before,
  * between and after its four kernels (router, gate_up, down, combine), on the launch
  * stream; stack graphs captured while on contain the event records.  The events are
@@ -257,7 +265,8 @@ typedef struct {
     int R;              /* reload margin in blocks (reload when F_blk >= T_blk + R) */
     const double *mass; /* [L][E] routing mass (Eq. 1), or NULL: use the context's
                            online routing statistics (pw_plan_step only) */
-    const double *phi;  /* [n_blocks][3] routed-input features (Eq. 5) */
+    const double *phi;  /* [n_blocks][3] routed-input features (Eq. 5), or NULL: the
+                           context's device features, pw_routing_features (pw_plan_step only) */
 } pw_obs;
 
 typedef struct {

@@ -213,6 +213,43 @@ def test_gated_shared_expert(name, T, prenorm):
         pw.pw_destroy(ctx)
 
 
+@pytest.mark.parametrize("prenorm", [False, True])
+def test_routed_input_features_match_eq5(prenorm):
+    """Eq. 5's phi per expert from the device sums, against the oracle's definition on the
+    oracle's routing of the same tokens; the planner reads them when obs->phi is NULL."""
+    from oracle import planner as opl
+    shape = syn.SHAPES["qwen"]
+    T = 16
+    data = LayerData(shape, 9, 0, T, prenorm=prenorm)
+    ctx = make_ctx(pw, shape, L=1, max_tokens=T)
+    try:
+        data.load(pw, ctx)
+        flags = pw.PW_PRENORM if prenorm else 0
+        for _ in range(2):  # the same tokens twice: the ratios and the maximum are unchanged
+            run_layer(ctx, data, T, flags=flags)
+        phi = pw.pw_routing_features(ctx, 0, shape.E)
+        ids, w, _ = omoe.route(data.x, data.Wr, data.bias, shape.K, prenorm=prenorm)
+        xin = bf16_to_f64(data.x)
+        if prenorm:
+            xin = omoe.rmsnorm(xin)
+        ref = opl.routed_input_features(xin, ids, w, shape.E)
+        assert np.allclose(phi, ref, rtol=1e-4, atol=1e-6)
+        assert (phi[:, 0] > 0).sum() == len(set(ids.ravel().tolist()))
+        # the planner's default features are these, expanded to both blocks of each expert
+        n = shape.E * 2
+        off = syn.gen_planner_offline_np(n, list(shape.bits), 4, 3)
+        off["n_stages"] = 3
+        obs = dict(T_blk=16, F_blk=2, B_KV=1.0e6, R=8, mass=None, phi=None)
+        p_dev = pw.pw_plan_step(ctx, n, obs, off)
+        obs["phi"] = np.repeat(phi, 2, axis=0)
+        p_exp = pw.pw_plan_step(ctx, n, obs, off)
+        assert p_dev == p_exp and p_dev["entries"]
+        pw.pw_routing_features(ctx, 0, shape.E, reset=True)
+        assert not pw.pw_routing_features(ctx, 0, shape.E).any()
+    finally:
+        pw.pw_destroy(ctx)
+
+
 def test_routing_statistics_match_eq1_inputs():
     shape = syn.SHAPES["tiny"]
     T = shape.decode_T[0]
