@@ -128,11 +128,40 @@ class Blocks:
         return self.bits.index(b)
 
 
+def merge_request_signals(requests, kv_blocks):
+    """Batched serving (Sec. 3.2): the request-level routing masses, prompt residuals,
+    confidence scores and clipping bounds merged into one batch-level table, each averaged
+    with the requests' KV-block usage as weights (w_r = kv_r / sum kv, summed in request
+    order).  requests: dicts with mass [L][E], rho_hat [n_blocks][n_bits-1], conf
+    [2][n_bits-1], rho_min, rho_max."""
+    tot = 0.0
+    for kv in kv_blocks:
+        tot += float(kv)
+    w = [float(kv) / tot for kv in kv_blocks]
+    out = {}
+    for key in ("mass", "rho_hat", "conf"):
+        acc = np.zeros_like(np.asarray(requests[0][key], dtype=np.float64))
+        for wr, r in zip(w, requests):
+            acc = acc + wr * np.asarray(r[key], dtype=np.float64)
+        out[key] = acc
+    for key in ("rho_min", "rho_max"):
+        acc = 0.0
+        for wr, r in zip(w, requests):
+            acc = acc + wr * float(r[key])
+        out[key] = acc
+    return out
+
+
 def score_step(blocks: Blocks, i: int, j: int, beta_i: int, phi_i, off) -> tuple:
-    """d_hat and Delta of block i stepping from level j to level j-1."""
+    """d_hat and Delta of block i stepping from level j to level j-1.  With a batch-level
+    table (off["rho_hat"], merged residuals), the residual is read from it instead of the
+    Eq. 5 head on phi."""
     u = blocks.utype[i]
     g = global_damage(blocks.s[i, j - 1], blocks.s[i, j])
-    rho = residual_head(off["head_w"][u][j - 1], off["head_a"][u][j - 1], phi_i)
+    if "rho_hat" in off:
+        rho = float(off["rho_hat"][i][j - 1])
+    else:
+        rho = residual_head(off["head_w"][u][j - 1], off["head_a"][u][j - 1], phi_i)
     eta = prompt_factor(off["alpha"], off["head_c"][u][j - 1], rho, off["rho_min"], off["rho_max"])
     d_hat = predicted_damage(off["eps"], off["mu"][beta_i], g, eta)
     delta = blocks.M[i, j] - blocks.M[i, j - 1]

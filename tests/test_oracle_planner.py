@@ -123,3 +123,41 @@ def test_eq5_features_hand_example():
     g = load_golden("eq5_features.json")
     phi = pl.routed_input_features(np.array(g["x"]), np.array(g["ids"]), np.array(g["weights"]), g["E"])
     assert np.allclose(phi, np.array(g["phi"]), rtol=1e-14, atol=0)
+
+
+def test_batch_merge_hand_example():
+    g = load_golden("batch_merge.json")
+    m = pl.merge_request_signals(g["requests"], g["kv_blocks"])
+    for key in ("mass", "rho_hat", "conf"):
+        assert np.allclose(m[key], np.array(g["merged"][key]), rtol=1e-15, atol=1e-15), key
+    assert m["rho_min"] == pytest.approx(g["merged"]["rho_min"], abs=1e-15)
+    assert m["rho_max"] == pytest.approx(g["merged"]["rho_max"], abs=1e-15)
+
+
+def test_single_request_merge_is_identity_and_residual_table_matches_heads():
+    """Merging one request changes nothing, and a residual table equal to the Eq. 5 heads'
+    predictions gives the same plan as the heads on phi."""
+    rng = np.random.default_rng(4)
+    n, bits = 12, [3, 4, 5, 6]
+    nb = len(bits)
+    q = rng.choice(bits, size=n)
+    utype = np.arange(n) % 2
+    layer = np.zeros(n, dtype=int)
+    expert = np.arange(n) // 2
+    M = np.array([[b * 1000.0 + 50.0 * (1 << b) for b in bits] for _ in range(n)])
+    s = -np.sort(-rng.lognormal(0.0, 1.0, size=(n, nb)), axis=1)
+    off = dict(s=s, head_w=rng.normal(0, 0.5, (2, nb - 1, 3)), head_a=rng.normal(0, 0.5, (2, nb - 1)),
+               head_c=rng.uniform(0.5, 1.0, (2, nb - 1)), alpha=1.0, rho_min=-2.0, rho_max=2.0,
+               mu=[4.0, 2.0, 1.0, 0.5], floors=[3, 3, 3, 3], eps=1e-12)
+    phi = np.abs(rng.normal(1.0, 0.5, (n, 3)))
+    mass = rng.dirichlet(np.ones(6))[None, :]
+    rho = np.array([[pl.residual_head(off["head_w"][utype[i]][j], off["head_a"][utype[i]][j], phi[i])
+                     for j in range(nb - 1)] for i in range(n)])
+    req = dict(mass=mass, rho_hat=rho, conf=off["head_c"], rho_min=off["rho_min"], rho_max=off["rho_max"])
+    m = pl.merge_request_signals([req], [5.0])
+    assert np.array_equal(m["rho_hat"], rho) and np.array_equal(m["mass"], mass)
+    blocks = pl.Blocks(bits, q, utype, layer, expert, M, s)
+    _, chosen_heads, _ = pl.plan_step(blocks, mass, phi, off, 3, 16, 2, 3000.0)
+    off_table = dict(off, rho_hat=m["rho_hat"], head_c=m["conf"], rho_min=m["rho_min"], rho_max=m["rho_max"])
+    _, chosen_table, _ = pl.plan_step(blocks, m["mass"], phi, off_table, 3, 16, 2, 3000.0)
+    assert chosen_heads == chosen_table
