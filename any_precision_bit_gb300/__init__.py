@@ -49,7 +49,12 @@ class pw_mem_info(C.Structure):
 
 class pw_obs(C.Structure):
     _fields_ = [("T_blk", C.c_int), ("F_blk", C.c_int), ("B_KV", C.c_double), ("R", C.c_int),
-                ("mass", C.c_void_p), ("phi", C.c_void_p)]
+                ("mass", C.c_void_p), ("phi", C.c_void_p), ("rho_hat", C.c_void_p)]
+
+
+class pw_request_signals(C.Structure):
+    _fields_ = [("mass", C.c_void_p), ("rho_hat", C.c_void_p), ("conf", C.c_void_p), ("rho_min", C.c_double),
+                ("rho_max", C.c_double), ("kv_blocks", C.c_double)]
 
 
 class pw_offline(C.Structure):
@@ -103,6 +108,8 @@ _SIGS = {
     "pw_set_fault": [_P, _I, _I],
     "pw_plan_host": [C.POINTER(pw_plan_problem), C.POINTER(pw_obs), C.POINTER(pw_offline), C.POINTER(pw_plan)],
     "pw_plan_step": [_P, C.POINTER(pw_obs), C.POINTER(pw_offline), C.POINTER(pw_plan)],
+    "pw_merge_requests": [C.POINTER(pw_request_signals), _I, _I, _I, _I, _I, _P, _P, _P, C.POINTER(C.c_double),
+                          C.POINTER(C.c_double)],
     "pw_route_noalloc": [_P, _I, _P, _I, _P, _P, _I, _P],
     "pw_set_profiling": [_P, _I],
     "pw_profile_read": [_P, _I, _P],
@@ -366,7 +373,9 @@ def pw_plan_host(bits, q, q_init, utype, layer, expert, M, L, E, obs: dict, off:
                            q_init=arr(q_init, np.int32), utype=arr(utype, np.int32), layer=arr(layer, np.int32),
                            expert=arr(expert, np.int32), M=arr(M, np.float64))
     o = pw_obs(T_blk=int(obs["T_blk"]), F_blk=int(obs["F_blk"]), B_KV=float(obs["B_KV"]), R=int(obs.get("R", 0)),
-               mass=arr(obs["mass"], np.float64), phi=arr(obs["phi"], np.float64))
+               mass=arr(obs["mass"], np.float64),
+               phi=arr(obs["phi"], np.float64) if obs.get("phi") is not None else None,
+               rho_hat=arr(obs["rho_hat"], np.float64) if obs.get("rho_hat") is not None else None)
     f = _offline_struct(off, keep)
     cap = capacity if capacity is not None else max(n, 1)
     entries = (pw_plan_entry * cap)()
@@ -384,9 +393,32 @@ def pw_plan_step(ctx, n_blocks, obs: dict, off: dict):
         return a.ctypes.data
     o = pw_obs(T_blk=int(obs["T_blk"]), F_blk=int(obs["F_blk"]), B_KV=float(obs["B_KV"]), R=int(obs.get("R", 0)),
                mass=arr(obs["mass"], np.float64) if obs.get("mass") is not None else None,
-               phi=arr(obs["phi"], np.float64) if obs.get("phi") is not None else None)
+               phi=arr(obs["phi"], np.float64) if obs.get("phi") is not None else None,
+               rho_hat=arr(obs["rho_hat"], np.float64) if obs.get("rho_hat") is not None else None)
     f = _offline_struct(off, keep)
     entries = (pw_plan_entry * n_blocks)()
     plan = pw_plan(entries=C.cast(entries, C.POINTER(pw_plan_entry)), capacity=n_blocks)
     _check(lib().pw_plan_step(ctx, C.byref(o), C.byref(f), C.byref(plan)), ctx)
     return _plan_result(plan, entries)
+
+
+def pw_merge_requests(requests, kv_blocks, L, E, n_blocks, n_bits):
+    """requests: dicts with mass [L][E], rho_hat [n_blocks][n_bits-1], conf [2][n_bits-1],
+    rho_min, rho_max; kv_blocks: one weight per request.  Returns the merged table as a dict."""
+    keep = []
+
+    def arr(v):
+        a = np.ascontiguousarray(v, dtype=np.float64)
+        keep.append(a)
+        return a.ctypes.data
+    reqs = (pw_request_signals * len(requests))()
+    for r, (q, kv) in enumerate(zip(requests, kv_blocks)):
+        reqs[r] = pw_request_signals(mass=arr(q["mass"]), rho_hat=arr(q["rho_hat"]), conf=arr(q["conf"]),
+                                     rho_min=float(q["rho_min"]), rho_max=float(q["rho_max"]), kv_blocks=float(kv))
+    mass = np.zeros((L, E))
+    rho = np.zeros((n_blocks, n_bits - 1))
+    conf = np.zeros((2, n_bits - 1))
+    lo, hi = C.c_double(), C.c_double()
+    _check(lib().pw_merge_requests(reqs, len(requests), L, E, n_blocks, n_bits, _ptr(mass), _ptr(rho), _ptr(conf),
+                                   C.byref(lo), C.byref(hi)))
+    return dict(mass=mass, rho_hat=rho, conf=conf, rho_min=lo.value, rho_max=hi.value)

@@ -50,7 +50,9 @@ def build(verbose: bool = False, force: bool = False) -> str:
     for src in sorted(glob.glob(os.path.join(CSRC, "*.cpp"))):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
         objs.append(obj)
-        jobs.append(["g++", "-std=c++17", "-O2", "-fPIC", "-Wall", *inc, "-c", src, "-o", obj])
+        # no fused multiply-add contraction: the host arithmetic (planner) rounds each
+        # operation on its own on every target, as numpy does
+        jobs.append(["g++", "-std=c++17", "-O2", "-ffp-contract=off", "-fPIC", "-Wall", *inc, "-c", src, "-o", obj])
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(HERE, "..", "include", "*.h"))
     newest_src = max(os.path.getmtime(p) for p in headers + [j[-3] for j in jobs])
     if not force and os.path.exists(OUT) and os.path.getmtime(OUT) > newest_src:

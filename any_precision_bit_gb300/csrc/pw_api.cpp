@@ -1152,7 +1152,7 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
   if (!c || !obs || !off || !out) return fail(c, PW_ERR_INVALID, "null argument");
   if (off->n_bits != c->n_bits) return fail(c, PW_ERR_INVALID, "offline table has %d bitwidths, context %d", off->n_bits, c->n_bits);
   std::vector<double> dev_phi;  // obs->phi == NULL: the device's routed-input features (Eq. 5)
-  if (!obs->phi) {
+  if (!obs->phi && !obs->rho_hat) {
     CU(c, cudaStreamSynchronize(c->compute));
     std::vector<double> lay((size_t)c->d.E * 3);
     dev_phi.resize(c->blocks.size() * 3);
@@ -1163,7 +1163,7 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
           for (int j = 0; j < 3; ++j) dev_phi[i * 3 + j] = lay[(size_t)c->blocks[i].expert * 3 + j];
     }
   }
-  const double *obs_phi = obs->phi ? obs->phi : dev_phi.data();
+  const double *obs_phi = obs->phi ? obs->phi : dev_phi.empty() ? nullptr : dev_phi.data();
   const int nb = c->n_bits, L = c->d.L, E = c->d.E;
   // A block whose pages are still in transfer (or whose landed reload awaits pw_commit)
   // cannot take another step yet: the problem holds the idle blocks only.
@@ -1175,7 +1175,7 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
   }
   const int n = (int)ids.size();
   std::vector<int> q(n), q0(n), ut(n), ly(n), ex(n);
-  std::vector<double> M((size_t)n * nb), phi((size_t)n * 3);
+  std::vector<double> M((size_t)n * nb), phi((size_t)n * 3), rho(obs->rho_hat ? (size_t)n * (nb - 1) : 0);
   for (int k = 0; k < n; ++k) {
     const HostBlock &b = c->blocks[ids[k]];
     q[k] = b.q;
@@ -1184,11 +1184,15 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
     ly[k] = b.layer;
     ex[k] = b.expert;
     for (int j = 0; j < nb; ++j) M[(size_t)k * nb + j] = (double)block_M(c, b, c->bits[j]);
-    for (int j = 0; j < 3; ++j) phi[(size_t)k * 3 + j] = obs_phi[(size_t)ids[k] * 3 + j];
+    if (obs_phi)
+      for (int j = 0; j < 3; ++j) phi[(size_t)k * 3 + j] = obs_phi[(size_t)ids[k] * 3 + j];
+    if (obs->rho_hat)
+      for (int j = 0; j < nb - 1; ++j) rho[(size_t)k * (nb - 1) + j] = obs->rho_hat[(size_t)ids[k] * (nb - 1) + j];
   }
   std::vector<double> mass;
   pw_obs o = *obs;
-  o.phi = phi.data();
+  o.phi = obs_phi ? phi.data() : nullptr;
+  o.rho_hat = obs->rho_hat ? rho.data() : nullptr;
   if (!o.mass) {  // Eq. 1 from the online routing statistics
     CU(c, cudaStreamSynchronize(c->compute));
     mass.resize((size_t)L * E);

@@ -4,6 +4,7 @@
 //   D       = max{0, T_blk + 1 - F_blk} * B_KV                           (Eq. 7)
 //   g       = max{s^{b'} - s^b, 0}                                       (Eq. 4)
 //   rho_hat = w_u^{b->b'} . phi_i + a_u^{b->b'}                          (Eq. 5)
+//             (or read from a batch-level table, obs->rho_hat)
 //   eta     = exp(alpha * c_u^{b->b'} * clip(rho_hat, rho_min, rho_max)) (Eq. 6)
 //   d_hat   = max{eps, mu_beta * g * eta}                                (Eq. 8)
 //   Delta   = M^b - M^{b'}                                               (Eq. 3)
@@ -54,11 +55,15 @@ void score(const Ctx &c, int i, int j, double *d_hat, double *delta) {
   const int nb = p->n_bits, u = p->utype[i], tr = j - 1;
   const double s_hi = f->s[(size_t)i * nb + j], s_lo = f->s[(size_t)i * nb + j - 1];
   const double g = std::max(s_lo - s_hi, 0.0);
-  const double *w = f->head_w + ((size_t)u * (nb - 1) + tr) * 3;
-  const double *phi = c.o->phi + (size_t)i * 3;
   double rho = 0.0;
-  for (int m = 0; m < 3; ++m) rho = rho + w[m] * phi[m];
-  rho = rho + f->head_a[(size_t)u * (nb - 1) + tr];
+  if (c.o->rho_hat) {
+    rho = c.o->rho_hat[(size_t)i * (nb - 1) + tr];
+  } else {
+    const double *w = f->head_w + ((size_t)u * (nb - 1) + tr) * 3;
+    const double *phi = c.o->phi + (size_t)i * 3;
+    for (int m = 0; m < 3; ++m) rho = rho + w[m] * phi[m];
+    rho = rho + f->head_a[(size_t)u * (nb - 1) + tr];
+  }
   const double cl = std::min(std::max(rho, f->rho_min), f->rho_max);
   const double eta = std::exp(f->alpha * f->head_c[(size_t)u * (nb - 1) + tr] * cl);
   *d_hat = std::max(f->eps, f->mu[c.beta[i]] * g * eta);
@@ -168,7 +173,8 @@ pw_status emit(const Ctx &c, const StagePlan &sp, int kind, int stage, double D,
 extern "C" pw_status pw_plan_host(const pw_plan_problem *p, const pw_obs *o, const pw_offline *f, pw_plan *out) {
   if (!p || !o || !f || !out || (!out->entries && out->capacity > 0)) return PW_ERR_INVALID;
   if (p->n_blocks < 0 || p->n_bits < 1 || p->n_bits != f->n_bits || p->L < 1 || p->E < 1) return PW_ERR_INVALID;
-  if (!p->bits || !p->q || !p->utype || !p->layer || !p->expert || !p->M || !o->phi || !o->mass) return PW_ERR_INVALID;
+  if (!p->bits || !p->q || !p->utype || !p->layer || !p->expert || !p->M || !(o->phi || o->rho_hat) || !o->mass)
+    return PW_ERR_INVALID;
   if (!f->s || !f->head_w || !f->head_a || !f->head_c || !f->mu || !f->floors) return PW_ERR_INVALID;
   if (f->n_buckets < 1 || f->n_stages < 1) return PW_ERR_INVALID;
   Ctx c{p, o, f, {}, {}, {}};
@@ -219,4 +225,32 @@ extern "C" pw_status pw_plan_host(const pw_plan_problem *p, const pw_obs *o, con
   none.to_level.assign(n, -1);
   none.released.assign(n, 0.0);
   return emit(c, none, 0, -1, D, out);
+}
+
+extern "C" pw_status pw_merge_requests(const pw_request_signals *req, int n_req, int L, int E, int n_blocks,
+                                       int n_bits, double *mass, double *rho_hat, double *conf, double *rho_min,
+                                       double *rho_max) {
+  if (!req || n_req < 1 || L < 1 || E < 1 || n_blocks < 0 || n_bits < 1) return PW_ERR_INVALID;
+  if (!mass || !rho_hat || !conf || !rho_min || !rho_max) return PW_ERR_INVALID;
+  double tot = 0.0;
+  for (int r = 0; r < n_req; ++r) {
+    if (!req[r].mass || !req[r].rho_hat || !req[r].conf || !(req[r].kv_blocks >= 0.0)) return PW_ERR_INVALID;
+    tot += req[r].kv_blocks;
+  }
+  if (!(tot > 0.0)) return PW_ERR_INVALID;
+  const size_t nm = (size_t)L * E, nr = (size_t)n_blocks * (n_bits - 1), nc = (size_t)2 * (n_bits - 1);
+  for (size_t i = 0; i < nm; ++i) mass[i] = 0.0;
+  for (size_t i = 0; i < nr; ++i) rho_hat[i] = 0.0;
+  for (size_t i = 0; i < nc; ++i) conf[i] = 0.0;
+  *rho_min = 0.0;
+  *rho_max = 0.0;
+  for (int r = 0; r < n_req; ++r) {
+    const double w = req[r].kv_blocks / tot;
+    for (size_t i = 0; i < nm; ++i) mass[i] = mass[i] + w * req[r].mass[i];
+    for (size_t i = 0; i < nr; ++i) rho_hat[i] = rho_hat[i] + w * req[r].rho_hat[i];
+    for (size_t i = 0; i < nc; ++i) conf[i] = conf[i] + w * req[r].conf[i];
+    *rho_min = *rho_min + w * req[r].rho_min;
+    *rho_max = *rho_max + w * req[r].rho_max;
+  }
+  return PW_OK;
 }

@@ -267,6 +267,9 @@ typedef struct {
                            online routing statistics (pw_plan_step only) */
     const double *phi;  /* [n_blocks][3] routed-input features (Eq. 5), or NULL: the
                            context's device features, pw_routing_features (pw_plan_step only) */
+    const double *rho_hat; /* [n_blocks][n_bits-1] prompt residuals, transition j = bits[j+1] ->
+                           bits[j], or NULL: Eq. 5 from phi.  A batch-level table from
+                           pw_merge_requests (Sec. 3.2, batched serving); phi is then unused */
 } pw_obs;
 
 typedef struct {
@@ -317,6 +320,26 @@ typedef struct {
  * restored first while the bytes fit in (F_blk - T_blk - R) * B_KV).  Host only. */
 pw_status pw_plan_host(const pw_plan_problem *prob, const pw_obs *obs,
                        const pw_offline *off, pw_plan *out);
+
+/* One request's planner signals, for the batch-level merge. */
+typedef struct {
+    const double *mass;      /* [L][E] the request's routing mass (Eq. 1) */
+    const double *rho_hat;   /* [n_blocks][n_bits-1] its prompt residuals (Eq. 5) */
+    const double *conf;      /* [2][n_bits-1] its confidence scores c_u^{b->b'} (Eq. 6) */
+    double rho_min, rho_max; /* its clipping bounds (Eq. 6) */
+    double kv_blocks;        /* KV blocks the request holds: its weight in the merge */
+} pw_request_signals;
+
+/* Batched serving (Sec. 3.2): "the planner first merges request-level signals into one
+ * batch-level table".  Routing masses, prompt residuals, confidence scores and clipping
+ * bounds are each averaged with weights kv_blocks / sum(kv_blocks), requests summed in
+ * order.  Outputs (caller storage): mass [L][E], rho_hat [n_blocks][n_bits-1], conf
+ * [2][n_bits-1], *rho_min, *rho_max; plan with them by passing rho_hat in pw_obs and conf
+ * and the bounds in pw_offline.  PW_ERR_INVALID if n_req < 1, a pointer is NULL, a weight
+ * is negative or the weights do not sum to a positive number.  Host only. */
+pw_status pw_merge_requests(const pw_request_signals *req, int n_req, int L, int E, int n_blocks,
+                            int n_bits, double *mass, double *rho_hat, double *conf, double *rho_min,
+                            double *rho_max);
 
 /* PlanStep on the context's page table (q_i, M_i^b) and, when obs->mass is NULL, its
  * online routing statistics (Eq. 1).  Blocks with a page transfer in flight, or a landed

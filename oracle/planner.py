@@ -184,7 +184,7 @@ def greedy_select(blocks: Blocks, beta_blk, phi, off, cap: int, D: float):
             return
         if lvl[i] - (j - 1) > cap:
             return
-        d_hat, delta = score_step(blocks, i, j, beta_blk[i], phi[i], off)
+        d_hat, delta = score_step(blocks, i, j, beta_blk[i], None if phi is None else phi[i], off)
         heapq.heappush(heap, (d_hat / delta, -delta, i, d_hat, delta))
 
     for i in range(len(blocks)):
@@ -239,7 +239,8 @@ def reload_plan(blocks: Blocks, q_init, mass, phi, off, T_blk: int, F_blk: int,
         j = cur[i]
         if j >= top[i]:
             return
-        d_hat, delta = score_step(blocks, i, j + 1, int(beta[blocks.layer[i], blocks.expert[i]]), phi[i], off)
+        d_hat, delta = score_step(blocks, i, j + 1, int(beta[blocks.layer[i], blocks.expert[i]]),
+                                  None if phi is None else phi[i], off)
         heapq.heappush(heap, (-(d_hat / delta), -delta, i, delta))
 
     for i in range(len(blocks)):

@@ -148,3 +148,47 @@ def test_planner_rejects_small_capacity():
     obs = dict(T_blk=16, F_blk=0, B_KV=1e9, R=8, mass=np.ones((L, E)) / E, phi=np.ones((len(q), 3)))
     with pytest.raises(pw.PwError):
         pw.pw_plan_host(bits, q, q_init, utype, layer, expert, M, L, E, obs, off, capacity=1)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_batch_merge_and_residual_table_match_oracle(seed):
+    """pw_merge_requests against the oracle's merge, and pw_plan_host planning from the merged
+    table against the oracle planner on the same table (Sec. 3.2, batched serving)."""
+    rng = np.random.default_rng(100 + seed)
+    bits, q, q_init, utype, layer, expert, M, L, E = _random_problem(rng)
+    n, nb = len(q), len(bits)
+    off = _offline(rng, n, nb)
+    reqs = []
+    for _ in range(int(rng.integers(1, 5))):
+        reqs.append(dict(mass=rng.dirichlet(np.ones(E), size=L), rho_hat=rng.normal(0, 1, (n, nb - 1)),
+                         conf=rng.uniform(0.5, 1.0, (2, nb - 1)), rho_min=float(rng.uniform(-3, -1)),
+                         rho_max=float(rng.uniform(1, 3))))
+    kv = rng.integers(1, 40, size=len(reqs)).astype(float)
+    got = pw.pw_merge_requests(reqs, kv, L, E, n, nb)
+    want = opl.merge_request_signals(reqs, kv)
+    for key in ("mass", "rho_hat", "conf", "rho_min", "rho_max"):
+        assert np.array_equal(np.asarray(got[key]), np.asarray(want[key])), key
+    off_m = dict(off, head_c=want["conf"], rho_min=want["rho_min"], rho_max=want["rho_max"])
+    B_KV = float(M[0, 1] - M[0, 0]) * 0.7
+    for F in (0, 5, 40):
+        obs = dict(T_blk=16, F_blk=F, B_KV=B_KV, R=8, mass=want["mass"], phi=None, rho_hat=want["rho_hat"])
+        plan = pw.pw_plan_host(bits, q, q_init, utype, layer, expert, M, L, E, obs, off_m)
+        blocks = opl.Blocks(bits, q, utype, layer, expert, M, off["s"])
+        off_t = dict(off_m, rho_hat=want["rho_hat"])
+        _, chosen, D = opl.plan_step(blocks, want["mass"], None, off_t, off["n_stages"], 16, F, B_KV)
+        assert plan["D"] == D
+        if D > 0:
+            stage, pl_, total = chosen
+            assert plan["kind"] == 1 and plan["stage"] == stage and plan["total"] == total
+            assert [(i, a, b, d) for i, (a, b, d) in pl_.items()] == plan["entries"]
+        else:
+            pl_, total = opl.reload_plan(blocks, q_init, want["mass"], None, off_t, 16, F, B_KV, 8)
+            assert [(i, a, b, d) for i, (a, b, d) in pl_.items()] == plan["entries"]
+
+
+def test_batch_merge_rejects_bad_weights():
+    req = dict(mass=np.ones((1, 2)) / 2, rho_hat=np.zeros((2, 1)), conf=np.ones((2, 1)), rho_min=-1.0, rho_max=1.0)
+    with pytest.raises(pw.PwError):
+        pw.pw_merge_requests([req], [0.0], 1, 2, 2, 2)
+    with pytest.raises(pw.PwError):
+        pw.pw_merge_requests([req, req], [1.0, -1.0], 1, 2, 2, 2)

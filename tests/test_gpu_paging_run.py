@@ -162,8 +162,10 @@ def oracle_plan(st, off, obs):
         mass[l] = mass[l] / tot if tot > 0 else 1.0 / E
     idx = np.array(idle, dtype=np.int64)
     sub = dict(off, s=np.asarray(off["s"])[idx])
+    if obs.get("rho_hat") is not None:  # a batch-level residual table, re-indexed like the blocks
+        sub["rho_hat"] = np.asarray(obs["rho_hat"])[idx]
     blocks = opl.Blocks(list(sh.bits), q, ut, ly, ex, np.array(M, dtype=np.float64), sub["s"])
-    phi = np.asarray(obs["phi"])[idx]
+    phi = None if obs.get("phi") is None else np.asarray(obs["phi"])[idx]
     _, chosen, D = opl.plan_step(blocks, mass, phi, sub, off["n_stages"], obs["T_blk"], obs["F_blk"], obs["B_KV"])
     if D > 0:
         stage, plan, total = chosen
@@ -269,6 +271,12 @@ def test_planner_leaves_blocks_in_transit_out():
         assert plan["entries"] == want[3]
         assert plan["kind"] == 1 and plan["entries"]
         assert not set(moved) & {blk for blk, _, _, _ in plan["entries"]}
+        # the same with a batch-level residual table in place of the Eq. 5 heads
+        obs_t = dict(obs, phi=None, rho_hat=np.random.default_rng(2).normal(0, 1, (st.n_blocks, len(MINI.bits) - 1)))
+        want = oracle_plan(st, off, obs_t)
+        plan = pw.pw_plan_step(st.ctx, st.n_blocks, obs_t, off)
+        assert (plan["kind"], plan["stage"], plan["D"]) == want[:3]
+        assert plan["entries"] == want[3] and plan["entries"]
         pw.pw_set_fault(st.ctx, 3, 0)
         pw.pw_sync_io(st.ctx)
         pw.pw_commit(st.ctx)
