@@ -1,7 +1,7 @@
-// pw_device.cuh -- device helpers shared by the kernels: number formats, the m16n8k16 MMA,
-// the bit-plane -> code transpose (also used by the debug read-back, so that
-// pw_unpack_indices checks the forward's own extraction), and thin wrappers over the
-// mbarrier / bulk-copy (TMA) / cp.async instructions of sm_90+.
+// pw_device.cuh -- device helpers shared by the kernels: number formats, the 8x8 bit
+// transpose behind the bit-plane -> code extraction (also used by the debug read-back, so
+// that pw_unpack_indices checks the forward's own extraction), thin wrappers over the
+// mbarrier, bulk-copy and TMA tensor instructions, and programmatic dependent launch.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -14,15 +14,6 @@ __device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(
 __device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__float2half_rn(f)); }
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) { return (lo & 0xFFFFu) | (hi << 16); }
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
 
 // 8x8 bit transpose inside every byte column of eight words:
 // out word s, bit (8e + p) = in word p, bit (8e + s).
@@ -47,50 +38,6 @@ __device__ __forceinline__ void transpose8(uint32_t (&X)[8]) {
     X[j + 1] ^= t;
     X[j] ^= t << 1;
   }
-}
-
-// Codes of one thread's fragment elements for one 128-column chunk.  w[p] = the two words
-// (row g, row g+8) of plane p.  Afterwards byte e of Yg[s] is the code of element (s, e)
-// of row g with plane 0 in bit 7 (MSB-aligned); the Q-bit code is byte >> (8 - Q).
-template <int Q>
-__device__ __forceinline__ void codes_from_planes(const uint2 (&w)[Q], uint32_t (&Yg)[8],
-                                                  uint32_t (&Y8)[8]) {
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    Yg[i] = 0u;
-    Y8[i] = 0u;
-  }
-#pragma unroll
-  for (int p = 0; p < Q; ++p) {
-    Yg[7 - p] = w[p].x;
-    Y8[7 - p] = w[p].y;
-  }
-  transpose8(Yg);
-  transpose8(Y8);
-}
-
-template <int Q>
-__device__ __forceinline__ uint32_t code_at(uint32_t Y, int e) {
-  return (Y >> (8 * e + 8 - Q)) & ((1u << Q) - 1u);
-}
-
-// Two 16-bit shared-memory loads packed into one register (low = first address).
-__device__ __forceinline__ uint32_t lds_pair(uint32_t a_lo, uint32_t a_hi) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .b16 lo, hi;\n ld.shared.b16 lo, [%1];\n ld.shared.b16 hi, [%2];\n"
-      " mov.b32 %0, {lo, hi};\n}\n"
-      : "=r"(r)
-      : "r"(a_lo), "r"(a_hi));
-  return r;
-}
-__device__ __forceinline__ void ldm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n" : "=r"(r0), "=r"(r1) : "r"(addr));
 }
 
 // ------------------------------------------------------------------ async copies, mbarriers
@@ -160,20 +107,4 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       "l"(tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
-// 16-byte asynchronous copy; src_bytes = 0 fills the destination with zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-// Arrive on `bar` once this thread's earlier cp.async copies have landed.
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
-}
-// cp.async groups: close the current group; wait until at most N of this thread's groups
-// are still in flight.
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
 }  // namespace pw

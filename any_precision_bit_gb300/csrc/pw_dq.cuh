@@ -10,7 +10,7 @@
 //           8j..8j+7 (column 8j + i in nibble i).  The row's LUT sits in registers as the
 //           low bytes and the high bytes of its centroids; byte permutes (prmt) look up four
 //           codes at a time and interleave the bytes into fp16 pairs.
-//   wider: an 8x8 bit transpose gives word s, byte e = the code (MSB-aligned) of column
+//   wider: an 8x8 bit transpose gives word s, byte e = the code of column
 //           8 (s & 3) + 2e + (s >> 2).  The LUT is in shared memory in the tiled layout of
 //           lut_dev_index (pw_internal.h): the code is byte 1 of its entry's address, so one
 //           byte permute forms the address, every lane of a warp reads its own bank, and a
@@ -105,14 +105,14 @@ __device__ __forceinline__ void dq_nib(const uint32_t (&S)[4], const LutRegs &L,
   }
 }
 
-// Q >= 5 (any Q works): codes of the 32 columns, word s byte e = code of column
-// 8 (s & 3) + 2e + (s >> 2), plane 0 in bit 7.
+// Q >= 4 (any Q works): codes of the 32 columns, word s byte e = code of column
+// 8 (s & 3) + 2e + (s >> 2), plane 0 in bit Q - 1 (the byte is the code itself).
 template <int Q>
 __device__ __forceinline__ void codes_byte(const uint32_t (&W)[8], uint32_t (&Y)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) Y[i] = 0u;
 #pragma unroll
-  for (int p = 0; p < Q; ++p) Y[7 - p] = W[p];
+  for (int p = 0; p < Q; ++p) Y[Q - 1 - p] = W[p];
   transpose8(Y);
 }
 
@@ -143,15 +143,15 @@ __device__ __forceinline__ void lut_pairs_smem(const LutLane &lu, uint32_t (&P)[
   }
 }
 
-// Q >= 5: centroids from the lane's LUT in shared memory.
+// Q >= 4: centroids from the lane's LUT in shared memory.
 template <int Q>
 __device__ __forceinline__ void dq_byte(const uint32_t (&Y)[8], const LutLane &lu, uint32_t (&v)[16]) {
-  // byte e of Z = the code (LSB-aligned) | byte 1 of the lane's word address; a permute with
-  // the address's other bytes is the entry's word address
+  // byte e of Z = the code | byte 1 of the lane's word address; a permute with the
+  // address's other bytes is the entry's word address
   const uint32_t hib = ((lu.word0 >> 8) & 0xFFu) * 0x01010101u;
   uint32_t Z[8];
 #pragma unroll
-  for (int s = 0; s < 8; ++s) Z[s] = (Y[s] >> (8 - Q)) | hib;
+  for (int s = 0; s < 8; ++s) Z[s] = Y[s] | hib;
 #pragma unroll
   for (int s = 0; s < 4; ++s)
 #pragma unroll
@@ -171,7 +171,7 @@ template <int Q>
 __device__ __forceinline__ uint32_t code_byte(const uint32_t (&Y)[8], int c) {
   const int j = c >> 3, i = c & 7;  // column 8j + i = 8 (s & 3) + 2e + (s >> 2)
   const int s = j + 4 * (i & 1), e = i >> 1;
-  return ((Y[s] >> (8 * e)) & 0xFFu) >> (8 - Q);
+  return (Y[s] >> (8 * e)) & 0xFFu;
 }
 
 }  // namespace pw

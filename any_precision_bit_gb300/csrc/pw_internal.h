@@ -113,13 +113,6 @@ PW_HD long lut_dev_index(int d, int c, int b) {
   return ct * (lut_tile_bytes(b) / 2) + ((long)c * 64 + (m >> 1) * 32 + L) * 2 + (m & 1);
 }
 
-// Operand tiles of the tensor-core MMAs are stored as 8x8 "core matrices" of fp16 (128
-// contiguous bytes, row i at byte 16 i); in a tile of R rows by 128 columns, core matrix
-// (row group rg, column group kc) sits at byte (rg * 16 + kc) * 128.
-PW_HD int core_offset128(int row, int col) {
-  return ((row >> 3) * 16 + (col >> 3)) * 128 + (row & 7) * 16 + (col & 7) * 2;
-}
-
 // Kernel-private layout of dense fp16 shared-expert weights (N x K): rows padded to a
 // multiple of 128, columns to a multiple of 128.  Each (128-row tile, 128-column chunk) is a
 // contiguous 32 KB operand tile, tiles ordered [tile][chunk]; inside it, the eight 16-column
