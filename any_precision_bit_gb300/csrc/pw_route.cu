@@ -3,8 +3,9 @@
 // PagedWeight Sec. 3.3 ("Fused Mixed-Precision MoE Kernel"): routing is the first step of
 // the fused layer.  One launch, grid (token groups of kRtTok) x (expert groups of kRtExp):
 //   every CTA        bulk-copies its kRtTok token rows and kRtExp router rows into shared
-//                    memory, takes the tokens' 1/rms (PW_PRENORM), writes the experts' fp16
-//                    input rows (expert group 0 only) and the fp32 logits of its experts;
+//                    memory, takes the tokens' 1/rms (PW_PRENORM), writes its column slice of
+//                    the experts' fp16 input rows and the fp32 logits of its experts (the
+//                    last expert group also the shared expert's gate);
 //   last CTA of a    (elected by a per-group atomic ticket once every expert group wrote its
 //   token group      logits) takes softmax and top-K of the group's tokens, one warp each;
 //   last CTA of all  (elected by a second ticket once every token group is ranked) buckets
@@ -13,7 +14,9 @@
 //                    statistics (the inputs of Eq. 1).
 // The single-CTA tail is short by construction: top-K runs in as many CTAs as there are
 // token groups, the bucket ranks come from warp-private match_any counts and block scans,
-// and the work lists and statistics are written one warp per expert.
+// the work lists are written a warp per expert, and the global loads of the tail (pairs,
+// bitwidths, running statistics, input norms) are issued in batches so that their latencies
+// overlap instead of adding up.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,18 +43,22 @@ __host__ __device__ inline int route_hchunk(int H) {
 }
 
 // Dynamic shared memory of a router launch.  The last CTA reuses it for the pair arrays
-// [ids][weights][slot weights] when they fit.
+// [ids][weights][slot weights] when they fit, and for [slot input norms][token input norms]
+// after them when those fit too.
 struct RouteSmem {
   int bytes;
   bool pairs;
+  bool norms;
 };
 __host__ __device__ inline RouteSmem route_smem(int T, int K, int H) {
   RouteSmem r;
   const int stage = kRtTok * H * 2 + kRtExp * route_hchunk(H) * 4;
-  const int pair_bytes = T * K * 12;
-  r.pairs = pair_bytes <= (stage > kRtStageBytes ? stage : kRtStageBytes);
-  r.bytes = stage;
-  if (r.pairs && pair_bytes > r.bytes) r.bytes = pair_bytes;
+  const int cap = stage > kRtStageBytes ? stage : kRtStageBytes;
+  const int pair_bytes = T * K * 12, norm_bytes = T * K * 16 + T * 4;
+  r.pairs = pair_bytes <= cap;
+  r.norms = norm_bytes <= cap;
+  const int need = r.norms ? norm_bytes : (r.pairs ? pair_bytes : 0);
+  r.bytes = need > stage ? need : stage;
   return r;
 }
 
@@ -160,7 +167,49 @@ __device__ void softmax_topk_warp(const FwdArgs &a, int t, int lane) {
   }
 }
 
-__global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
+// Per expert: the sum of its slot weights r and the sums behind Eq. 5's routed-input
+// features (sum r n, sum r n^2, max n; n = the slot token's input norm), G lanes per expert
+// over its slots [offsets[e], offsets[e] + count[e]) in a fixed order.  An expert holds at
+// most T slots: decode batches take G = 4, larger ones a warp.
+template <int G>
+__device__ __forceinline__ void slot_sums(const FwdArgs &a, const RouteSmem &rs, const float *psw,
+                                          const float *s_n, const int *s_cnt, const int *s_off,
+                                          int warp, int lane, float *s_fsum, float (*s_phi)[256]) {
+  const int E = a.E, sub = lane / G, gl = lane % G;
+  for (int eb = warp * (32 / G); eb < E; eb += kRtWarps * (32 / G)) {
+    const int ee = eb + sub;
+    float wsum = 0.f, s1 = 0.f, s2 = 0.f, mx = 0.f;
+    if (ee < E) {
+      const int o1 = s_off[ee] + s_cnt[ee];
+#pragma unroll 4
+      for (int sl = s_off[ee] + gl; sl < o1; sl += G) {
+        const float r = rs.pairs ? psw[sl] : __ldcg(psw + sl);
+        const float n = rs.norms ? s_n[sl] : __ldcg(a.s.xnorm + a.s.slot_tok[sl]);
+        wsum += r;
+        s1 = fmaf(r, n, s1);
+        s2 = fmaf(r * n, n, s2);
+        mx = fmaxf(mx, n);
+      }
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (gl == 0 && ee < E) {
+      s_fsum[ee] = wsum;
+      s_phi[0][ee] = s1;
+      s_phi[1][ee] = s2;
+      s_phi[2][ee] = mx;
+    }
+  }
+}
+
+// Two CTAs per SM at most (the staged rows take up to 96 KB of shared memory each), so the
+// register budget is half the register file per CTA.
+__global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int H = a.H, E = a.E, K = a.K;
   const int hc = route_hchunk(H);
@@ -207,7 +256,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
       // unit-gain RMSNorm of the layer input (PW_PRENORM): one warp per staged token
       if (warp < nt) {
         float ss = 0.f;
-        const float *wsg = blockIdx.y == 0 ? a.lay.wsg : nullptr;  // shared-expert gate
+        // the shared-expert gate goes to the last expert group, which holds the fewest experts
+        const float *wsg = blockIdx.y == gridDim.y - 1 ? a.lay.wsg : nullptr;
         float gz = 0.f;
         for (int h = lane * 2; h < H; h += 64) {
           const uint32_t v = *reinterpret_cast<const uint32_t *>(xs + warp * H + h);
@@ -232,10 +282,12 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
           if (blockIdx.y == 0) a.s.xnorm[t0 + warp] = sqrtf(ss) * inv;
         }
       }
-      if (blockIdx.y == 0) {  // the experts' fp16 input rows
+      {  // the experts' fp16 input rows, a slice of 8-column vectors per expert group
         __syncthreads();
-        for (int v = tid; v < nt * H / 8; v += kRtThreads) {
-          const int t = v / (H / 8), c = (v % (H / 8)) * 8;
+        const int nv = H / 8, per = (nv + gridDim.y - 1) / gridDim.y;
+        const int v0 = blockIdx.y * per, wid = min(nv, v0 + per) - v0;
+        for (int v = tid; v < nt * wid; v += kRtThreads) {
+          const int t = v / wid, c = (v0 + v % wid) * 8;
           const uint4 raw = *reinterpret_cast<const uint4 *>(xs + t * H + c);
           const float inv = s_inv[t];
           const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -298,6 +350,21 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   int *s_ids = reinterpret_cast<int *>(smem_raw);
   float *s_w = reinterpret_cast<float *>(smem_raw) + TK;
   float *s_sw = reinterpret_cast<float *>(smem_raw) + 2 * TK;
+  float *s_n = reinterpret_cast<float *>(smem_raw) + 3 * TK;   // slot input norms (rs.norms)
+  float *s_xn = reinterpret_cast<float *>(smem_raw) + 4 * TK;  // token input norms (rs.norms)
+  // Loads whose latency overlaps the bucketing: the committed bitwidths of the layer's blocks
+  // and the running statistics of this thread's expert (E <= kRtThreads).
+  const BlockDev *tab = a.table + (size_t)a.layer * E * 2;
+  const int q1 = tid < E ? tab[2 * tid].q : 0, q2 = tid < E ? tab[2 * tid + 1].q : 0;
+  const size_t si = (size_t)a.layer * E + tid;
+  double st_c = 0., st_w = 0., st_p[4] = {0., 0., 0., 0.};
+  if (tid < E) {
+    st_c = a.s.stat_count[si];
+    st_w = a.s.stat_wsum[si];
+    if (a.s.stat_phi)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) st_p[i] = a.s.stat_phi[si * 4 + i];
+  }
   if (rs.pairs) {  // the pairs were written by other CTAs: read them through L2
     for (int j0 = 0; j0 < TK; j0 += 4 * kRtThreads) {
       int iv[4];
@@ -317,6 +384,8 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
         }
       }
     }
+    if (rs.norms)
+      for (int t = tid; t < T; t += kRtThreads) s_xn[t] = __ldcg(a.s.xnorm + t);
   }
   const int *pid = rs.pairs ? s_ids : a.s.ids;
   const float *pwt = rs.pairs ? s_w : a.s.w;
@@ -338,12 +407,22 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
   const unsigned lt = (1u << lane) - 1u;
   const int span = (TK + kRtWarps - 1) / kRtWarps;
   const int j0 = warp * span, j1 = min(TK, j0 + span);
-  for (int jb = j0; jb < j1; jb += 32) {
-    const int j = jb + lane;
-    const int ee = j < j1 ? (rs.pairs ? pid[j] : __ldcg(pid + j)) : -1 - lane;  // invalid lanes match nothing valid
-    const unsigned peers = __match_any_sync(0xffffffffu, ee);
-    if (j < j1 && (peers & lt) == 0u) s_wc[warp][ee] += __popc(peers);
-    __syncwarp();
+  // each warp walks its span 32 pairs at a time, with the loads of four batches in flight;
+  // lanes past the span hold -1 - lane, which matches no expert and no other lane
+  for (int jb = j0; jb < j1; jb += 4 * 32) {
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = jb + 32 * u + lane;
+      ev[u] = j < j1 ? (rs.pairs ? pid[j] : __ldcg(pid + j)) : -1 - lane;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (jb + 32 * u >= j1) break;  // warp-uniform
+      const unsigned peers = __match_any_sync(0xffffffffu, ev[u]);
+      if (ev[u] >= 0 && (peers & lt) == 0u) s_wc[warp][ev[u]] += __popc(peers);
+      __syncwarp();
+    }
   }
   __syncthreads();
   const int tiles1 = (2 * a.I + kCtaRows - 1) / kCtaRows;
@@ -367,8 +446,6 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
     // (ties by expert id), separately for the two projections: an item's time grows with its
     // bitwidth, and items are claimed in list order, so the longest go first and the tail of
     // the launch is made of the shortest.
-    const BlockDev *tab = a.table + (size_t)a.layer * E * 2;
-    const int q1 = tid < E ? tab[2 * tid].q : 0, q2 = tid < E ? tab[2 * tid + 1].q : 0;
     if (tid < E) {
       s_q[0][tid] = q1;
       s_q[1][tid] = q2;
@@ -429,19 +506,33 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
     a.s.n_items[0] = s_itm1[E];
     a.s.n_items[1] = s_itm2[E];
   }
-  for (int jb = j0; jb < j1; jb += 32) {
-    const int j = jb + lane;
-    const int ee = j < j1 ? (rs.pairs ? pid[j] : __ldcg(pid + j)) : -1 - lane;
-    const unsigned peers = __match_any_sync(0xffffffffu, ee);
-    if (j < j1) {
-      const int slot = s_off[ee] + s_wc[warp][ee] + __popc(peers & lt);
-      a.s.slot_tok[slot] = j / K;
-      a.s.pair_slot[j] = slot;
-      psw[slot] = rs.pairs ? pwt[j] : __ldcg(pwt + j);
+  for (int jb = j0; jb < j1; jb += 4 * 32) {
+    int ev[4];
+    float wv[4], nv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = jb + 32 * u + lane;
+      const bool in = j < j1;
+      ev[u] = in ? (rs.pairs ? pid[j] : __ldcg(pid + j)) : -1 - lane;
+      wv[u] = in ? (rs.pairs ? pwt[j] : __ldcg(pwt + j)) : 0.f;
+      nv[u] = in && rs.norms ? s_xn[j / K] : 0.f;
     }
-    __syncwarp();
-    if (j < j1 && (peers & lt) == 0u) s_wc[warp][ee] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (jb + 32 * u >= j1) break;  // warp-uniform
+      const int j = jb + 32 * u + lane, ee = ev[u];
+      const unsigned peers = __match_any_sync(0xffffffffu, ee);
+      if (ee >= 0) {
+        const int slot = s_off[ee] + s_wc[warp][ee] + __popc(peers & lt);
+        a.s.slot_tok[slot] = j / K;
+        a.s.pair_slot[j] = slot;
+        psw[slot] = wv[u];
+        if (rs.norms) s_n[slot] = nv[u];
+      }
+      __syncwarp();
+      if (ee >= 0 && (peers & lt) == 0u) s_wc[warp][ee] += __popc(peers);
+      __syncwarp();
+    }
   }
   // work items of the shared expert first (they are the heaviest), one thread each
   for (int i = tid; i < sh1; i += kRtThreads) {
@@ -458,66 +549,39 @@ __global__ void __launch_bounds__(kRtThreads) route_kernel(FwdArgs a) {
                  WorkItem{1, 0, tile, c * tc, min(tc, T - c * tc), part * per, min(total, (part + 1) * per), part});
     }
   }
-  // routed work items, one thread each: item i of a projection belongs to the expert whose
-  // rank's range [first[r], first[r + 1]) holds it; within an expert, (row tile, token
-  // chunk) with the token chunks of a row tile consecutive, so that CTAs claiming them
-  // together share the tile's planes in L2
+  // routed work items, a warp per expert rank: rank r's items are [first[r], first[r + 1]),
+  // (row tile, token chunk) with the token chunks of a row tile consecutive, so that CTAs
+  // claiming them together share the tile's planes in L2
   for (int u = 0; u < 2; ++u) {
     const int *first = u ? s_itm2 : s_itm1;
     WorkItem *dst = u ? a.s.items2 : a.s.items1;
-    for (int i = (u ? sh2 : sh1) + tid; i < first[E]; i += kRtThreads) {
-      int lo = 0, hi = E - 1;  // the largest rank r with first[r] <= i
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (first[mid] <= i)
-          lo = mid;
-        else
-          hi = mid - 1;
+    const int kc1 = u ? kc_d : kc_gu;
+    for (int r = warp; r < E; r += kRtWarps) {
+      const int ee = s_rk[u][r], cnt = s_cnt[ee], ch = (cnt + tc - 1) / tc;
+      const int i0 = first[r], n = first[r + 1] - i0;
+      for (int loc = lane; loc < n; loc += 32) {
+        const int tile = loc / ch, c = loc - tile * ch;
+        store_item(dst + i0 + loc, WorkItem{0, ee, tile, c * tc, min(tc, cnt - c * tc), 0, kc1, 0});
       }
-      const int ee = s_rk[u][lo], cnt = s_cnt[ee], ch = (cnt + tc - 1) / tc, loc = i - first[lo];
-      const int c = loc % ch;
-      store_item(dst + i, WorkItem{0, ee, loc / ch, c * tc, min(tc, cnt - c * tc), 0, u ? kc_d : kc_gu, 0});
     }
   }
-  __syncthreads();  // every slot weight is in place
-  // per expert (one warp each): its routing statistics and the sums behind Eq. 5's routed-
-  // input features, over its slots in a fixed order (n = the token's input norm)
-  for (int ee = warp; ee < E; ee += kRtWarps) {
-    const int cnt = s_cnt[ee], o0 = s_off[ee];
-    float wsum = 0.f, s1 = 0.f, s2 = 0.f, mx = 0.f;
-    for (int sl = lane; sl < cnt; sl += 32) {
-      const float r = rs.pairs ? psw[o0 + sl] : __ldcg(psw + o0 + sl);
-      const float n = __ldcg(a.s.xnorm + a.s.slot_tok[o0 + sl]);
-      wsum += r;
-      s1 = fmaf(r, n, s1);
-      s2 = fmaf(r * n, n, s2);
-      mx = fmaxf(mx, n);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      s_fsum[ee] = wsum;
-      s_phi[0][ee] = s1;
-      s_phi[1][ee] = s2;
-      s_phi[2][ee] = mx;
-    }
-  }
+  __syncthreads();  // every slot weight and slot norm is in place
+  // per expert: its routing statistics and the sums behind Eq. 5's routed-input features
+  if (T <= 256)
+    slot_sums<4>(a, rs, psw, s_n, s_cnt, s_off, warp, lane, s_fsum, s_phi);
+  else
+    slot_sums<32>(a, rs, psw, s_n, s_cnt, s_off, warp, lane, s_fsum, s_phi);
   __syncthreads();
-  // the running statistics: one thread per expert, every read-modify-write in flight at once
-  for (int ee = tid; ee < E; ee += kRtThreads) {
-    a.s.stat_count[(size_t)a.layer * E + ee] += (double)s_cnt[ee];
-    a.s.stat_wsum[(size_t)a.layer * E + ee] += (double)s_fsum[ee];
-    if (a.s.stat_phi && s_cnt[ee] > 0) {
-      double *ph = a.s.stat_phi + ((size_t)a.layer * E + ee) * 4;
-      ph[0] += (double)s_fsum[ee];
-      ph[1] += (double)s_phi[0][ee];
-      ph[2] += (double)s_phi[1][ee];
-      ph[3] = fmax(ph[3], (double)s_phi[2][ee]);
+  // the running statistics of this thread's expert (loaded at the start of the tail)
+  if (tid < E) {
+    a.s.stat_count[si] = st_c + (double)s_cnt[tid];
+    a.s.stat_wsum[si] = st_w + (double)s_fsum[tid];
+    if (a.s.stat_phi && s_cnt[tid] > 0) {
+      double *ph = a.s.stat_phi + si * 4;
+      ph[0] = st_p[0] + (double)s_fsum[tid];
+      ph[1] = st_p[1] + (double)s_phi[0][tid];
+      ph[2] = st_p[2] + (double)s_phi[1][tid];
+      ph[3] = fmax(st_p[3], (double)s_phi[2][tid]);
     }
   }
   if (tid == 0) {

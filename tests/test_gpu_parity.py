@@ -213,13 +213,15 @@ def test_gated_shared_expert(name, T, prenorm):
         pw.pw_destroy(ctx)
 
 
-@pytest.mark.parametrize("prenorm", [False, True])
-def test_routed_input_features_match_eq5(prenorm):
+# decode batches (one thread per expert), a prefill batch whose slot norms sit in shared
+# memory, and one whose pairs are too many for it (the sums read the slots from memory)
+@pytest.mark.parametrize("name,T,prenorm", [("qwen", 16, False), ("qwen", 16, True),
+                                            ("qwen", 600, True), ("g128", 1100, False)])
+def test_routed_input_features_match_eq5(name, T, prenorm):
     """Eq. 5's phi per expert from the device sums, against the oracle's definition on the
     oracle's routing of the same tokens; the planner reads them when obs->phi is NULL."""
     from oracle import planner as opl
-    shape = syn.SHAPES["qwen"]
-    T = 16
+    shape = syn.SHAPES[name]
     data = LayerData(shape, 9, 0, T, prenorm=prenorm)
     ctx = make_ctx(pw, shape, L=1, max_tokens=T)
     try:
