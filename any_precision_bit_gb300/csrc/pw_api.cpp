@@ -388,7 +388,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
   };
   bool ok = salloc((void **)&c->s.logits, sizeof(float) * Tm * d.E) &&
             salloc((void **)&c->s.ids, sizeof(int) * TK) && salloc((void **)&c->s.w, sizeof(float) * TK) &&
-            salloc((void **)&c->s.counts, sizeof(int) * d.E) &&
+            salloc((void **)&c->s.ranks, sizeof(int) * 4 * kRankStride) &&
             salloc((void **)&c->s.offsets, sizeof(int) * (d.E + 1)) &&
             salloc((void **)&c->s.slot_tok, sizeof(int) * TK) &&
             salloc((void **)&c->s.pair_slot, sizeof(int) * TK) &&

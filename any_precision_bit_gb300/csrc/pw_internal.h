@@ -66,6 +66,69 @@ PW_HD int shared_down_splits(int I, int Is) {
   return n < 1 ? 1 : (n > 8 ? 8 : n);
 }
 
+// Work-list tables of one launch, written by the router's last CTA: for each projection u
+// (0 gate_up, 1 down) first[u][r] = the first work item of the expert at rank r (ranks by
+// decreasing committed bitwidth, ties by expert id; first[u][0] = the shared expert's item
+// count, first[u][E] = the total) and rk[u][r] = that expert.  Row stride kRankStride.
+constexpr int kRankStride = 257;
+
+// Work item i of projection u from the tables and the expert-sorted slot offsets off[0..E].
+// Items [0, first[0]) are the shared expert's: (row tile, token chunk), and for the down
+// projection also the K part, with the chunks and parts of a tile consecutive.  Items
+// [first[r], first[r + 1]) are the expert at rank r's: (row tile, slot chunk) with the slot
+// chunks of a row tile consecutive, so that CTAs claiming them together share the tile's
+// planes in L2.
+PW_HD WorkItem work_item(int u, int i, const int *first, const int *rk, const int *off, int E, int T, int H,
+                         int I, int Is) {
+  const int tc = tok_chunk_for(T), tchunks = (T + tc - 1) / tc;
+  const int kc_gu = kpad_cols(H) / kChunkCols, kc_d = kpad_cols(I) / kChunkCols;
+  WorkItem w;
+  if (i < first[0]) {
+    int tile, c, kc0 = 0, kc1 = kc_gu, part = 0;
+    if (u == 0) {
+      tile = i / tchunks;
+      c = i - tile * tchunks;
+    } else {
+      const int nsplit = shared_down_splits(I, Is);
+      const int total = (Is / 16 + 7) / 8, per = (total + nsplit - 1) / nsplit;
+      tile = i / (tchunks * nsplit);
+      const int rem = i - tile * tchunks * nsplit;
+      c = rem / nsplit;
+      part = rem - c * nsplit;
+      kc0 = part * per;
+      kc1 = total < (part + 1) * per ? total : (part + 1) * per;
+    }
+    w.kind = 1;
+    w.expert = 0;
+    w.tile = tile;
+    w.tok0 = c * tc;
+    w.ntok = tc < T - c * tc ? tc : T - c * tc;
+    w.kc0 = kc0;
+    w.kc1 = kc1;
+    w.part = part;
+    return w;
+  }
+  int lo = 0, hi = E - 1;  // the largest rank r with first[r] <= i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (first[mid] <= i)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int e = rk[lo], cnt = off[e + 1] - off[e], ch = (cnt + tc - 1) / tc, loc = i - first[lo];
+  const int tile = loc / ch, c = loc - tile * ch;
+  w.kind = 0;
+  w.expert = e;
+  w.tile = tile;
+  w.tok0 = c * tc;
+  w.ntok = tc < cnt - c * tc ? tc : cnt - c * tc;
+  w.kc0 = 0;
+  w.kc1 = u ? kc_d : kc_gu;
+  w.part = 0;
+  return w;
+}
+
 // device row of an original row (u = 0 gate_up with I features, u = 1 identity)
 PW_HD int dev_row(int r, int u, int I) {
   if (u != 0) return r;
@@ -159,7 +222,7 @@ struct Scratch {
   float *logits;       // [Tm][E]
   int *ids;            // [Tm][K]
   float *w;            // [Tm][K]
-  int *counts;         // [E]
+  int *ranks;          // [4][kRankStride] work-list tables: first[2][E + 1], then rk[2][E]
   int *offsets;        // [E + 1]
   int *slot_tok;       // [Tm*K] token of each expert-sorted slot
   int *pair_slot;      // [Tm*K] slot of pair (t, k)

@@ -73,18 +73,68 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
   }
 }
 
-// The layer input's rows in expert-sorted slot order (xs[slot] = xh[token of slot]), so that
-// every routed gate_up work item reads consecutive rows with TMA boxes.  16-byte vectors,
-// grid-stride.
-__global__ void gather_kernel(FwdArgs a) {
+__device__ __forceinline__ void store_item(WorkItem *dst, const WorkItem &w) {
+  int4 *p = reinterpret_cast<int4 *>(dst);
+  p[0] = make_int4(w.kind, w.expert, w.tile, w.tok0);
+  p[1] = make_int4(w.ntok, w.kc0, w.kc1, w.part);
+}
+
+// Two jobs between the router and the expert kernels, grid-stride over every CTA:
+//  * the layer input's rows in expert-sorted slot order (xs[slot] = xh[token of slot]), so
+//    that every routed gate_up work item reads consecutive rows with TMA boxes (16-byte
+//    vectors);
+//  * the work items of both projections, expanded from the router's work-list tables (one
+//    thread per item).
+// The tables' loads are issued first and land while the rows are copied.
+__global__ void __launch_bounds__(256) gather_kernel(FwdArgs a) {
   pdl_trigger();
   pdl_wait();
+  __shared__ int s_first[2][kRankStride], s_rk[2][kRankStride], s_off[kRankStride];
+  const int E = a.E, tid = threadIdx.x;  // blockDim.x == 256 >= E
+  const int *R = a.s.ranks;
+  int f0 = 0, f1 = 0, k0 = 0, k1 = 0, of = 0, fE0 = 0, fE1 = 0, oE = 0;
+  if (tid <= E) {
+    f0 = R[tid];
+    f1 = R[kRankStride + tid];
+    of = a.s.offsets[tid];
+  }
+  if (tid < E) {
+    k0 = R[2 * kRankStride + tid];
+    k1 = R[3 * kRankStride + tid];
+  }
+  const bool last = tid == 0 && E == 256;  // entry E of first and offsets when E == blockDim.x
+  if (last) {
+    fE0 = R[E];
+    fE1 = R[kRankStride + E];
+    oE = a.s.offsets[E];
+  }
   const int vec = a.H / 8;
   const long n = (long)a.T * a.K * vec;
-  for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long)gridDim.x * blockDim.x) {
+  for (long i = (long)blockIdx.x * blockDim.x + tid; i < n; i += (long)gridDim.x * blockDim.x) {
     const int s = (int)(i / vec), v = (int)(i % vec);
     const int t = a.s.slot_tok[s];
     reinterpret_cast<uint4 *>(a.s.xs + (size_t)s * a.H)[v] = reinterpret_cast<const uint4 *>(a.s.xh + (size_t)t * a.H)[v];
+  }
+  if (tid <= E) {
+    s_first[0][tid] = f0;
+    s_first[1][tid] = f1;
+    s_off[tid] = of;
+  }
+  if (tid < E) {
+    s_rk[0][tid] = k0;
+    s_rk[1][tid] = k1;
+  }
+  if (last) {
+    s_first[0][E] = fE0;
+    s_first[1][E] = fE1;
+    s_off[E] = oE;
+  }
+  __syncthreads();
+  const int n1 = s_first[0][E], n_all = n1 + s_first[1][E];
+  for (int i = blockIdx.x * blockDim.x + tid; i < n_all; i += gridDim.x * blockDim.x) {
+    const int u = i >= n1 ? 1 : 0, iu = u ? i - n1 : i;
+    store_item((u ? a.s.items2 : a.s.items1) + iu,
+               work_item(u, iu, s_first[u], s_rk[u], s_off, E, a.T, a.H, a.I, a.Is));
   }
 }
 

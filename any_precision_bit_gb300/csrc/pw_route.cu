@@ -10,13 +10,13 @@
 //   token group      logits) takes softmax and top-K of the group's tokens, one warp each;
 //   last CTA of all  (elected by a second ticket once every token group is ranked) buckets
 //                    the (token, k) pairs by expert in the stable (expert, token, k) order,
-//                    writes the expert kernels' work lists and adds the layer's routing
-//                    statistics (the inputs of Eq. 1).
+//                    writes the tables of the expert kernels' work lists and adds the
+//                    layer's routing statistics (the inputs of Eq. 1 and Eq. 5).
 // The single-CTA tail is short by construction: top-K runs in as many CTAs as there are
 // token groups, the bucket ranks come from warp-private match_any counts and block scans,
-// the work lists are written a warp per expert, and the global loads of the tail (pairs,
-// bitwidths, running statistics, input norms) are issued in batches so that their latencies
-// overlap instead of adding up.
+// the work items are expanded from the tables by the many CTAs of the gather kernel, and
+// the global loads of the tail (pairs, bitwidths, running statistics, input norms) are
+// issued in batches so that their latencies overlap instead of adding up.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -89,12 +89,6 @@ __device__ __forceinline__ void top8_insert(uint64_t (&v)[8], uint64_t key) {
       v[s] = v[s - 1];
       v[s - 1] = t;
     }
-}
-
-__device__ __forceinline__ void store_item(WorkItem *dst, const WorkItem &w) {
-  int4 *p = reinterpret_cast<int4 *>(dst);
-  p[0] = make_int4(w.kind, w.expert, w.tile, w.tok0);
-  p[1] = make_int4(w.ntok, w.kc0, w.kc1, w.part);
 }
 
 // Softmax and top-K of token t, one warp: each lane takes experts lane, lane + 32, ... with
@@ -432,7 +426,6 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   const int nsplit = shared_down_splits(a.I, a.Is);
   const int sh1 = a.Is > 0 ? ((2 * a.Is + kCtaRows - 1) / kCtaRows) * tchunks : 0;
   const int sh2 = a.Is > 0 ? tiles2 * tchunks * nsplit : 0;
-  const int kc_gu = kpad_cols(a.H) / kChunkCols, kc_d = kpad_cols(a.I) / kChunkCols;
   {
     int cnt = 0;
     if (tid < E)
@@ -534,37 +527,16 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
       __syncwarp();
     }
   }
-  // work items of the shared expert first (they are the heaviest), one thread each
-  for (int i = tid; i < sh1; i += kRtThreads) {
-    const int tile = i / tchunks, c = i % tchunks;
-    store_item(a.s.items1 + i,
-               WorkItem{1, 0, tile, c * tc, min(tc, T - c * tc), 0, kc_gu, 0});
-  }
-  {
-    const int total = (a.Is / 16 + 7) / 8, per = (total + nsplit - 1) / nsplit;
-    for (int i = tid; i < sh2; i += kRtThreads) {
-      const int tile = i / (tchunks * nsplit), rem = i % (tchunks * nsplit);
-      const int c = rem / nsplit, part = rem % nsplit;
-      store_item(a.s.items2 + i,
-                 WorkItem{1, 0, tile, c * tc, min(tc, T - c * tc), part * per, min(total, (part + 1) * per), part});
-    }
-  }
-  // routed work items, a warp per expert rank: rank r's items are [first[r], first[r + 1]),
-  // (row tile, token chunk) with the token chunks of a row tile consecutive, so that CTAs
-  // claiming them together share the tile's planes in L2
-  for (int u = 0; u < 2; ++u) {
-    const int *first = u ? s_itm2 : s_itm1;
-    WorkItem *dst = u ? a.s.items2 : a.s.items1;
-    const int kc1 = u ? kc_d : kc_gu;
-    for (int r = warp; r < E; r += kRtWarps) {
-      const int ee = s_rk[u][r], cnt = s_cnt[ee], ch = (cnt + tc - 1) / tc;
-      const int i0 = first[r], n = first[r + 1] - i0;
-      for (int loc = lane; loc < n; loc += 32) {
-        const int tile = loc / ch, c = loc - tile * ch;
-        store_item(dst + i0 + loc, WorkItem{0, ee, tile, c * tc, min(tc, cnt - c * tc), 0, kc1, 0});
+  // the work-list tables (the gather kernel that follows writes the work items from them)
+  if (a.s.ranks)
+    for (int i = tid; i <= E; i += kRtThreads) {
+      a.s.ranks[i] = s_itm1[i];
+      a.s.ranks[kRankStride + i] = s_itm2[i];
+      if (i < E) {
+        a.s.ranks[2 * kRankStride + i] = s_rk[0][i];
+        a.s.ranks[3 * kRankStride + i] = s_rk[1][i];
       }
     }
-  }
   __syncthreads();  // every slot weight and slot norm is in place
   // per expert: its routing statistics and the sums behind Eq. 5's routed-input features
   if (T <= 256)

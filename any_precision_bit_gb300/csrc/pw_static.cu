@@ -40,24 +40,20 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   if (pw_status st = route_args(ctx, layer, x, T, ids, w, flags & PW_PRENORM, &a)) return st;
 
   // scratch the router kernel touches, carved from the static array (256-byte aligned)
+  // (the work items themselves are written from the rank tables by the gather kernel of a
+  // forward, which this call does not run)
   const long TK = (long)T * a.K;
-  const int tiles1 = (2 * a.I + kCtaRows - 1) / kCtaRows;
-  const int tiles2 = (a.H + kCtaRows - 1) / kCtaRows;
-  const long tch = (T + kTokChunk - 1) / kTokChunk;
-  const long chunks = (a.E < TK ? a.E : TK) + TK / kTokChunk + 1;
-  const long n1 = tiles1 * chunks + (a.Is ? ((2L * a.Is + kCtaRows - 1) / kCtaRows) * tch : 0);
-  const long n2 = tiles2 * chunks + (a.Is ? tiles2 * tch * shared_down_splits(a.I, a.Is) : 0);
   const size_t sizes[] = {
       sizeof(float) * T * a.E,      // logits
       sizeof(int) * TK,             // ids
       sizeof(float) * TK,           // w
-      sizeof(int) * a.E,            // counts
+      sizeof(int) * 4 * kRankStride,  // ranks: the work-list tables
       sizeof(int) * (a.E + 1),      // offsets
       sizeof(int) * TK,             // slot_tok
       sizeof(int) * TK,             // pair_slot
       sizeof(float) * TK,           // slot_w
-      sizeof(WorkItem) * n1,        // items1
-      sizeof(WorkItem) * n2,        // items2
+      0,                            // items1 (not used)
+      0,                            // items2 (not used)
       sizeof(int) * 2,              // n_items
       sizeof(unsigned) * (1 + (T + 7) / 8),  // tickets: all token groups, then one per group
       sizeof(float) * T,            // inv_rms
@@ -101,13 +97,13 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   s.logits = reinterpret_cast<float *>(take(sizes[0]));
   s.ids = reinterpret_cast<int *>(take(sizes[1]));
   s.w = reinterpret_cast<float *>(take(sizes[2]));
-  s.counts = reinterpret_cast<int *>(take(sizes[3]));
+  s.ranks = reinterpret_cast<int *>(take(sizes[3]));
   s.offsets = reinterpret_cast<int *>(take(sizes[4]));
   s.slot_tok = reinterpret_cast<int *>(take(sizes[5]));
   s.pair_slot = reinterpret_cast<int *>(take(sizes[6]));
   s.slot_w = reinterpret_cast<float *>(take(sizes[7]));
-  s.items1 = reinterpret_cast<WorkItem *>(take(sizes[8]));
-  s.items2 = reinterpret_cast<WorkItem *>(take(sizes[9]));
+  s.items1 = nullptr;
+  s.items2 = nullptr;
   s.n_items = reinterpret_cast<int *>(take(sizes[10]));
   s.ticket = reinterpret_cast<unsigned *>(take(sizes[11]));
   s.inv_rms = reinterpret_cast<float *>(take(sizes[12]));
@@ -116,8 +112,8 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   s.xh = reinterpret_cast<uint16_t *>(take(sizes[15]));
   s.xnorm = reinterpret_cast<float *>(take(sizes[16]));
   s.sgate = reinterpret_cast<float *>(take(sizes[17]));
-  s.max_items1 = (int)n1;
-  s.max_items2 = (int)n2;
+  s.max_items1 = 0;
+  s.max_items2 = 0;
   a.s = s;
   a.layer = 0;  // the kernel indexes its statistics by layer; these go to the discarded slots
 
