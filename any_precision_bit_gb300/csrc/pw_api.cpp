@@ -375,7 +375,11 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
   const long chunks_routed = std::min<long>(d.E, TK) + TK / kTokChunk + 1;
   c->s.max_items1 = (int)(tiles1 * chunks_routed + (d.Is ? ((2 * d.Is + kCtaRows - 1) / kCtaRows) * tch : 0));
   const int nsplit = shared_down_splits(d.I, d.Is);
-  c->s.max_items2 = (int)(tiles2 * chunks_routed + (d.Is ? tiles2 * tch * nsplit : 0));
+  const int dsplit = routed_down_splits(1, d.I);  // the most K parts of a routed down item
+  c->s.max_items2 = (int)(tiles2 * chunks_routed * dsplit + (d.Is ? tiles2 * tch * nsplit : 0));
+  // routed down partial sums: one part of T*K rows for prefill-sized batches, dsplit parts
+  // for decode-sized ones
+  const long o_rows = std::max<long>(TK, (long)dsplit * std::min<long>(Tm, kPrefillMinT - 1) * d.K);
   auto salloc = [&](void **p, size_t n) -> bool {
     n = std::max<size_t>(n, 16);
     if (cudaMalloc(p, n) != cudaSuccess) {
@@ -398,7 +402,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.n_items, sizeof(int) * 2) && salloc((void **)&c->s.ticket, sizeof(unsigned) * (1 + (Tm + 7) / 8)) &&
             salloc((void **)&c->s.h_routed, sizeof(uint16_t) * TK * d.I) &&
             salloc((void **)&c->s.h_shared, sizeof(uint16_t) * Tm * std::max(d.Is, 1)) &&
-            salloc((void **)&c->s.o_routed, sizeof(float) * TK * d.H) &&
+            salloc((void **)&c->s.o_routed, sizeof(float) * o_rows * d.H) &&
             salloc((void **)&c->s.o_shared, sizeof(float) * nsplit * Tm * d.H) &&
             salloc((void **)&c->s.inv_rms, sizeof(float) * Tm) && salloc((void **)&c->s.sgate, sizeof(float) * Tm) &&
             salloc((void **)&c->s.xnorm, sizeof(float) * Tm) &&

@@ -676,8 +676,8 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
               a.s.h_shared[(size_t)(v.row0 + j) * a.Is + f] = hv;
           }
         } else if (R < v.N && j < v.ntok) {
-          if (v.routed)
-            a.s.o_routed[(size_t)(v.row0 + j) * a.H + R] = acc;
+          if (v.routed)  // the K part's partial sums (one part but at decode batch sizes)
+            a.s.o_routed[((size_t)w.part * a.T * a.K + v.row0 + j) * a.H + R] = acc;
           else
             a.s.o_shared[((size_t)w.part * a.T + v.row0 + j) * a.H + R] = acc;
         }

@@ -58,12 +58,30 @@ PW_HD int kpad_cols(int K) { return (K + kChunkCols - 1) / kChunkCols * kChunkCo
 // The shared expert's down projection (K = Is) is split along K into this many items per
 // row tile, so that each is about as long as a routed down item (K = I); the parts are
 // summed, in order, by the combine kernel.
+// Every part holds at least one stage: parts are ceil(stages / n) stages long, so when the
+// cap of 8 applies the count is what that length needs (9 stages in parts of 2 make 5).
 PW_HD int shared_down_splits(int I, int Is) {
   if (Is <= 0) return 1;
   const int sh = (Is / 16 + 7) / 8;           // 128-column stages of the shared down
   const int rt = kpad_cols(I) / kChunkCols;   // stages of a routed down
-  const int n = (sh + rt - 1) / rt;
-  return n < 1 ? 1 : (n > 8 ? 8 : n);
+  int n = (sh + rt - 1) / rt;
+  n = n < 1 ? 1 : (n > 8 ? 8 : n);
+  const int per = (sh + n - 1) / n;
+  return (sh + per - 1) / per;
+}
+
+// The routed down projection (K = I) is split along K into this many parts per (row tile,
+// slot chunk) at decode batch sizes, so that a launch of a few long items (8 experts of
+// 112 stages, say) becomes many of about 16 stages; each part writes its own partial-sum
+// buffer, which the combine kernel adds in order.  Prefill-sized batches have items enough
+// and keep one part.  Every part holds at least one stage.
+PW_HD int routed_down_splits(int T, int I) {
+  if (T >= kPrefillMinT) return 1;
+  const int st = kpad_cols(I) / kChunkCols;
+  int n = (st + 15) / 16;
+  n = n < 1 ? 1 : (n > 8 ? 8 : n);
+  const int per = (st + n - 1) / n;
+  return (st + per - 1) / per;
 }
 
 // Work-list tables of one launch, written by the router's last CTA: for each projection u
@@ -77,7 +95,8 @@ constexpr int kRankStride = 257;
 // projection also the K part, with the chunks and parts of a tile consecutive.  Items
 // [first[r], first[r + 1]) are the expert at rank r's: (row tile, slot chunk) with the slot
 // chunks of a row tile consecutive, so that CTAs claiming them together share the tile's
-// planes in L2.
+// planes in L2; for the down projection each (row tile, K part) has its slot chunks
+// consecutive, the parts of a tile one after the other.
 PW_HD WorkItem work_item(int u, int i, const int *first, const int *rk, const int *off, int E, int T, int H,
                          int I, int Is) {
   const int tc = tok_chunk_for(T), tchunks = (T + tc - 1) / tc;
@@ -117,15 +136,18 @@ PW_HD WorkItem work_item(int u, int i, const int *first, const int *rk, const in
       hi = mid - 1;
   }
   const int e = rk[lo], cnt = off[e + 1] - off[e], ch = (cnt + tc - 1) / tc, loc = i - first[lo];
-  const int tile = loc / ch, c = loc - tile * ch;
+  const int np = u ? routed_down_splits(T, I) : 1;  // K parts
+  const int tile = loc / (np * ch), rem = loc - tile * np * ch;
+  const int part = rem / ch, c = rem - part * ch;
+  const int kcn = u ? kc_d : kc_gu, per = (kcn + np - 1) / np;
   w.kind = 0;
   w.expert = e;
   w.tile = tile;
   w.tok0 = c * tc;
   w.ntok = tc < cnt - c * tc ? tc : cnt - c * tc;
-  w.kc0 = 0;
-  w.kc1 = u ? kc_d : kc_gu;
-  w.part = 0;
+  w.kc0 = part * per;
+  w.kc1 = kcn < (part + 1) * per ? kcn : (part + 1) * per;
+  w.part = part;
   return w;
 }
 
@@ -235,7 +257,7 @@ struct Scratch {
   uint16_t *xs;        // fp16 [Tm*K][H]: xh rows in expert-sorted slot order
   uint16_t *h_routed;  // fp16 [Tm*K][I]
   uint16_t *h_shared;  // fp16 [Tm][Is]
-  float *o_routed;     // [Tm*K][H]
+  float *o_routed;     // [parts][T*K][H] partial sums of the routed down projection (routed_down_splits)
   float *o_shared;     // [splits][T][H] partial sums of the shared down projection
   float *inv_rms;      // [Tm] per-token 1/rms of the layer input (PW_PRENORM)
   float *sgate;        // [Tm] per-token shared-expert gate sigmoid(x . w_sg) (layers with a gate)

@@ -9,7 +9,8 @@
 //                  the work lists and routing statistics
 //   ffn (phase 1)  gate_up of every active expert and of the shared expert, SiLU(g)*u
 //   ffn (phase 2)  down projection of every active expert and of the shared expert
-//   combine_kernel y_t = sum_k r_tk o_tk (k order) + shared (+ y when accumulating)
+//   combine_kernel y_t = sum_k r_tk o_tk (k order; o_tk the sum of its K parts in order)
+//                  + shared (+ y when accumulating)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -35,15 +36,36 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
     s_w[threadIdx.x] = a.s.w[t * K + threadIdx.x];
   }
   __syncthreads();
+  const int np = routed_down_splits(a.T, a.I);  // K parts of the routed down projection
+  const size_t pstride = (size_t)a.T * K * H;
   for (int h = h_begin + threadIdx.x * 4; h < h_end; h += 256 * 4) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < K; ++k) {
-      const float4 o = *reinterpret_cast<const float4 *>(a.s.o_routed + (size_t)s_slot[k] * H + h);
-      const float r = s_w[k];
-      acc.x = fmaf(r, o.x, acc.x);
-      acc.y = fmaf(r, o.y, acc.y);
-      acc.z = fmaf(r, o.z, acc.z);
-      acc.w = fmaf(r, o.w, acc.w);
+    if (np == 1) {
+      for (int k = 0; k < K; ++k) {
+        const float4 o = *reinterpret_cast<const float4 *>(a.s.o_routed + (size_t)s_slot[k] * H + h);
+        const float r = s_w[k];
+        acc.x = fmaf(r, o.x, acc.x);
+        acc.y = fmaf(r, o.y, acc.y);
+        acc.z = fmaf(r, o.z, acc.z);
+        acc.w = fmaf(r, o.w, acc.w);
+      }
+    } else {
+      for (int k = 0; k < K; ++k) {
+        const float *op = a.s.o_routed + (size_t)s_slot[k] * H + h;
+        float4 o = *reinterpret_cast<const float4 *>(op);
+        for (int p = 1; p < np; ++p) {  // the parts' partial sums, in order
+          const float4 ov = *reinterpret_cast<const float4 *>(op + p * pstride);
+          o.x += ov.x;
+          o.y += ov.y;
+          o.z += ov.z;
+          o.w += ov.w;
+        }
+        const float r = s_w[k];
+        acc.x = fmaf(r, o.x, acc.x);
+        acc.y = fmaf(r, o.y, acc.y);
+        acc.z = fmaf(r, o.z, acc.z);
+        acc.w = fmaf(r, o.w, acc.w);
+      }
     }
     if (a.Is > 0) {  // the shared expert's partial sums, in order
       const int nsplit = shared_down_splits(a.I, a.Is);

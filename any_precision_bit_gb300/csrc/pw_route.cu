@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
     __syncthreads();
     if (tid < E) {  // item counts in rank order (the q table is no longer needed)
       s_q[0][r1] = ch * tiles1;
-      s_q[1][r2] = ch * tiles2;
+      s_q[1][r2] = ch * tiles2 * routed_down_splits(T, a.I);
       s_rk[0][r1] = tid;
       s_rk[1][r2] = tid;
     }

@@ -130,6 +130,34 @@ def test_tiny_layer_accumulate_in_place_and_renorm():
             pw.pw_destroy(ctx)
 
 
+# Split K parts.  NARROW: a routed down projection of one 128-column stage (I <= 128) beside
+# a long shared down projection (Is = 1200: ten stages), whose K parts hit the cap of 8 and
+# come out five parts of two stages.  LONGDOWN: a routed down projection of 40 stages
+# (I = 5008, not a multiple of 128), split at decode sizes into parts of 14, 14 and 12.
+NARROW = syn.LayerShape("narrow", H=256, E=8, I=112, K=2, Is=1200, L=1, bmax=8, bits=(3, 4, 5, 6, 7, 8),
+                        sigma_lut=0.02, zipf_a=None, q_rule="uniform")
+LONGDOWN = syn.LayerShape("longdown", H=256, E=6, I=5008, K=2, Is=0, L=1, bmax=8, bits=(3, 4, 5, 6, 7, 8),
+                          sigma_lut=0.02, zipf_a=None, q_rule="uniform")
+
+
+@pytest.mark.parametrize("name,T", [("narrow", 8), ("narrow", 40), ("longdown", 24), ("longdown", 200)])
+def test_split_k_parts(name, T):
+    shape = NARROW if name == "narrow" else LONGDOWN
+    data = LayerData(shape, 4, 0, T, real=range(shape.E))
+    ctx = make_ctx(pw, shape, L=1, max_tokens=T)
+    try:
+        data.load(pw, ctx)
+        y, ids, w = run_layer(ctx, data, T)
+        y_ref, ids_ref, w_ref = data.oracle()
+        assert np.array_equal(ids, ids_ref)
+        assert np.allclose(w, w_ref, rtol=1e-5, atol=1e-7)
+        assert_close(y, y_ref, f"{name} T={T}")
+        again, _, _ = run_layer(ctx, data, T)  # the parts are added in a fixed order
+        assert np.array_equal(y, again)
+    finally:
+        pw.pw_destroy(ctx)
+
+
 # ---------------------------------------------------------------- model-shaped layers
 CASES = [("qwen", 1), ("qwen", 16), ("qwen", 64), ("g128", 1), ("g128", 32), ("mixtral", 1), ("mixtral", 8)]
 
