@@ -76,8 +76,8 @@ PW_HD int shared_down_splits(int I, int Is) {
 // buffer, which the combine kernel adds in order.  Prefill-sized batches have items enough
 // and keep one part.  Every part holds at least one stage.
 PW_HD int routed_down_splits(int T, int I) {
-  if (T >= kPrefillMinT) return 1;
   const int st = kpad_cols(I) / kChunkCols;
+  if (T >= kPrefillMinT || st <= 16) return 1;
   int n = (st + 15) / 16;
   n = n < 1 ? 1 : (n > 8 ? 8 : n);
   const int per = (st + n - 1) / n;
@@ -137,11 +137,22 @@ PW_HD WorkItem work_item(int u, int i, const int *first, const int *rk, const in
   }
   const int e = rk[lo], cnt = off[e + 1] - off[e], ch = (cnt + tc - 1) / tc, loc = i - first[lo];
   const int np = u ? routed_down_splits(T, I) : 1;  // K parts
-  const int tile = loc / (np * ch), rem = loc - tile * np * ch;
-  const int part = rem / ch, c = rem - part * ch;
-  const int kcn = u ? kc_d : kc_gu, per = (kcn + np - 1) / np;
+  const int kcn = u ? kc_d : kc_gu;
   w.kind = 0;
   w.expert = e;
+  if (np == 1) {  // the whole K (every gate_up, and every down but long ones at decode sizes)
+    const int tile = loc / ch, c = loc - tile * ch;
+    w.tile = tile;
+    w.tok0 = c * tc;
+    w.ntok = tc < cnt - c * tc ? tc : cnt - c * tc;
+    w.kc0 = 0;
+    w.kc1 = kcn;
+    w.part = 0;
+    return w;
+  }
+  const int tile = loc / (np * ch), rem = loc - tile * np * ch;
+  const int part = rem / ch, c = rem - part * ch;
+  const int per = (kcn + np - 1) / np;
   w.tile = tile;
   w.tok0 = c * tc;
   w.ntok = tc < cnt - c * tc ? tc : cnt - c * tc;
