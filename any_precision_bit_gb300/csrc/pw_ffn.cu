@@ -37,6 +37,9 @@
 //     the chunk's slabs, A buffer and B tile when the MMAs are done;
 //   * epilogue (4 warps, one per lane quarter): tcgen05.ld of the accumulator, then
 //     h = silu(g) * u (gate_up) or the down output, while the next item is being computed.
+//     A down item that covers one K part (the shared expert's down, and at decode sizes a
+//     long routed down) writes that part's partial-sum buffer; the combine kernel adds the
+//     parts in order.
 // Every mbarrier wait is bounded: on expiry the kernel records an error (PW_ERR_TIMEOUT on
 // the host), every role stops, the producers and the MMA thread wait (bounded) for what they
 // issued, and tensor memory is freed before the kernel returns.
