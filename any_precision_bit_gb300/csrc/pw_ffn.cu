@@ -3,7 +3,7 @@
 //
 // PagedWeight Sec. 3.3: every active expert's linear block is read directly from its
 // bit-planes and LUT at its committed bitwidth q_i (Sec. 3.1 weight page table), the gate_up
-// output goes through SiLU(gate)*up ("expert activation"), and the down projection follows.
+// output goes through the expert activation SiLU(gate)*up, and the down projection follows.
 // The shared expert of the layer (Table 1) rides in the same launches.
 //
 // A work item is a 128-row tile of one block times up to TOK tokens: D[128][N] = W x X^T,

@@ -330,8 +330,8 @@ typedef struct {
     double kv_blocks;        /* KV blocks the request holds: its weight in the merge */
 } pw_request_signals;
 
-/* Batched serving (Sec. 3.2): "the planner first merges request-level signals into one
- * batch-level table".  Routing masses, prompt residuals, confidence scores and clipping
+/* Batched serving (Sec. 3.2): before planning, the signals of the batch's requests are
+ * merged into a single batch-level table.  Routing masses, prompt residuals, confidence scores and clipping
  * bounds are each averaged with weights kv_blocks / sum(kv_blocks), requests summed in
  * order.  Outputs (caller storage): mass [L][E], rho_hat [n_blocks][n_bits-1], conf
  * [2][n_bits-1], *rho_min, *rho_max; plan with them by passing rho_hat in pw_obs and conf
