@@ -13,9 +13,13 @@ Quality-Aware Weight Quantization"):
 * ``moe``     -- router, top-K, expert FFN and routing-weighted combine (Sec. 2.1, Sec. 3.3)
 * ``planner`` -- Eqs. 1, 2, 4-8 and the greedy planner step (Sec. 3.2, Algorithm 1)
 * ``pages``   -- the offload / reload ordering of weight pages (Sec. 3.1, Sec. 3.3, Fig. 4)
+* ``kv``      -- KV-block accounting coupled to the weight pages: the free-block count F_blk
+  of Eq. 7 from the budget the weights leave, the blocks held and the pending growth
+  (Sec. 3.2, Sec. 3.3)
 
 Parity status: ``ap`` and ``moe`` are pinned by closed forms, hand-worked examples and
 brute force; ``planner`` is pinned for Eqs. 1, 2, 4, 6, 7, 8 and a hand-sorted greedy
 example, but the stage/cap policy and the reload policy are readings of Algorithm 1
-with no printed numbers: parity unpinned for those two policies.
+with no printed numbers: parity unpinned for those two policies.  ``kv`` is pinned by a
+hand-worked sequence from its readings (the pages give the signals, not a formula).
 """
