@@ -44,7 +44,13 @@ class pw_block_info(C.Structure):
 
 class pw_mem_info(C.Structure):
     _fields_ = [("resident_bytes", C.c_int64), ("device_pool_bytes", C.c_int64),
-                ("device_pool_free", C.c_int64), ("pinned_bytes", C.c_int64), ("scratch_bytes", C.c_int64)]
+                ("device_pool_free", C.c_int64), ("pinned_bytes", C.c_int64), ("scratch_bytes", C.c_int64),
+                ("held_bytes", C.c_int64)]
+
+
+class pw_kv_stats(C.Structure):
+    _fields_ = [(n, C.c_int64) for n in ("budget_bytes", "block_bytes", "weight_bytes", "capacity_blocks",
+                                         "used_blocks", "pending_blocks", "free_blocks", "headroom_bytes")]
 
 
 class pw_obs(C.Structure):
@@ -111,6 +117,16 @@ _SIGS = {
     "pw_merge_requests": [C.POINTER(pw_request_signals), _I, _I, _I, _I, _I, _P, _P, _P, C.POINTER(C.c_double),
                           C.POINTER(C.c_double)],
     "pw_route_noalloc": [_P, _I, _P, _I, _P, _P, _I, _P],
+    "pw_kv_create": [C.c_int64, C.c_int64, C.POINTER(C.c_void_p)],
+    "pw_kv_destroy": [_P],
+    "pw_kv_set_weight_bytes": [_P, C.c_int64],
+    "pw_kv_attach": [_P, _P],
+    "pw_kv_announce": [_P, C.c_int64, C.c_int64],
+    "pw_kv_grow": [_P, C.c_int64, C.c_int64, _P],
+    "pw_kv_release": [_P, C.c_int64, C.POINTER(C.c_int64)],
+    "pw_kv_request": [_P, C.c_int64, C.POINTER(C.c_int64), C.POINTER(C.c_int64)],
+    "pw_kv_blocks": [_P, C.c_int64, _P, C.c_int64, C.POINTER(C.c_int64)],
+    "pw_kv_get_stats": [_P, C.POINTER(pw_kv_stats)],
     "pw_set_profiling": [_P, _I],
     "pw_profile_read": [_P, _I, _P],
     "pw_tc_selftest": [_P, _P, _I, _I, _I, _P, _P, _P],
@@ -134,7 +150,7 @@ def lib():
         for name, args in _SIGS.items():
             f = getattr(L, name)
             f.argtypes = args
-            f.restype = None if name == "pw_destroy" else (C.c_char_p if name in ("pw_last_error", "pw_version") else C.c_int)
+            f.restype = None if name in ("pw_destroy", "pw_kv_destroy") else (C.c_char_p if name in ("pw_last_error", "pw_version") else C.c_int)
         _lib = L
     return _lib
 
@@ -422,3 +438,62 @@ def pw_merge_requests(requests, kv_blocks, L, E, n_blocks, n_bits):
     _check(lib().pw_merge_requests(reqs, len(requests), L, E, n_blocks, n_bits, _ptr(mass), _ptr(rho), _ptr(conf),
                                    C.byref(lo), C.byref(hi)))
     return dict(mass=mass, rho_hat=rho, conf=conf, rho_min=lo.value, rho_max=hi.value)
+
+
+# ---------------------------------------------------------------- KV-block allocator
+def pw_kv_create(budget_bytes, block_bytes):
+    """A KV-block allocator over `budget_bytes` shared with the weight pages (handle)."""
+    kv = C.c_void_p()
+    _check(lib().pw_kv_create(int(budget_bytes), int(block_bytes), C.byref(kv)))
+    return kv
+
+
+def pw_kv_destroy(kv):
+    lib().pw_kv_destroy(kv)
+
+
+def pw_kv_set_weight_bytes(kv, weight_bytes):
+    _check(lib().pw_kv_set_weight_bytes(kv, int(weight_bytes)))
+
+
+def pw_kv_attach(kv, ctx):
+    _check(lib().pw_kv_attach(kv, ctx))
+
+
+def pw_kv_announce(kv, request, n_blocks):
+    _check(lib().pw_kv_announce(kv, int(request), int(n_blocks)))
+
+
+def pw_kv_grow(kv, request, n_blocks) -> np.ndarray:
+    """Grow a request; returns the granted block ids (int32).  PwError(PW_ERR_OOM) when the
+    free blocks do not suffice."""
+    ids = np.zeros(max(int(n_blocks), 1), dtype=np.int32)
+    _check(lib().pw_kv_grow(kv, int(request), int(n_blocks), ids.ctypes.data))
+    return ids[:int(n_blocks)]
+
+
+def pw_kv_release(kv, request) -> int:
+    n = C.c_int64()
+    _check(lib().pw_kv_release(kv, int(request), C.byref(n)))
+    return n.value
+
+
+def pw_kv_request(kv, request):
+    """(blocks held, blocks announced) of a request."""
+    held, ann = C.c_int64(), C.c_int64()
+    _check(lib().pw_kv_request(kv, int(request), C.byref(held), C.byref(ann)))
+    return held.value, ann.value
+
+
+def pw_kv_blocks(kv, request) -> np.ndarray:
+    n = C.c_int64()
+    _check(lib().pw_kv_blocks(kv, int(request), None, 0, C.byref(n)))
+    ids = np.zeros(max(n.value, 1), dtype=np.int32)
+    _check(lib().pw_kv_blocks(kv, int(request), ids.ctypes.data, n.value, C.byref(n)))
+    return ids[:n.value]
+
+
+def pw_kv_get_stats(kv) -> dict:
+    st = pw_kv_stats()
+    _check(lib().pw_kv_get_stats(kv, C.byref(st)))
+    return {name: getattr(st, name) for name, _ in pw_kv_stats._fields_}

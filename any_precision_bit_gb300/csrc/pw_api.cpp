@@ -1087,8 +1087,14 @@ pw_status pw_query(pw_ctx *c, int block, pw_block_info *info) {
 pw_status pw_memory(pw_ctx *c, pw_mem_info *info) {
   if (!c || !info) return fail(c, PW_ERR_INVALID, "null argument");
   *info = pw_mem_info{};
-  for (const auto &b : c->blocks)
-    if (b.packed) info->resident_bytes += block_M(c, b, b.q);
+  for (const auto &b : c->blocks) {
+    if (!b.packed) continue;
+    info->resident_bytes += block_M(c, b, b.q);
+    for (int p = 0; p < kMaxPlanes; ++p)
+      if (b.dplane[p]) info->held_bytes += (int64_t)b.plane_bytes;
+    for (int bb = 1; bb <= 8; ++bb)
+      if (b.dlut[bb]) info->held_bytes += (int64_t)b.lut_bytes[bb];
+  }
   info->device_pool_bytes = c->dpool.reserved;
   info->device_pool_free = c->dpool.free_bytes;
   info->pinned_bytes = c->hpool.reserved;

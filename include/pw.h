@@ -246,6 +246,8 @@ typedef struct {
     int64_t device_pool_free; /* of which free for reuse */
     int64_t pinned_bytes;     /* pinned host bytes reserved for CPU-resident pages */
     int64_t scratch_bytes;    /* forward scratch */
+    int64_t held_bytes;       /* device bytes of the weight pages the GPU holds: resident, in
+                                 transfer, or lowered but not yet retired by pw_commit */
 } pw_mem_info;
 pw_status pw_memory(pw_ctx *ctx, pw_mem_info *info);
 
@@ -347,6 +349,61 @@ pw_status pw_merge_requests(const pw_request_signals *req, int n_req, int L, int
  * entry of the plan can be applied at once.  Writes the desired bitwidth d_i of every
  * planned block.  Applying the plan is the caller's pw_offload / pw_reload. */
 pw_status pw_plan_step(pw_ctx *ctx, const pw_obs *obs, const pw_offline *off, pw_plan *out);
+
+/* ---------------------------------------------------------------- KV-block allocator */
+
+/* The KV blocks of a paged KV cache and the weight pages share one device budget: the pages
+ * an offload retires become headroom for KV blocks, and the planner follows the free KV
+ * blocks, the allocator headroom and the pending KV growth (Sec. 3.3).  This allocator hands
+ * out logical block ids and keeps the free-block count F_blk that Eq. 7 (Sec. 3.2) turns into
+ * the planner's byte target, with S the budget, W the weight-page bytes and B the block size:
+ *   capacity  C = floor(max(0, S - W) / B) blocks
+ *   U = blocks held by requests, P = blocks announced as pending growth
+ *   F_blk = C - U - P  (negative when the budget is overcommitted; pass it as pw_obs.F_blk)
+ *   headroom = S - W - U * B bytes
+ * W is either set by the caller or read, on every call that needs it, from an attached
+ * context (its pw_mem_info.held_bytes, so pages count until pw_commit retires them).  A
+ * request is any int64 key.  Host only; an allocator is used by one thread at a time. */
+typedef struct pw_kv pw_kv;
+
+typedef struct {
+    int64_t budget_bytes;     /* S */
+    int64_t block_bytes;      /* B */
+    int64_t weight_bytes;     /* W */
+    int64_t capacity_blocks;  /* C */
+    int64_t used_blocks;      /* U */
+    int64_t pending_blocks;   /* P */
+    int64_t free_blocks;      /* F_blk = C - U - P */
+    int64_t headroom_bytes;   /* S - W - U * B */
+} pw_kv_stats;
+
+/* budget_bytes >= 0, block_bytes > 0 and budget_bytes / block_bytes < 2^31 (ids are int32),
+ * else PW_ERR_INVALID.  W starts at 0. */
+pw_status pw_kv_create(int64_t budget_bytes, int64_t block_bytes, pw_kv **out);
+void pw_kv_destroy(pw_kv *kv);
+/* W = weight_bytes (>= 0) from now on; detaches a context. */
+pw_status pw_kv_set_weight_bytes(pw_kv *kv, int64_t weight_bytes);
+/* W = ctx's held weight-page bytes from now on (ctx must outlive the attachment; NULL
+ * detaches and keeps the last value read).  PW_ERR_* of pw_memory when reading fails. */
+pw_status pw_kv_attach(pw_kv *kv, pw_ctx *ctx);
+/* Request r expects to need n_blocks (>= 0) more blocks soon; replaces its previous
+ * announcement.  The announced blocks count as taken in F_blk. */
+pw_status pw_kv_announce(pw_kv *kv, int64_t request, int64_t n_blocks);
+/* Grow request r by n_blocks (>= 0): c = min(n, r's announcement) of them come out of the
+ * announcement, the other n - c must fit in F_blk, else PW_ERR_OOM and nothing changes.
+ * The granted ids -- the lowest free ones, ascending -- go to ids_out[0..n-1] (NULL: not
+ * written). */
+pw_status pw_kv_grow(pw_kv *kv, int64_t request, int64_t n_blocks, int32_t *ids_out);
+/* Return every block of request r and drop its announcement; the count to *n_released
+ * (may be NULL).  An unknown request releases nothing. */
+pw_status pw_kv_release(pw_kv *kv, int64_t request, int64_t *n_released);
+/* Blocks request r holds and has announced (0 and 0 for an unknown request); either
+ * pointer may be NULL.  The held count is the request's weight in pw_merge_requests. */
+pw_status pw_kv_request(const pw_kv *kv, int64_t request, int64_t *held, int64_t *announced);
+/* Request r's block table in the order granted: *n = its block count, and the first
+ * min(*n, capacity) ids go to ids_out. */
+pw_status pw_kv_blocks(const pw_kv *kv, int64_t request, int32_t *ids_out, int64_t capacity, int64_t *n);
+pw_status pw_kv_get_stats(pw_kv *kv, pw_kv_stats *out);
 
 /* ---------------------------------------------------------------- inspection */
 

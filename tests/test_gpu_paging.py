@@ -174,3 +174,44 @@ def test_resident_bytes_follow_eq3(tiny):
     pw.pw_sync_io(ctx)
     pw.pw_commit(ctx)
     assert pw.pw_memory(ctx).resident_bytes == expected()
+
+
+def test_kv_allocator_follows_the_held_pages(tiny):
+    """The KV-block allocator attached to a context: its weight bytes are the device pages
+    the context holds, so an offload frees KV blocks only once pw_commit retires its pages,
+    and a reload takes them back when it allocates its pages (Sec. 3.3)."""
+    shape, T, data, ctx = tiny
+    B = 4096
+    mem = pw.pw_memory(ctx)
+    W0 = mem.held_bytes
+    assert W0 == mem.resident_bytes  # every page resident, LUT rows a multiple of 128
+    S = W0 + 40 * B + 123
+    kv = pw.pw_kv_create(S, B)
+    try:
+        pw.pw_kv_attach(kv, ctx)
+        pw.pw_kv_grow(kv, 7, 5)
+        st = pw.pw_kv_get_stats(kv)
+        assert st["weight_bytes"] == W0 and st["free_blocks"] == (S - W0) // B - 5
+        block = syn.block_id(0, data.routed[0], 0, shape.E)
+        N, K = syn.block_shape(shape, 0)
+        delta = ap.delta_bytes(N, K, shape.bits, 6, 3)
+        pw.pw_set_fault(ctx, 3, 1)  # hold the copy in flight
+        pw.pw_offload(ctx, block, 3)
+        assert pw.pw_memory(ctx).resident_bytes == W0 - delta
+        assert pw.pw_kv_get_stats(kv) == st  # the pages are still held
+        pw.pw_sync_io(ctx)
+        pw.pw_set_fault(ctx, 3, 0)
+        pw.pw_commit(ctx)
+        st = pw.pw_kv_get_stats(kv)
+        assert st["weight_bytes"] == W0 - delta
+        assert st["free_blocks"] == (S - W0 + delta) // B - 5
+        assert st["headroom_bytes"] == S - (W0 - delta) - 5 * B
+        pw.pw_reload(ctx, block, 6)  # allocates the pages at once
+        assert pw.pw_kv_get_stats(kv)["weight_bytes"] == W0
+        pw.pw_sync_io(ctx)
+        assert pw.pw_commit(ctx) == 1
+        assert pw.pw_kv_get_stats(kv)["free_blocks"] == (S - W0) // B - 5
+        pw.pw_kv_set_weight_bytes(kv, 0)  # detached
+        assert pw.pw_kv_get_stats(kv)["weight_bytes"] == 0
+    finally:
+        pw.pw_kv_destroy(kv)
