@@ -229,3 +229,32 @@ def test_planner_loop_closed_through_the_allocator(seed):
         assert {1, 2} <= kinds  # pressure met by offloads, and slack returned by reloads
     finally:
         lib.close()
+
+
+def test_batch_merge_weighted_by_the_allocator():
+    """F4 fed by F1: the batch-level table merges each live request's signals with the KV
+    blocks the allocator says it holds (Sec. 3.2, batched serving), and equals the oracle's
+    merge with its own accounting's counts."""
+    rng = np.random.default_rng(11)
+    L, E, n, nb = 2, 6, 24, 4
+    S, B = 1 << 30, 1 << 20
+    lib, ref = Lib(S, B), okv.KVAllocator(S, B)
+    try:
+        live = list(range(5))
+        for r in live:
+            k = int(rng.integers(1, 30))
+            assert apply(lib, "grow", r, k) == apply(ref, "grow", r, k)
+        assert apply(lib, "release", 2, 0) == apply(ref, "release", 2, 0)
+        live.remove(2)
+        reqs = [dict(mass=rng.dirichlet(np.ones(E), size=L), rho_hat=rng.normal(0, 1, (n, nb - 1)),
+                     conf=rng.uniform(0.5, 1.0, (2, nb - 1)), rho_min=float(rng.uniform(-3, -1)),
+                     rho_max=float(rng.uniform(1, 3))) for _ in live]
+        w_c = [float(lib.request(r)[0]) for r in live]
+        w_o = [float(ref.request(r)[0]) for r in live]
+        assert w_c == w_o and all(w > 0 for w in w_c)
+        got = pw.pw_merge_requests(reqs, w_c, L, E, n, nb)
+        want = opl.merge_request_signals(reqs, w_o)
+        for key in ("mass", "rho_hat", "conf", "rho_min", "rho_max"):
+            assert np.array_equal(np.asarray(got[key]), np.asarray(want[key])), key
+    finally:
+        lib.close()
