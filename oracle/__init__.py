@@ -19,7 +19,7 @@ Quality-Aware Weight Quantization"):
 
 Parity status: ``ap`` and ``moe`` are pinned by closed forms, hand-worked examples and
 brute force; ``planner`` is pinned for Eqs. 1, 2, 4, 6, 7, 8 and a hand-sorted greedy
-example, but the stage/cap policy and the reload policy are readings of Algorithm 1
-with no printed numbers: parity unpinned for those two policies.  ``kv`` is pinned by a
+example, and its stage/cap policy and reload policy -- readings of Algorithm 1 with no
+printed numbers -- by invariants that hold on any input.  ``kv`` is pinned by a
 hand-worked sequence from its readings (the pages give the signals, not a formula).
 """

@@ -6,7 +6,10 @@ Closed forms: routing mass (Eq. 1), Hessian-weighted sensitivity (Eq. 2), global
 target bytes, then for every bitwidth-floor stage ScoreActions -> GreedySelect ->
 RefreshPlanQueue, then SelectBestPlan when pressure is triggered.
 
-Readings of what Algorithm 1 leaves open (parity unpinned beyond the hand example):
+Readings of what Algorithm 1 leaves open.  The pages print no numbers for them; they are
+pinned by the hand-sorted greedy example and by invariants that hold on any input (level
+caps, bucket floors, Eq. 3 deltas, stage monotonicity, the choice of SelectBestPlan, the
+reload budget and where a reload stops):
 * a step is a single-level reduction b -> b' (b' the next lower supported bitwidth);
   taking a block's step unlocks its next lower step;
 * buckets: experts of a layer sorted by routing mass (descending, ties to the lower
