@@ -154,6 +154,18 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# ---------------------------------------------------------------- ranks
+def reduce_max_over_ranks(dist, values, device):
+    """The job's time is its slowest rank's: each value replaced by its maximum over the
+    ranks (a no-op without a process group)."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 # ---------------------------------------------------------------- workload set-up
 def load_stack(pw, torch, shape, L, T, seed, device):
     from synthetic.gen_torch import gen_block_torch, gen_shared_torch
@@ -387,9 +399,8 @@ def run_ours(args, shape, L, T):
     ms = ev0.elapsed_time(ev1) / args.steps
     clk = clocks.stop()
     if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        dist.barrier()
+    ms = reduce_max_over_ranks(dist, [ms], "cuda")[0]
     # Kernel durations, per layer: a second timed pass with CUDA events recorded between the
     # kernels on the launching stream.  The events serialise the kernels (the step above lets
     # each kernel start while its predecessor drains, through programmatic dependent launch),
@@ -464,10 +475,15 @@ def run_ours(args, shape, L, T):
         xh = torch.from_numpy(syn.gen_tokens_np(shape, args.seed, 0, T).view(np.int16)).pin_memory()
         yh = torch.empty_like(xh).pin_memory()
         pw.pw_stack_forward_host(ctx, xh, T, yh)
+        if dist:
+            dist.barrier()
         t0 = time.perf_counter()
         for _ in range(args.steps):
             pw.pw_stack_forward_host(ctx, xh, T, yh)
         te = (time.perf_counter() - t0) / args.steps
+        if dist:
+            dist.barrier()
+        te = reduce_max_over_ranks(dist, [te], "cuda")[0]
         line["e2e"] = {"value": world * T * L / te, "unit": "tokens/s", "ms_per_step": te * 1e3,
                        "h2d_bytes_per_step": T * shape.H * 2, "d2h_bytes_per_step": T * shape.H * 2}
     if rank == 0 and not args.no_cpu_baseline:
