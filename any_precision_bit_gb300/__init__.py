@@ -128,6 +128,7 @@ _SIGS = {
     "pw_kv_blocks": [_P, C.c_int64, _P, C.c_int64, C.POINTER(C.c_int64)],
     "pw_kv_get_stats": [_P, C.POINTER(pw_kv_stats)],
     "pw_set_profiling": [_P, _I],
+    "pw_set_gemv_tokens": [_P, _I],
     "pw_profile_read": [_P, _I, _P],
     "pw_tc_selftest": [_P, _P, _I, _I, _I, _P, _P, _P],
     "pw_unpack_indices": [_P, _I, _I, _P],
@@ -305,6 +306,10 @@ def pw_set_fault(ctx, kind, n):
 
 def pw_route_noalloc(ctx, layer, x, T, ids, w, flags=0, stream=None):
     _check(lib().pw_route_noalloc(ctx, layer, _ptr(x), T, _ptr(ids), _ptr(w), flags, _stream(stream)), ctx)
+
+
+def pw_set_gemv_tokens(ctx, max_tokens):
+    _check(lib().pw_set_gemv_tokens(ctx, int(max_tokens)), ctx)
 
 
 def pw_set_profiling(ctx, on):

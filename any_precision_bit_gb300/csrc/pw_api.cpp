@@ -23,9 +23,10 @@ namespace {
 thread_local std::string g_thread_err;
 
 // 2-D fp16 tensor map over a row-major [rows][cols] buffer: boxes of 64 columns (128 bytes)
-// by box_rows rows with the 128-byte swizzle, out-of-range elements read as zero.  The encoder is
-// the driver's, looked up through the runtime (no link-time dependency on the driver library).
-bool encode_act_map(TmaDesc *out, void *base, long rows, long cols, unsigned box_rows) {
+// by box_rows rows with the 128-byte swizzle (or, with box_cols = 128, 128 columns by box_rows
+// rows without swizzle), out-of-range elements read as zero.  The encoder is the driver's,
+// looked up through the runtime (no link-time dependency on the driver library).
+bool encode_act_map(TmaDesc *out, void *base, long rows, long cols, unsigned box_rows, unsigned box_cols = 64) {
   using Encode = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                               const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -43,11 +44,11 @@ bool encode_act_map(TmaDesc *out, void *base, long rows, long cols, unsigned box
   static_assert(sizeof(CUtensorMap) == sizeof(TmaDesc), "tensor map size");
   const cuuint64_t dim[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t stride[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estride[2] = {1, 1};
   return fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base, dim, stride, box, estride,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // ------------------------------------------------------------------ page pools
@@ -175,6 +176,7 @@ struct pw_ctx {
   int sticky = 0;
   int fault_copy = 0, fault_alloc = 0;
   int hold = 0;  // testing: transfers are not observed as landed while set
+  int gemv_max = kGemvDefaultTokens;  // routed items of at most this many tokens run on the CUDA cores
 };
 
 namespace {
@@ -426,6 +428,8 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             encode_act_map(&m.h_routed, c->s.h_routed, TK, d.I, br) &&
             (d.Is == 0 || encode_act_map(&m.h_shared, c->s.h_shared, Tm, d.Is, br));
     }
+    enc = enc && encode_act_map(&c->bmaps.gemv.xs, c->s.xs, TK, d.H, 8u, 128u) &&
+          encode_act_map(&c->bmaps.gemv.h_routed, c->s.h_routed, TK, d.I, 8u, 128u);
     if (!enc) {
       fail(nullptr, PW_ERR_CUDA, "tensor map encoding failed");
       return bail(PW_ERR_CUDA);
@@ -701,6 +705,7 @@ static pw_status forward_args(pw_ctx *c, int layer, const void *x, int T, void *
   a->ids_out = ids;
   a->w_out = w;
   a->sm_count = c->sm_count;
+  a->gemv_max = c->gemv_max;
   a->bmaps = c->has_bmaps ? &c->bmaps : nullptr;
   return PW_OK;
 }
@@ -1228,6 +1233,16 @@ pw_status pw_plan_step(pw_ctx *c, const pw_obs *obs, const pw_offline *off, pw_p
     out->entries[k].block = ids[out->entries[k].block];
     c->blocks[out->entries[k].block].d = out->entries[k].to_bits;
   }
+  return PW_OK;
+}
+
+// ================================================================== decode kernel choice
+pw_status pw_set_gemv_tokens(pw_ctx *c, int max_tokens) {
+  if (!c) return fail(nullptr, PW_ERR_INVALID, "null context");
+  if (max_tokens < 0 || max_tokens > kGemvMaxTokens)
+    return fail(c, PW_ERR_INVALID, "GEMV token threshold %d outside 0..%d", max_tokens, kGemvMaxTokens);
+  if (c->gemv_max != max_tokens) drop_graphs(c);  // captured launches hold the old threshold
+  c->gemv_max = max_tokens;
   return PW_OK;
 }
 

@@ -15,28 +15,49 @@ __device__ __forceinline__ uint16_t f2h(float f) { return __half_as_ushort(__flo
 __device__ __forceinline__ uint32_t pack2(uint32_t lo, uint32_t hi) { return (lo & 0xFFFFu) | (hi << 16); }
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
+// One step of a bit-matrix transpose: the bits of b under mask M trade places with the bits
+// of a under M << S.  Written as two masked merges (one three-input logic operation each)
+// of a with b << S and of b with a >> S, which takes fewer integer-pipe instructions than
+// the usual exchange through a XOR difference.
+// Shifts by a constant written as multiplies (low and high word of x * 2^s), which the
+// multiply-add pipe executes, to leave the integer/logic pipe to the masked merges.
+template <int S>
+__device__ __forceinline__ uint32_t shl_mul(uint32_t x) {
+  uint32_t r;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(r) : "r"(x), "n"(1u << S));
+  return r;
+}
+template <int S>
+__device__ __forceinline__ uint32_t shr_mul(uint32_t x) {
+  uint32_t r;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(r) : "r"(x), "n"(1u << (32 - S)));
+  return r;
+}
+
+template <int S, uint32_t M>
+__device__ __forceinline__ void bit_swap(uint32_t &a, uint32_t &b) {
+  constexpr uint32_t MH = M << S;
+  const uint32_t bs = shl_mul<S>(b), as = shr_mul<S>(a);
+  const uint32_t na = (a & ~MH) | (bs & MH);
+  const uint32_t nb = (b & ~M) | (as & M);
+  a = na;
+  b = nb;
+}
+
 // 8x8 bit transpose inside every byte column of eight words:
 // out word s, bit (8e + p) = in word p, bit (8e + s).
 __device__ __forceinline__ void transpose8(uint32_t (&X)[8]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t t = ((X[j] >> 4) ^ X[j + 4]) & 0x0F0F0F0Fu;
-    X[j + 4] ^= t;
-    X[j] ^= t << 4;
-  }
+  for (int j = 0; j < 4; ++j) bit_swap<4, 0x0F0F0F0Fu>(X[j], X[j + 4]);
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const int j = (jj & 1) + (jj >> 1) * 4;  // 0,1,4,5
-    uint32_t t = ((X[j] >> 2) ^ X[j + 2]) & 0x33333333u;
-    X[j + 2] ^= t;
-    X[j] ^= t << 2;
+    bit_swap<2, 0x33333333u>(X[j], X[j + 2]);
   }
 #pragma unroll
   for (int jj = 0; jj < 4; ++jj) {
     const int j = 2 * jj;  // 0,2,4,6
-    uint32_t t = ((X[j] >> 1) ^ X[j + 1]) & 0x55555555u;
-    X[j + 1] ^= t;
-    X[j] ^= t << 1;
+    bit_swap<1, 0x55555555u>(X[j], X[j + 1]);
   }
 }
 
@@ -63,6 +84,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// try_wait with a suspend-time hint: a thread whose phase is not complete is taken off the
+// scheduler until the phase completes or about `ns` nanoseconds pass, instead of spending
+// issue slots on polling.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
       : "memory");
   return ok != 0;
 }

@@ -13,8 +13,12 @@
 //   wider: an 8x8 bit transpose gives word s, byte e = the code of column
 //           8 (s & 3) + 2e + (s >> 2).  The LUT is in shared memory in the tiled layout of
 //           lut_dev_index (pw_internal.h): the code is byte 1 of its entry's address, so one
-//           byte permute forms the address, every lane of a warp reads its own bank, and a
-//           second permute picks the row's half of each word.
+//           byte permute forms the address, every lane of a warp reads its own bank, and two
+//           16-bit loads joined by a multiply-add give each pair.
+// The decode keeps the integer/logic pipe busiest (it issues at half the rate of the
+// multiply-add pipe), so the steps are chosen to spend as few of its instructions as they
+// can: masked-merge transposes, no separate step for the table's address bits, and the
+// pairs joined on the multiply-add pipe.
 #pragma once
 #include <stdint.h>
 
@@ -25,7 +29,10 @@ namespace pw {
 // Widths up to this one look centroids up in registers (byte permutes); wider ones in the
 // shared-memory LUT.  At 4 bits the shared-memory path is the faster one: the register path
 // needs a second level of permutes to pick between two 8-entry halves.
-constexpr int kRegLutMaxQ = 3;
+#ifndef PW_REG_LUT_MAX_Q
+#define PW_REG_LUT_MAX_Q 3
+#endif
+constexpr int kRegLutMaxQ = PW_REG_LUT_MAX_Q;
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
@@ -37,17 +44,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // out word s, bit (4i + p) = in word p, bit (4i + s).
 __device__ __forceinline__ void transpose4(uint32_t (&X)[4]) {
 #pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint32_t t = ((X[j] >> 2) ^ X[j + 2]) & 0x33333333u;
-    X[j + 2] ^= t;
-    X[j] ^= t << 2;
-  }
+  for (int j = 0; j < 2; ++j) bit_swap<2, 0x33333333u>(X[j], X[j + 2]);
 #pragma unroll
-  for (int j = 0; j < 4; j += 2) {
-    const uint32_t t = ((X[j] >> 1) ^ X[j + 1]) & 0x55555555u;
-    X[j + 1] ^= t;
-    X[j] ^= t << 1;
-  }
+  for (int j = 0; j < 4; j += 2) bit_swap<1, 0x55555555u>(X[j], X[j + 1]);
 }
 
 // A LUT of up to 16 centroids as byte planes: lo[m] byte b = low byte of entry 4m + b,
@@ -106,11 +105,14 @@ __device__ __forceinline__ void dq_nib(const uint32_t (&S)[4], const LutRegs &L,
 }
 
 // Q >= 4 (any Q works): codes of the 32 columns, word s byte e = code of column
-// 8 (s & 3) + 2e + (s >> 2), plane 0 in bit Q - 1 (the byte is the code itself).
+// 8 (s & 3) + 2e + (s >> 2), plane 0 in bit Q - 1 (the byte is the code itself).  For Q <= 7
+// bit 7 of every byte is bit 7 of `top` (0 or ~0): the shared-memory LUT addressing below
+// uses it for the table's address bit 15.
 template <int Q>
-__device__ __forceinline__ void codes_byte(const uint32_t (&W)[8], uint32_t (&Y)[8]) {
+__device__ __forceinline__ void codes_byte(const uint32_t (&W)[8], uint32_t (&Y)[8], uint32_t top = 0u) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) Y[i] = 0u;
+  if constexpr (Q < 8) Y[7] = top;
 #pragma unroll
   for (int p = 0; p < Q; ++p) Y[Q - 1 - p] = W[p];
   transpose8(Y);
@@ -119,16 +121,32 @@ __device__ __forceinline__ void codes_byte(const uint32_t (&W)[8], uint32_t (&Y)
 // Shared-memory LUT of the tiled layout (lut_dev_index) as seen by one lane: `word0` is the
 // address of the lane's word for code 0 (table base + 128 (m >> 1) + 4 L for lane quarter m,
 // lane L; the table base is 64 KB-aligned, or 32 KB past that for a table of at most 128
-// codes), `half` selects the lane's row in each word (0x5410: low halves, 0x7632: high).
+// codes), `half` selects the lane's row in each word (0x5410: low halves, 0x7632: high),
+// `h16` is the address of the lane's own 16-bit centroid of code 0 and `top` the word that
+// codes_byte needs for the table's address bit 15.
 struct LutLane {
-  uint32_t word0, half;
+  uint32_t word0, half, h16, top;
 };
 __device__ __forceinline__ LutLane lut_lane(uint32_t table, int quarter, int lane) {
-  return LutLane{table + 128u * (uint32_t)(quarter >> 1) + 4u * (uint32_t)lane, (quarter & 1) ? 0x7632u : 0x5410u};
+  const uint32_t w0 = table + 128u * (uint32_t)(quarter >> 1) + 4u * (uint32_t)lane;
+  return LutLane{w0, (quarter & 1) ? 0x7632u : 0x5410u, w0 + 2u * (uint32_t)(quarter & 1),
+                 (table & 0x8000u) ? 0xFFFFFFFFu : 0u};
 }
 __device__ __forceinline__ uint32_t lds_b32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+// lo | hi << 16 for 16-bit lo and hi, as a multiply-add (the multiply-add pipe is idle while
+// the decode keeps the integer pipe busy)
+__device__ __forceinline__ uint32_t pack_mad(uint32_t lo, uint32_t hi) {
+  uint32_t v;
+  asm("mad.lo.u32 %0, %1, 65536, %2;" : "=r"(v) : "r"(hi), "r"(lo));
   return v;
 }
 
@@ -143,22 +161,19 @@ __device__ __forceinline__ void lut_pairs_smem(const LutLane &lu, uint32_t (&P)[
   }
 }
 
-// Q >= 4: centroids from the lane's LUT in shared memory.
+// Q >= 4: centroids from the lane's LUT in shared memory.  The code is byte 1 of its entry's
+// address (codes_byte put the table's address bit 15 into bit 7 of each code byte), so one
+// byte permute with the lane's address forms it; two 16-bit loads and a multiply-add make
+// the pair.
 template <int Q>
 __device__ __forceinline__ void dq_byte(const uint32_t (&Y)[8], const LutLane &lu, uint32_t (&v)[16]) {
-  // byte e of Z = the code | byte 1 of the lane's word address; a permute with the
-  // address's other bytes is the entry's word address
-  const uint32_t hib = ((lu.word0 >> 8) & 0xFFu) * 0x01010101u;
-  uint32_t Z[8];
-#pragma unroll
-  for (int s = 0; s < 8; ++s) Z[s] = Y[s] | hib;
 #pragma unroll
   for (int s = 0; s < 4; ++s)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t lo = lds_b32(prmt(Z[s], lu.word0, 0x7604u | ((uint32_t)e << 4)));
-      const uint32_t hi = lds_b32(prmt(Z[s + 4], lu.word0, 0x7604u | ((uint32_t)e << 4)));
-      v[4 * s + e] = prmt(lo, hi, lu.half);
+      const uint32_t lo = lds_u16(prmt(Y[s], lu.h16, 0x7604u | ((uint32_t)e << 4)));
+      const uint32_t hi = lds_u16(prmt(Y[s + 4], lu.h16, 0x7604u | ((uint32_t)e << 4)));
+      v[4 * s + e] = pack_mad(lo, hi);
     }
 }
 
@@ -171,7 +186,7 @@ template <int Q>
 __device__ __forceinline__ uint32_t code_byte(const uint32_t (&Y)[8], int c) {
   const int j = c >> 3, i = c & 7;  // column 8j + i = 8 (s & 3) + 2e + (s >> 2)
   const int s = j + 4 * (i & 1), e = i >> 1;
-  return (Y[s] >> (8 * e)) & 0xFFu;
+  return (Y[s] >> (8 * e)) & ((1u << Q) - 1u);
 }
 
 }  // namespace pw

@@ -53,8 +53,15 @@
 
 namespace pw {
 
-constexpr int kDq = 16;                     // dequantising warps 0..15
-constexpr int kEpi = 4;                     // epilogue warps 16..19
+// Routed work items of at most FwdArgs::gemv_max tokens (decode tiling) run on the CUDA cores
+// (GEMV) instead of the tensor cores; kGemvMaxTok bounds that threshold.
+constexpr int kGemvMaxTok = kGemvMaxTokens;
+static_assert(kGemvMaxTok >= 1 && kGemvMaxTok <= 8, "GEMV items hold at most 8 tokens");
+constexpr int kGxSlots = 4;                 // activation slots of the GEMV items: one per chunk stream
+constexpr int kGxBytes = 8 * kChunkCols * 2;  // one slot: 8 rows x 128 fp16 columns
+constexpr int kDqStreams = 4;               // chunk streams of dequantising warps
+constexpr int kDq = 4 * kDqStreams;         // dequantising warps 0 .. 15 (warp w: lane quarter w & 3, stream w >> 2)
+constexpr int kEpi = 4;                     // epilogue warps
 constexpr int kWarpP = kDq + kEpi;          // weight producer
 constexpr int kWarpAB = kWarpP + 1;         // activation producer
 constexpr int kWarpMma = kWarpP + 2;        // MMA issuer, tensor-memory owner
@@ -62,6 +69,7 @@ constexpr int kWarpLut = kWarpP + 3;        // LUT producer
 constexpr int kTcThreads = (kWarpLut + 1) * 32;
 constexpr int kSlab = kCtaRows * 16;        // 2 KB: one plane of a 128-row tile and 128 columns
 constexpr int kRing = 16;                   // chunks in flight (full/empty barrier pairs)
+static_assert(kRing % kDqStreams == 0, "each barrier of the routed-chunk rings belongs to one chunk stream");
 constexpr int kQueue = 8;                   // claimed work items published to the roles
 constexpr int kQueueReaders = kDq + kEpi + 3;  // warps that read the queue (all but the weight producer)
 constexpr int kAStagesMax = 6;              // tensor-memory A buffers (at most)
@@ -91,14 +99,17 @@ struct Tiling {
   static constexpr int kBoxRows = TOK == 64 ? 16 : 128;  // rows of one TMA box
   static constexpr int kAStages = TOK == 64 ? 4 : 4;
   static_assert(kAStages <= kAStagesMax && kAColBase + kAStages * kACols <= kTmemCols, "tensor memory");
+  static_assert(kAStages % 4 == 0, "each A buffer belongs to one chunk stream");
   static_assert(kBStages <= kBStagesMax, "activation stages");
 };
-constexpr long kSpinLimit = 1L << 22;
+constexpr uint32_t kWaitSleepNs = 20000;          // suspend-time hint of a barrier wait
+constexpr long long kWaitLimitCycles = 1LL << 32;  // a wait gives up after this many SM cycles (about 2 s)
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
 // Shared-memory map.  The host fills npad_max, b_bytes and smem (the dynamic size);
 // the kernel places the regions by absolute shared address: the first kBLowStages
-// activation stages and the mbarriers at the start of the dynamic area, the two LUT slots at
+// activation stages, the GEMV items' activation slots and the mbarriers at the start of the
+// dynamic area, the two LUT slots at
 // [64 KB, 128 KB) (the tiled LUT layout needs a 64 KB-aligned table), then the other
 // activation stages (prefill tiling), and the slab ring to the end.
 struct TcLayout {
@@ -111,6 +122,7 @@ struct TcLayout {
   int b_off;       // activation stages 0 .. kBLowStages - 1
   int b_hi;        // activation stages kBLowStages ..
   int lut_off;     // LUT slots
+  int gx_off;      // activation slots of the GEMV items
   int bar_off;     // mbarriers
 };
 constexpr uint32_t kLutAddr = 64 * 1024;
@@ -120,11 +132,13 @@ constexpr uint32_t kRingAddr = 128 * 1024;
 enum {
   kWFR = 0, kWFD = kWFR + kRing, kWE = kWFD + kRing, kTAF = kWE + kRing, kTAE = kTAF + kAStagesMax, kBF = kTAE + kAStagesMax,
   kBE = kBF + kBStagesMax, kLF = kBE + kBStagesMax, kLE = kLF + 2, kAF = kLE + 2, kAE = kAF + 2, kDrain = kAE + 2,
-  kIQF = kDrain + 1, kIQE = kIQF + kQueue, kNumBars = kIQE + kQueue
+  kIQF = kDrain + 1, kIQE = kIQF + kQueue, kGXF = kIQE + kQueue, kGXE = kGXF + kGxSlots, kGAG = kGXE + kGxSlots,
+  kAFG = kGAG + 2, kRD = kAFG + 2, kNumBars = kRD + kRing
 };
 
 struct ItemView {
   bool routed;
+  bool gemv;     // routed item of at most kGemvMaxTok tokens at the decode tiling: CUDA-core dot products
   int q;         // routed: committed bitwidth
   int nr;        // rows of this CTA tile
   int KC;        // 128-column chunks of the K dimension
@@ -152,8 +166,10 @@ __device__ __forceinline__ ItemView view_item(const FwdArgs &a, const WorkItem &
     v.row0 = a.s.offsets[w.expert] + w.tok0;
     v.W = nullptr;
     v.lut = v.bd->lut[v.q];
+    v.gemv = a.T < kPrefillMinT && w.ntok <= min(a.gemv_max, kGemvMaxTok);
   } else {
     v.routed = false;
+    v.gemv = false;
     v.bd = nullptr;
     v.q = 0;
     v.N = (PHASE == 1) ? 2 * a.Is : a.H;
@@ -190,8 +206,9 @@ struct LutSched {
 };
 
 // Position in the slab ring, replayed identically by every role: chunk c (all items, in
-// order) takes q slabs (routed) or 16 slabs starting at an even slab (dense; one padding
-// slab when needed, so that no 4 KB piece wraps).  n = slabs consumed, padding included.
+// order) takes q consecutive slabs (routed; the ring's tail is skipped when they would wrap,
+// so that the dequantising warps address the planes from one base) or 16 slabs starting at
+// an even slab (dense; one padding slab when needed, so that no 4 KB piece wraps).  n = slabs consumed, padding included.
 // Routed and dense chunks also count separately (seq): their "weights landed" barriers are
 // separate sequences, because the dequantising warps wait only on routed chunks and skip
 // the dense ones.  A waiter that skipped fills of a barrier could otherwise run two phases
@@ -199,10 +216,14 @@ struct LutSched {
 struct RingPos {
   uint32_t slot = 0, c = 0, rc = 0, dc = 0;
   __device__ __forceinline__ uint32_t take(bool routed, int q, int S, uint32_t &n, uint32_t &seq) {
-    const uint32_t pad = routed ? 0u : (slot & 1u);
+    uint32_t pad = routed ? 0u : (slot & 1u);
     const uint32_t nd = routed ? (uint32_t)q : (uint32_t)kDenseSlabs;
     uint32_t base = slot + pad;
     if (base >= (uint32_t)S) base -= (uint32_t)S;
+    if (routed && base + nd > (uint32_t)S) {  // a routed chunk's planes never wrap: one base address
+      pad += (uint32_t)S - base;
+      base = 0;
+    }
     slot = base + nd;
     if (slot >= (uint32_t)S) slot -= (uint32_t)S;
     n = pad + nd;
@@ -220,16 +241,16 @@ __device__ __forceinline__ uint32_t ring_add(uint32_t a, uint32_t b, int S) {
   return r >= (uint32_t)S ? r - (uint32_t)S : r;
 }
 
-// Bounded wait on an mbarrier phase; false on expiry or when another warp gave up.
-// Waiting warps back off (and look at the abort flag) every 16 polls, so that they take
-// fewer issue slots from the warps they wait for.
+// Bounded wait on an mbarrier phase; false on expiry or when another warp gave up.  A
+// waiting thread sleeps in the barrier (suspend-time hint) rather than polling, so that it
+// takes no issue slots from the warps it waits for; the bound is on elapsed SM clock cycles.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
-  for (long i = 0; i < kSpinLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15) == 15) {
-      if (*abort_flag) return false;
-      __nanosleep(64);
-    }
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) break;
   }
   *abort_flag = 1;
   atomicExch(err, 1);
@@ -237,8 +258,22 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 // Wait that ignores the abort flag (used to drain what this thread issued); bounded.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
-  for (long i = 0; i < kSpinLimit && !mbar_try_wait(bar, parity); ++i) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs) && clock64() - t0 <= kWaitLimitCycles) {
   }
+}
+// Two waits taken by a whole warp; when both phases are already complete (the common case
+// on the MMA warp) the two checks overlap their latencies.
+__device__ __forceinline__ bool wait2_all(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, volatile int *abort_flag,
+                                          int *err) {
+  const bool r1 = mbar_try_wait(b1, p1);
+  const bool r2 = mbar_try_wait(b2, p2);
+  if (__all_sync(0xffffffffu, r1 && r2)) return true;
+  return __all_sync(0xffffffffu, wait_bar(b1, p1, abort_flag, err) && wait_bar(b2, p2, abort_flag, err));
+}
+// The same wait taken by a whole warp, with one outcome for every lane.
+__device__ __forceinline__ bool wait_bar_all(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *err) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err));
 }
 
 // Work items are claimed one at a time (atomic counter) by the weight producer and published,
@@ -260,7 +295,9 @@ struct ItemQueue {
 // items are exhausted (or on a timeout).
 __device__ __forceinline__ bool queue_read(const ItemQueue &qu, uint32_t k, unsigned lanes, volatile int *abort_flag,
                                            int *err, WorkItem &w, ItemView &v) {
-  if (!wait_bar(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1, abort_flag, err)) return false;
+  bool ok = wait_bar(qu.bars + 8 * (kIQF + k % kQueue), (k / kQueue) & 1, abort_flag, err);
+  if (lanes == 0xffffffffu) ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
   const QEntry &e = qu.slot[k % kQueue];
   const int it = e.it;
   if (it >= 0) {
@@ -296,9 +333,11 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
   const int n_items = a.s.n_items[PHASE - 1];
   RingPos pos;
   // room accounting (the same in every lane); the chunks in flight are kept across the
-  // lanes: lane i holds chunk c with c % kRing == i (its slab count and landed barrier)
+  // lanes: lane i holds chunk c with c % kRing == i (its slab count, landed barrier and the
+  // barrier that frees its slabs: for a routed chunk the dequantising warps' "read", for a
+  // dense one the MMAs' completion)
   uint32_t head = 0, released = 0, oldest = 0;
-  uint32_t my_n = 0, my_wf = 0, my_par = 0;
+  uint32_t my_n = 0, my_wf = 0, my_par = 0, my_rel = 0, my_rpar = 0;
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
     // claim the next work item only now that this one is needed, and publish it to the other
@@ -348,7 +387,9 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
       const uint32_t full = wf_bar(bars, v.routed, seq);
       // room: at most kRing chunks in flight and their slabs within the ring
       while (head + n > released + (uint32_t)S || c - oldest >= (uint32_t)kRing) {
-        if (lane == 0) ok = wait_bar(bars + 8 * (kWE + oldest % kRing), (oldest / kRing) & 1, abort_flag, a.s.err);
+        const uint32_t rb = __shfl_sync(0xffffffffu, my_rel, oldest % kRing);
+        const uint32_t rp = __shfl_sync(0xffffffffu, my_rpar, oldest % kRing);
+        if (lane == 0) ok = wait_bar(rb, rp, abort_flag, a.s.err);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         released += __shfl_sync(0xffffffffu, my_n, oldest % kRing);
@@ -359,6 +400,8 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
         my_n = n;
         my_wf = full;
         my_par = (seq / kRing) & 1;
+        my_rel = bars + 8 * ((v.routed ? kRD : kWE) + seq % kRing);
+        my_rpar = (seq / kRing) & 1;
       }
       head += n;
       if (lane == 0) mbar_arrive_expect_tx(full, tx);
@@ -411,12 +454,31 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
                             const ItemQueue &qu, volatile int *abort_flag) {
   using T_ = Tiling<TOK>;
   const int lane = threadIdx.x & 31;
-  uint32_t b_seq = 0;
+  const uint32_t gx = smem_u32(sm) + (uint32_t)L.gx_off;
+  uint32_t b_seq = 0, a_seq = 0, gx_seq[kGxSlots] = {0u, 0u, 0u, 0u};
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
     WorkItem w;
     ItemView v;
     if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
+    if (v.gemv) {  // one 8-row box of 128 columns per chunk into its stream's GEMV slot
+      const TmaDesc *map = PHASE == 1 ? &bm.gemv.xs : &bm.gemv.h_routed;
+      for (int kc = w.kc0; kc < w.kc1; ++kc) {
+        const uint32_t gs = a_seq++ % kDqStreams;
+        if (lane == 0) {
+          ok = wait_bar(bars + 8 * (kGXE + gs), (gx_seq[gs] & 1) ^ 1, abort_flag, a.s.err);
+          if (ok) {
+            mbar_arrive_expect_tx(bars + 8 * (kGXF + gs), (uint32_t)kGxBytes);
+            tma_load_2d(gx + gs * kGxBytes, map, kc * kChunkCols, v.row0, bars + 8 * (kGXF + gs));
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        ++gx_seq[gs];
+      }
+      continue;
+    }
+    if (v.routed) a_seq += (uint32_t)(w.kc1 - w.kc0);
     const ActMaps &mm = T_::kBoxRows == 16 ? bm.rows16 : bm.rows128;
     const TmaDesc *map = PHASE == 1 ? (v.routed ? &mm.xs : &mm.xh) : (v.routed ? &mm.h_routed : &mm.h_shared);
     const int rows = (v.npad + T_::kBoxRows - 1) / T_::kBoxRows * T_::kBoxRows;  // rows loaded per stage
@@ -439,9 +501,12 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
   }
   // the last fills (the only ones whose barrier phase may still be open) land before exit
   __syncwarp();
-  if (lane == 0)
+  if (lane == 0) {
     for (uint32_t i = b_seq > (uint32_t)T_::kBSlots ? b_seq - T_::kBSlots : 0u; i < b_seq; ++i)
       drain_bar(bars + 8 * (kBF + i % T_::kBSlots), (i / T_::kBSlots) & 1);
+    for (int j = 0; j < kGxSlots; ++j)
+      if (gx_seq[j] > 0) drain_bar(bars + 8 * (kGXF + j), (gx_seq[j] - 1) & 1);
+  }
 }
 
 // Descriptor of K-step 0 of an activation stage: 128-byte swizzled rows in 8-row atoms of
@@ -449,101 +514,168 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
 // inside shared memory).
 __device__ __forceinline__ uint64_t b_desc(uint32_t stage) { return smem_desc_sw128(stage, 1024); }
 
+// The MMA warp.  Every lane runs the loop on the same (warp-uniform) values and one elected
+// lane issues the tensor-core instructions: an MMA issued this way costs about 75 cycles
+// (M = 128, K = 16, any N up to 128) against about 108 from a lane that runs the loop alone,
+// as its operands stay in the uniform datapath.  For a GEMV item the warp only grants the
+// accumulator buffer to the dequantising warps and returns each chunk's slabs to the weight
+// producer once those warps have read them.
 template <int PHASE, int TOK>
 __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                            const ItemQueue &qu, volatile int *abort_flag) {
   using T_ = Tiling<TOK>;
-  if ((threadIdx.x & 31) != 0) return;
   const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
   const int S = L.slabs;
   RingPos pos;
-  uint32_t b_seq = 0, a_seq = 0, item_seq = 0;
+  uint32_t a_seq = 0, item_seq = 0, m_seq = 0, gi_seq = 0;
+  // next B slot and the phase parities of the B slot and A buffer barriers the next chunk waits on
+  uint32_t b_slot = 0, b_par = 0, a_par = 0;
+  // K-step 0 of B stage 0, and the step between stages (stages are equally spaced when they all
+  // sit below the LUT slots, as in the decode tiling; the prefill tiling computes each one)
+  const uint64_t bdesc0 = b_desc(b_stage<TOK>(sm, L, 0));
+  const uint64_t bstep = (uint64_t)(L.b_bytes >> 4);
   bool ok = true;
   for (uint32_t k = 0; ok; ++k) {
     WorkItem w;
     ItemView v;
-    if (!queue_read(qu, k, 1u, abort_flag, a.s.err, w, v)) break;
-    const uint32_t idesc = idesc_f16_f32(128, v.npad);
+    if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
     const int acs = item_seq % 2;
-    ok = wait_bar(bars + 8 * (kAE + acs), ((item_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
+    ok = wait_bar_all(bars + 8 * (kAE + acs), ((item_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
     if (!ok) break;
+    ++item_seq;
+    if (v.gemv) {  // computed by the dequantising warps: grant them the accumulator buffer
+      if (elect_one()) mbar_arrive(bars + 8 * (kGAG + gi_seq % 2));
+      __syncwarp();
+      ++gi_seq;
+      for (int kc = w.kc0; kc < w.kc1 && ok; ++kc) {
+        uint32_t n, seq;
+        pos.take(true, v.q, S, n, seq);
+        const int ts = a_seq & (T_::kAStages - 1);
+        ok = wait_bar_all(bars + 8 * (kTAF + ts), a_par, abort_flag, a.s.err);
+        if (((++a_seq) & (T_::kAStages - 1)) == 0) a_par ^= 1u;
+        if (ok && elect_one()) tc_commit(bars + 8 * (kTAE + ts));  // after the MMAs issued so far
+        __syncwarp();
+      }
+      continue;
+    }
+    const uint32_t idesc = idesc_f16_f32(128, v.npad);
     tc_fence_after();
     const uint32_t d = tmem + acs * T_::kAccCols;
     bool first = true;
     for (int kc = w.kc0; kc < w.kc1; ++kc) {
-      const uint32_t c = pos.c;
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
-      const int ts = a_seq % T_::kAStages;
-      if (v.routed)
-        ok = wait_bar(bars + 8 * (kTAF + ts), (a_seq / T_::kAStages) & 1, abort_flag, a.s.err);
-      else
-        ok = wait_bar(wf_bar(bars, false, seq), (seq / kRing) & 1, abort_flag, a.s.err);
-      if (!ok) break;
-      const int bs = b_seq % T_::kBSlots;
-      ok = wait_bar(bars + 8 * (kBF + bs), (b_seq / T_::kBSlots) & 1, abort_flag, a.s.err);
+      const int ts = a_seq & (T_::kAStages - 1);
+      const int bs = b_slot;
+      // the chunk's A operand (or dense weights) and its B slot; both checks are issued together
+      ok = v.routed ? wait2_all(bars + 8 * (kTAF + ts), a_par, bars + 8 * (kBF + bs), b_par, abort_flag, a.s.err)
+                    : wait2_all(wf_bar(bars, false, seq), (seq / kRing) & 1, bars + 8 * (kBF + bs), b_par, abort_flag,
+                                a.s.err);
       if (!ok) break;
       tc_fence_after();
-      // this thread shares its scheduler with dequantising warps: keep the per-MMA work to an
-      // add or two on values computed once per stage
       const uint32_t acc0 = first ? 0u : 1u;
-      if (v.routed) {
-        const uint32_t at = tmem + T_::kAColBase + ts * kACols;
+      if (elect_one()) {
+        if (v.routed) {
+          const uint32_t at = tmem + T_::kAColBase + ts * kACols;
 #pragma unroll
-        for (int piece = 0; piece < T_::kBPieces; ++piece) {
-          const uint64_t bd = b_desc(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece));
+          for (int piece = 0; piece < T_::kBPieces; ++piece) {
+            uint64_t bd;
+            if constexpr (T_::kBLowStages == T_::kBStages)
+              bd = bdesc0 + (uint64_t)(bs * T_::kBPieces + piece) * bstep;
+            else
+              bd = b_desc(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece));
 #pragma unroll
-          for (int t = 0; t < T_::kBSteps; ++t)
-            tc_mma_f16_ta(d, at + 8 * (piece * T_::kBSteps + t), bd + t * T_::kDescStep, idesc,
-                          piece + t == 0 ? acc0 : 1u);
-        }
-      } else {
-#pragma unroll
-        for (int piece = 0; piece < T_::kBPieces; ++piece) {
-          const uint64_t bd = b_desc(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece));
-#pragma unroll
-          for (int t = 0; t < T_::kBSteps; ++t) {
-            const int kt = piece * T_::kBSteps + t;
-            tc_mma_f16(d, smem_desc(ring + ring_add(base, 2 * kt, S) * kSlab, 128, 256), bd + t * T_::kDescStep, idesc,
-                       kt == 0 ? acc0 : 1u);
+            for (int t = 0; t < T_::kBSteps; ++t)
+              tc_mma_f16_ta(d, at + 8 * (piece * T_::kBSteps + t), bd + t * T_::kDescStep, idesc,
+                            piece + t == 0 ? acc0 : 1u);
           }
+          tc_commit(bars + 8 * (kBE + bs));
+          tc_commit(bars + 8 * (kTAE + ts));
+        } else {
+#pragma unroll
+          for (int piece = 0; piece < T_::kBPieces; ++piece) {
+            const uint64_t bd = b_desc(b_stage<TOK>(sm, L, bs * T_::kBPieces + piece));
+#pragma unroll
+            for (int t = 0; t < T_::kBSteps; ++t) {
+              const int kt = piece * T_::kBSteps + t;
+              tc_mma_f16(d, smem_desc(ring + ring_add(base, 2 * kt, S) * kSlab, 128, 256), bd + t * T_::kDescStep,
+                         idesc, kt == 0 ? acc0 : 1u);
+            }
+          }
+          tc_commit(bars + 8 * (kBE + bs));
+          tc_commit(bars + 8 * (kWE + seq % kRing));  // the dense chunk's slabs
         }
       }
-      tc_commit(bars + 8 * (kBE + bs));
-      ++b_seq;
-      if (v.routed) {
-        tc_commit(bars + 8 * (kTAE + ts));
-        ++a_seq;
+      __syncwarp();
+      if (++b_slot == T_::kBSlots) {
+        b_slot = 0;
+        b_par ^= 1u;
       }
+      if (v.routed && ((++a_seq & (T_::kAStages - 1)) == 0)) a_par ^= 1u;
       first = false;
-      tc_commit(bars + 8 * (kWE + c % kRing));  // the chunk's slabs
     }
     if (!ok) break;
-    tc_commit(bars + 8 * (kAF + acs));
-    ++item_seq;
+    if (elect_one()) tc_commit(bars + 8 * (kAF + m_seq % 2));
+    __syncwarp();
+    ++m_seq;
   }
   // every MMA issued must complete before tensor memory is freed
-  tc_commit(bars + 8 * kDrain);
+  if (elect_one()) tc_commit(bars + 8 * kDrain);
+  __syncwarp();
   drain_bar(bars + 8 * kDrain, 0);
 }
 
-// A dequantising warp's tensor-memory store of A buffer ts: completed (tcgen05.st reads its
-// source registers asynchronously, so they may be rewritten only after this), made visible
-// and signalled to the MMA thread at once.  Deferring the signal to the next chunk, to hide
-// the store's latency, delays the MMAs by a chunk and was measured slower.
-__device__ __forceinline__ void signal_store(uint32_t bars, int ts, int lane) {
-  tmem_wait_st();
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bars + 8 * (kTAF + ts));
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2 *>(&u); }
+
+// Centroids of one row and one 32-column group of a routed chunk from its q plane words.
+template <int Q>
+__device__ __forceinline__ void dq_words(const uint32_t (&W)[8], const LutRegs &Lr, const LutLane &lu,
+                                         uint32_t (&v16)[16]) {
+  if constexpr (Q <= kRegLutMaxQ) {
+    uint32_t S4[4];
+    codes_nib<Q>(W, S4);
+    dq_nib<Q>(S4, Lr, v16);
+  } else {
+    uint32_t Y[8];
+    codes_byte<Q>(W, Y, lu.top);
+    dq_byte<Q>(Y, lu, v16);
+  }
 }
 
-// One routed item for a dequantising thread: row r of the tile, columns [32 cg, 32 cg + 32)
-// of every chunk.
+// The dequantising warps form kDqStreams chunk streams per tensor-memory lane quarter: warp
+// w serves lane quarter w & 3 and stream w >> 2, and stream j takes the routed chunks whose
+// sequence number (over all routed chunks of the launch) is j modulo kDqStreams, all 128
+// columns of the quarter's 32 rows.  The four warps of an SM sub-partition (which all serve
+// the same lane quarter) thus work on different chunks, and their memory and barrier
+// latencies do not line up.  Every barrier slot a warp waits on belongs to its own stream
+// (the rings of "routed chunk landed", "slabs read" and A-buffer barriers have lengths that
+// are multiples of kDqStreams, and each stream has its own GEMV activation slot), so a warp
+// sees every phase of the barriers it waits on.
+//
+// One routed item for a dequantising warp.  The warp reads a chunk's plane words group by
+// group; after the last group's words it tells the weight producer that it is done with the
+// chunk's slabs (the barrier completes when the stream's four warps have), so that a routed
+// chunk does not hold ring space while the tensor cores work on it.
+// Tensor-core items: the four 32-column groups go to the chunk's A buffer one after the
+// other, from two register sets used in turn (a set is rewritten only after the store that
+// read it has completed, and that store had a group's arithmetic to complete in).  GEMV items
+// (decode tiling, at most kGemvMaxTok tokens): the same centroids multiplied on the CUDA cores
+// by the item's activation rows (one 8-row box of 128 columns per chunk in the stream's GEMV
+// slot, read by the whole warp at one address per load), each 32-column group summed in
+// packed fp16 pairs (16 products per half) and then added in fp32 to the thread's running
+// dot products; at the end of the item the stream's sums go to tensor memory (columns
+// 8 stream + t of the item's accumulator buffer), where the epilogue adds the streams in
+// order.  Either way the warp then signals the chunk's A-buffer barrier.
 template <int PHASE, int TOK, int Q>
 __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, const TcLayout &L,
-                        uint32_t bars, uint32_t tmem, uint32_t lut_slot, int quarter, int cg, RingPos &pos,
-                        uint32_t &a_seq, volatile int *abort_flag) {
+                        uint32_t bars, uint32_t tmem, uint32_t lut_slot, int quarter, int stream, RingPos &pos,
+                        uint32_t &a_seq, uint32_t &gx_seq, uint32_t &gi_seq, uint32_t acs, volatile int *abort_flag) {
+  using T_ = Tiling<TOK>;
   const int lane = threadIdx.x & 31;
   const int r = 32 * quarter + lane;
   const bool rv = r < v.nr;
@@ -555,37 +687,97 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
     lut_pairs_smem<Q>(lu, P);
     lut_regs(P, Lr);
   }
-  const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off + (uint32_t)(cg * v.nr + r) * 4;
+  const uint32_t cg_off = (uint32_t)v.nr * 4;  // column-group stride inside a slab
+  const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off + (uint32_t)r * 4;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-  uint32_t v16[16];
+  const bool gemv = TOK == kTokChunk && v.gemv;
+  const uint32_t gx = smem_u32(sm) + (uint32_t)L.gx_off + (uint32_t)stream * kGxBytes;
+  float acc[kGemvMaxTok];
+#pragma unroll
+  for (int t = 0; t < kGemvMaxTok; ++t) acc[t] = 0.f;
+  uint32_t va[16], vb[16];
   for (int kc = w.kc0; kc < w.kc1; ++kc) {
     uint32_t n, seq;
-    uint32_t sl = pos.take(true, Q, S, n, seq);
-    const int ts = a_seq % Tiling<TOK>::kAStages;
-    if (!wait_bar(wf_bar(bars, true, seq), (seq / kRing) & 1, abort_flag, a.s.err)) return false;
+    const uint32_t sl = pos.take(true, Q, S, n, seq);
+    const uint32_t as = a_seq++;
+    if ((int)(as % kDqStreams) != stream) continue;
+    const int ts = as % T_::kAStages;
+    if (!wait_bar_all(wf_bar(bars, true, seq), (seq / kRing) & 1, abort_flag, a.s.err)) return false;
+    const uint32_t src = ring + sl * kSlab;
     uint32_t W[8];
+    if (!gemv) {
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      W[p] = 0u;
-      if (p < Q) {
-        if (rv) W[p] = lds32(ring + sl * kSlab);
-        sl = (sl + 1 == (uint32_t)S) ? 0u : sl + 1;
+      for (int p = 0; p < 8; ++p) W[p] = (p < Q && rv) ? lds32(src + p * kSlab) : 0u;
+      dq_words<Q>(W, Lr, lu, va);
+      if (!wait_bar_all(bars + 8 * (kTAE + ts), ((as / T_::kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
+      tc_fence_after();
+      const uint32_t at = tmem + lane_base + T_::kAColBase + ts * kACols;
+      tmem_st16(at, va);
+#pragma unroll
+      for (int j = 1; j < 4; ++j) {
+        uint32_t(&vv)[16] = (j & 1) ? vb : va;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) W[p] = (p < Q && rv) ? lds32(src + j * cg_off + p * kSlab) : 0u;
+        if (j == 3) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + 8 * (kRD + seq % kRing));  // ordered after the reads
+        }
+        dq_words<Q>(W, Lr, lu, vv);
+        tmem_wait_st();
+        tmem_st16(at + 16 * j, vv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bars + 8 * (kTAF + ts));
+    } else {
+      if (!wait_bar_all(bars + 8 * (kGXF + stream), gx_seq & 1, abort_flag, a.s.err)) return false;
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int p = 0; p < 8; ++p) W[p] = (p < Q && rv) ? lds32(src + j * cg_off + p * kSlab) : 0u;
+        if (j == 3) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + 8 * (kRD + seq % kRing));
+        }
+        dq_words<Q>(W, Lr, lu, va);
+#pragma unroll
+        for (int t = 0; t < kGemvMaxTok; ++t) {
+          if (t < v.ntok) {
+            __half2 h = __float2half2_rn(0.f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint4 x4 = lds128(gx + t * (kChunkCols * 2) + 64 * j + 16 * i);
+              h = __hfma2(as_h2(va[4 * i + 0]), as_h2(x4.x), h);
+              h = __hfma2(as_h2(va[4 * i + 1]), as_h2(x4.y), h);
+              h = __hfma2(as_h2(va[4 * i + 2]), as_h2(x4.z), h);
+              h = __hfma2(as_h2(va[4 * i + 3]), as_h2(x4.w), h);
+            }
+            acc[t] += __low2float(h) + __high2float(h);
+          }
+        }
+      }
+      ++gx_seq;
+      if (!wait_bar_all(bars + 8 * (kTAE + ts), ((as / T_::kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bars + 8 * (kGXE + stream));
+        mbar_arrive(bars + 8 * (kTAF + ts));
       }
     }
-    if constexpr (Q <= kRegLutMaxQ) {
-      uint32_t S4[4];
-      codes_nib<Q>(W, S4);
-      dq_nib<Q>(S4, Lr, v16);
-    } else {
-      uint32_t Y[8];
-      codes_byte<Q>(W, Y);
-      dq_byte<Q>(Y, lu, v16);
-    }
-    if (!wait_bar(bars + 8 * (kTAE + ts), ((a_seq / Tiling<TOK>::kAStages) & 1) ^ 1, abort_flag, a.s.err)) return false;
+  }
+  if (gemv) {  // the accumulator buffer is this item's once the MMA warp has granted it
+    if (!wait_bar_all(bars + 8 * (kGAG + gi_seq % 2), (gi_seq / 2) & 1, abort_flag, a.s.err)) return false;
     tc_fence_after();
-    tmem_st16(tmem + lane_base + Tiling<TOK>::kAColBase + ts * kACols + 16 * cg, v16);
-    signal_store(bars, ts, lane);
-    ++a_seq;
+    uint32_t r8[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) r8[t] = t < kGemvMaxTok ? __float_as_uint(acc[t < kGemvMaxTok ? t : 0]) : 0u;
+    tmem_st8(tmem + lane_base + acs * T_::kAccCols + 8 * stream, r8);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (kAFG + gi_seq % 2));
+    ++gi_seq;
   }
   return true;
 }
@@ -594,15 +786,16 @@ template <int PHASE, int TOK>
 __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                             const ItemQueue &qu, volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quarter = warp & 3, cg = warp >> 2;
+  const int quarter = warp & 3, stream = warp >> 2;
   const uint32_t lut0 = lut_base(sm, L);
   RingPos pos;
-  uint32_t a_seq = 0;
+  uint32_t a_seq = 0, gx_seq = 0, gi_seq = 0, item_seq = 0;
   LutSched ls;
   for (uint32_t k = 0;; ++k) {
     WorkItem w;
     ItemView v;
     if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
+    const uint32_t acs = item_seq++ % 2;
     if (!v.routed) {  // dense chunks: only the ring position moves
       for (int kc = w.kc0; kc < w.kc1; ++kc) {
         uint32_t n, seq;
@@ -612,14 +805,15 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     }
     bool both;
     const int slot = ls.next(v.q, both);
-    if (!wait_bar(bars + 8 * (kLF + slot), ls.fills[slot] & 1, abort_flag, a.s.err)) return;
+    if (!wait_bar_all(bars + 8 * (kLF + slot), ls.fills[slot] & 1, abort_flag, a.s.err)) return;
     ++ls.fills[slot];
     const uint32_t lut_slot = lut0 + slot * kLutSlot;
     bool ok;
     switch (v.q) {
-#define PW_DQ_CASE(QQ)                                                                                       \
-  case QQ:                                                                                                   \
-    ok = dq_item<PHASE, TOK, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, abort_flag);   \
+#define PW_DQ_CASE(QQ)                                                                                          \
+  case QQ:                                                                                                      \
+    ok = dq_item<PHASE, TOK, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, stream, pos, a_seq, gx_seq, gi_seq, acs, \
+                                 abort_flag);                                                                  \
     break;
       PW_DQ_CASE(1)
       PW_DQ_CASE(2)
@@ -629,7 +823,8 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       PW_DQ_CASE(6)
       PW_DQ_CASE(7)
       default:
-        ok = dq_item<PHASE, TOK, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, cg, pos, a_seq, abort_flag);
+        ok = dq_item<PHASE, TOK, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, stream, pos, a_seq, gx_seq, gi_seq, acs,
+                                    abort_flag);
         break;
 #undef PW_DQ_CASE
     }
@@ -648,22 +843,44 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
                          volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
-  uint32_t item_seq = 0;
+  uint32_t item_seq = 0, m_seq = 0, gi_seq = 0;
   for (uint32_t k = 0;; ++k) {
     WorkItem w;
     ItemView v;
     if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
     const int acs = item_seq % 2;
-    if (!wait_bar(bars + 8 * (kAF + acs), (item_seq / 2) & 1, abort_flag, a.s.err)) return;
+    const bool gemv = TOK == kTokChunk && v.gemv;
+    bool ok;
+    if (gemv) {
+      ok = wait_bar_all(bars + 8 * (kAFG + gi_seq % 2), (gi_seq / 2) & 1, abort_flag, a.s.err);
+      ++gi_seq;
+    } else {
+      ok = wait_bar_all(bars + 8 * (kAF + m_seq % 2), (m_seq / 2) & 1, abort_flag, a.s.err);
+      ++m_seq;
+    }
+    if (!ok) return;
     tc_fence_after();
     const int row = 32 * quarter + lane;  // tile row = tensor-memory lane
     const int R = w.tile * kCtaRows + row;
     const bool empty = w.kc1 <= w.kc0;     // nothing accumulated (an empty split part)
     const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * Tiling<TOK>::kAccCols;
-    for (int c = 0; c < v.npad; c += 8) {
+    for (int c = 0; c < (gemv ? 8 : v.npad); c += 8) {
       uint32_t r8[8];
-      tmem_ld8(taddr + c, r8);
-      tmem_wait_ld();
+      if (gemv) {  // the column-group sets' dot products, added in order
+        float f8[8];
+#pragma unroll
+        for (int g = 0; g < kDqStreams; ++g) {
+          tmem_ld8(taddr + 8 * g, r8);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) f8[i] = g == 0 ? __uint_as_float(r8[i]) : f8[i] + __uint_as_float(r8[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) r8[i] = __float_as_uint(f8[i]);
+      } else {
+        tmem_ld8(taddr + c, r8);
+        tmem_wait_ld();
+      }
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const float acc = empty ? 0.f : __uint_as_float(r8[i]);
@@ -705,7 +922,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
     const uint32_t base = smem_u32(sm);
     constexpr int low = T_::kBLowStages;
     L.b_off = 0;
-    L.bar_off = low * L.b_bytes;
+    L.gx_off = low * L.b_bytes;
+    L.bar_off = L.gx_off + kGxSlots * kGxBytes;
     L.lut_off = (int)(kLutAddr - base);
     L.b_hi = (int)(kRingAddr - base);
     L.ring_off = L.b_hi + (T_::kBStages - low) * L.b_bytes;
@@ -720,12 +938,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   const uint32_t bars = smem_u32(sm + L.bar_off);
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRing; ++i) {
+      mbar_init(bars + 8 * (kRD + i), kDq / kDqStreams);  // the chunk's stream has read its slabs
       mbar_init(bars + 8 * (kWFR + i), 1);
       mbar_init(bars + 8 * (kWFD + i), 1);
       mbar_init(bars + 8 * (kWE + i), 1);
     }
     for (int i = 0; i < T_::kAStages; ++i) {
-      mbar_init(bars + 8 * (kTAF + i), kDq);
+      mbar_init(bars + 8 * (kTAF + i), kDq / kDqStreams);  // the chunk's stream, one warp per lane quarter
       mbar_init(bars + 8 * (kTAE + i), 1);
     }
     for (int i = 0; i < T_::kBSlots; ++i) {
@@ -742,6 +961,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(bars + 8 * (kIQF + i), 1);
       mbar_init(bars + 8 * (kIQE + i), kQueueReaders);
+    }
+    for (int i = 0; i < kGxSlots; ++i) {
+      mbar_init(bars + 8 * (kGXF + i), 1);    // lane 0 of the activation producer
+      mbar_init(bars + 8 * (kGXE + i), kDq / kDqStreams);  // the stream's warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bars + 8 * (kGAG + i), 1);    // the MMA warp
+      mbar_init(bars + 8 * (kAFG + i), kDq);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -788,7 +1015,8 @@ static int launch_tiled(const FwdArgs &a, int phase, cudaStream_t st) {
   if (!a.bmaps) return (int)cudaErrorInvalidValue;
   const BMaps bm = *a.bmaps;
   L.smem = kSmemLimit;
-  if (T_::kBLowStages * L.b_bytes + kNumBars * 8 + 2048 > (int)kLutAddr) return (int)cudaErrorInvalidConfiguration;
+  if (T_::kBLowStages * L.b_bytes + kGxSlots * kGxBytes + kNumBars * 8 + 2048 > (int)kLutAddr)
+    return (int)cudaErrorInvalidConfiguration;
   const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
   const int grid = min(max_items, a.sm_count);
   if (phase == 1) {

@@ -247,8 +247,15 @@ struct ActMaps {
   TmaDesc h_routed;  // [Tm*K][I] (routed down)
   TmaDesc h_shared;  // [Tm][Is] (shared down)
 };
+// Activation rows of the CUDA-core (GEMV) work items: boxes of 128 columns by 8 rows, no
+// swizzle (row t of a box at byte 256 t), rows past the end read as zeros.
+struct GemvMaps {
+  TmaDesc xs;        // [Tm*K][H] routed gate_up input in slot order
+  TmaDesc h_routed;  // [Tm*K][I] routed down input
+};
 struct BMaps {
   ActMaps rows16, rows128;
+  GemvMaps gemv;
 };
 
 struct Scratch {
@@ -299,8 +306,11 @@ struct FwdArgs {
   int *ids_out;           // optional
   float *w_out;           // optional
   int sm_count;
+  int gemv_max;           // routed work items of at most this many tokens run on the CUDA cores (decode tiling)
   const BMaps *bmaps;     // host copy of the activation tensor maps
 };
+constexpr int kGemvMaxTokens = 8;      // largest GEMV item
+constexpr int kGemvDefaultTokens = 4;  // default threshold of a context
 
 // ev: null, or five timing events recorded before, between and after the four kernels
 int launch_forward(const FwdArgs &a, void *stream, void *const *ev);

@@ -304,7 +304,7 @@ __device__ void unpack_group(const BlockDev &bd, int ct, int kc, int cg, int r, 
     for (int c = 0; c < 32; ++c) codes[c] = code_nib<Q>(S, c);
   } else {
     uint32_t Y[8];
-    codes_byte<Q>(W, Y);
+    codes_byte<Q>(W, Y, lu.top);
     dq_byte<Q>(Y, lu, v);
 #pragma unroll
     for (int c = 0; c < 32; ++c) codes[c] = code_byte<Q>(Y, c);

@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gemv-tokens", type=int, default=None,
+                    help="routed work items of at most this many tokens run on the CUDA cores (default: the library's)")
     ap.add_argument("--paging", action="store_true",
                     help="dynamic paging run: a free-KV-block trace drives the planner, offload and reload every step")
     return ap.parse_args()
@@ -345,6 +347,8 @@ def run_ours(args, shape, L, T):
     t_setup = time.time() - t_setup
     stream = torch.cuda.Stream()
     pw.pw_set_stream(ctx, stream)
+    if args.gemv_tokens is not None:
+        pw.pw_set_gemv_tokens(ctx, args.gemv_tokens)
     x0 = torch.from_numpy(syn.gen_tokens_np(shape, args.seed, 0, T).view(np.int16)).cuda()
     xw = torch.empty_like(x0)
     torch.cuda.synchronize()

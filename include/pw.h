@@ -173,6 +173,17 @@ pw_status pw_routing_stats(pw_ctx *ctx, int layer, double *count, double *weight
  * phi.  Output host double [E][3].  Waits for the compute stream. */
 pw_status pw_routing_features(pw_ctx *ctx, int layer, double *phi, int reset);
 
+/* Decode kernel choice (the benchmark spec (d): CUDA-core bit-plane GEMV for the memory-bound decode
+ * regime, tensor cores only where the path is a dense contraction; the paper's fused kernel,
+ * Sec. 3.3, has one path).  At decode batch sizes (T < 512) a routed work item -- a 128-row
+ * tile of one expert's block times the tokens routed to that expert -- with at most
+ * `max_tokens` tokens is computed on the CUDA cores (packed fp16 products of the decoded
+ * centroids and the activations, summed in fp32 per 32 columns); larger items go to the
+ * tensor cores.  0 sends every item to the tensor cores.  Default 4; valid 0..8, else
+ * PW_ERR_INVALID.  Takes effect at the next forward launch (captured stack graphs are
+ * dropped). */
+pw_status pw_set_gemv_tokens(pw_ctx *ctx, int max_tokens);
+
 /* Tracing: while on, every forward records five CUDA timing events per layer, before,
  * between and after its four kernels (router, gate_up, down, combine), on the launch
  * stream; stack graphs captured while on contain the event records.  The events are

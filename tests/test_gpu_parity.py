@@ -339,3 +339,42 @@ def test_stack_graph_replay_equals_layer_by_layer():
         assert np.array_equal(yh.view(np.int16), xa.cpu().numpy())
     finally:
         pw.pw_destroy(ctx)
+
+
+# ---------------------------------------------------------------- the two decode kernels
+@pytest.mark.parametrize("gemv", [0, 8])
+@pytest.mark.parametrize("name,T", [("tiny", 8), ("odd", 6), ("qwen", 16), ("qwen", 64), ("g128", 32),
+                                    ("mixtral", 8), ("longdown", 24)])
+def test_decode_item_paths(name, T, gemv):
+    """Routed items on the tensor cores only (threshold 0) and, with threshold 8, every item of
+    up to 8 tokens on the CUDA cores: both against the oracle and bit-for-bit repeatable."""
+    shape = {"odd": ODD, "longdown": LONGDOWN}.get(name) or syn.SHAPES[name]
+    small = name in ("tiny", "odd", "longdown")
+    data = LayerData(shape, 6, 0, T, real=range(shape.E) if small else None, tiny=(name == "tiny"))
+    ctx = make_ctx(pw, shape, L=1, max_tokens=T)
+    try:
+        data.load(pw, ctx)
+        pw.pw_set_gemv_tokens(ctx, gemv)
+        y, ids, w = run_layer(ctx, data, T)
+        y_ref, ids_ref, w_ref = data.oracle()
+        assert np.array_equal(ids, ids_ref)
+        assert np.allclose(w, w_ref, rtol=1e-5, atol=1e-7)
+        assert_close(y, y_ref, f"{name} T={T} gemv<={gemv}")
+        again, _, _ = run_layer(ctx, data, T)
+        assert np.array_equal(y, again)
+    finally:
+        pw.pw_destroy(ctx)
+
+
+def test_gemv_threshold_is_checked():
+    shape = syn.SHAPES["tiny"]
+    ctx = make_ctx(pw, shape, L=1, max_tokens=8)
+    try:
+        for bad in (-1, 9):
+            with pytest.raises(pw.PwError) as ei:
+                pw.pw_set_gemv_tokens(ctx, bad)
+            assert ei.value.status == pw.PW_ERR_INVALID
+        pw.pw_set_gemv_tokens(ctx, 0)
+        pw.pw_set_gemv_tokens(ctx, 8)
+    finally:
+        pw.pw_destroy(ctx)
