@@ -385,15 +385,30 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
       uint32_t n, seq;
       const uint32_t base = pos.take(v.routed, v.q, S, n, seq);
       const uint32_t full = wf_bar(bars, v.routed, seq);
-      // room: at most kRing chunks in flight and their slabs within the ring
+      // room: at most kRing chunks in flight and their slabs within the ring.  Every lane
+      // checks its own chunk in flight at once, and the run of released chunks from the oldest
+      // on is retired in one step; only when the oldest is still in use does lane 0 wait.
       while (head + n > released + (uint32_t)S || c - oldest >= (uint32_t)kRing) {
-        const uint32_t rb = __shfl_sync(0xffffffffu, my_rel, oldest % kRing);
-        const uint32_t rp = __shfl_sync(0xffffffffu, my_rpar, oldest % kRing);
-        if (lane == 0) ok = wait_bar(rb, rp, abort_flag, a.s.err);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        released += __shfl_sync(0xffffffffu, my_n, oldest % kRing);
-        ++oldest;
+        const uint32_t age = ((uint32_t)lane - oldest) % kRing;  // lane < kRing holds chunk oldest + age
+        const bool mine = lane < kRing && oldest + age < c;
+        const bool done = mine && mbar_try_wait(my_rel, my_rpar);
+        uint32_t run = (mine && !done) ? age : c - oldest;  // released chunks from the oldest on
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) run = min(run, __shfl_xor_sync(0xffffffffu, run, off));
+        uint32_t freed = (mine && age < run) ? my_n : 0u;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) freed += __shfl_xor_sync(0xffffffffu, freed, off);
+        released += freed;
+        oldest += run;
+        if (run == 0) {  // the oldest chunk is still being read: wait for it
+          const uint32_t rb = __shfl_sync(0xffffffffu, my_rel, oldest % kRing);
+          const uint32_t rp = __shfl_sync(0xffffffffu, my_rpar, oldest % kRing);
+          if (lane == 0) ok = wait_bar(rb, rp, abort_flag, a.s.err);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          released += __shfl_sync(0xffffffffu, my_n, oldest % kRing);
+          ++oldest;
+        }
       }
       if (!ok) break;
       if (lane == (int)(c % kRing)) {
@@ -404,9 +419,10 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
         my_rpar = (seq / kRing) & 1;
       }
       head += n;
-      if (lane == 0) mbar_arrive_expect_tx(full, tx);
-      __syncwarp();
+      // the copies first: a barrier's transaction count may run below zero until the expected
+      // bytes are announced, and the phase cannot complete before that arrival
       if (copies) bulk_g2s(ring + ring_add(base, lane_slab, S) * kSlab, src, cbytes, full);
+      if (lane == 0) mbar_arrive_expect_tx(full, tx);
       src += src_step;
     }
   }

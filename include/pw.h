@@ -179,8 +179,8 @@ pw_status pw_routing_features(pw_ctx *ctx, int layer, double *phi, int reset);
  * tile of one expert's block times the tokens routed to that expert -- with at most
  * `max_tokens` tokens is computed on the CUDA cores (packed fp16 products of the decoded
  * centroids and the activations, summed in fp32 per 32 columns); larger items go to the
- * tensor cores.  0 sends every item to the tensor cores.  Default 4; valid 0..8, else
- * PW_ERR_INVALID.  Takes effect at the next forward launch (captured stack graphs are
+ * tensor cores.  0 sends every item to the tensor cores.  Default 0 (on GB300 the
+ * tensor-core items measured faster at every decode size); valid 0..8, else PW_ERR_INVALID.  Takes effect at the next forward launch (captured stack graphs are
  * dropped). */
 pw_status pw_set_gemv_tokens(pw_ctx *ctx, int max_tokens);
 
