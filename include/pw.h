@@ -75,13 +75,23 @@ typedef struct {
 
 /* ---------------------------------------------------------------- lifetime */
 
-/* Create a context on desc->device.  Requires H % 16 == 0, I % 8 == 0, Is % 8 == 0,
+/* Create a context on desc->device.  The context holds the state the paper describes for one
+ * model: the per-block weight pages and the device weight page table of Sec. 3.1 ("Paged
+ * Weight Representation": committed bitwidth q_i, desired bitwidth d_i, per-page residency),
+ * the compute and side streams of Sec. 3.3 ("Asynchronous Page Movement"), and the forward
+ * scratch of the fused layer of Sec. 3.3.  The paper specifies no API; the call itself is this
+ * library's (the benchmark spec (b): a small C-ABI library).  Requires H % 16 == 0, I % 8 == 0, Is % 8 == 0,
  * K <= E <= 256, K <= 8.  Allocates the page table, scratch for max_tokens tokens and
  * the two streams (compute stream = a new non-blocking stream, side stream for page
  * copies).  Errors: PW_ERR_INVALID on bad shapes, PW_ERR_CUDA / PW_ERR_OOM otherwise. */
 pw_status pw_create(const pw_desc *desc, pw_ctx **out);
+/* Release everything the context owns (device pages, pinned host pages, scratch, streams it
+ * created); waits for its streams first.  NULL is ignored. */
 void pw_destroy(pw_ctx *ctx);
+/* Message of the last failing call on ctx (or of the calling thread when ctx is NULL); owned
+ * by the library, valid until the next call on the same context or thread. */
 const char *pw_last_error(const pw_ctx *ctx);
+/* Library version string (static storage). */
 const char *pw_version(void);
 
 /* Stream on which commits (pw_set_bits, pw_offload's lowering, pw_commit's raising) and
@@ -145,7 +155,9 @@ pw_status pw_moe_forward(pw_ctx *ctx, int layer, const void *x, int T, void *y,
 
 /* Wait for the compute stream and report whether a bounded wait inside an expert kernel
  * expired since the last check (PW_ERR_TIMEOUT; the outputs of that launch are invalid).
- * Also reports sticky CUDA errors. */
+ * Also reports sticky CUDA errors.  No counterpart in the paper: the fused kernel of
+ * Sec. 3.3 synchronises its warps on device barriers, and this library bounds every such
+ * wait and reports the ones that gave up here. */
 pw_status pw_check(pw_ctx *ctx);
 
 /* The whole stack in place: for l = 0..L-1, x <- bf16(x + layer_l(RMSNorm(x))), i.e.
@@ -184,7 +196,8 @@ pw_status pw_routing_features(pw_ctx *ctx, int layer, double *phi, int reset);
  * dropped). */
 pw_status pw_set_gemv_tokens(pw_ctx *ctx, int max_tokens);
 
-/* Tracing: while on, every forward records five CUDA timing events per layer, before,
+/* Tracing (no counterpart in the paper; measurement only): while on, every forward records
+ * five CUDA timing events per layer, before,
  * between and after its four kernels (router, gate_up, down, combine), on the launch
  * stream; stack graphs captured while on contain the event records.  The events are
  * owned by the context.  pw_profile_read waits for the latest recording of `layer` and
@@ -222,8 +235,12 @@ typedef struct {
 } pw_block_info;
 
 /* Commit bitwidth q for a block now (stream-ordered write of the device table entry on
- * the ctx stream).  Every page below q must be GPU-resident and no transfer pending,
- * else PW_ERR_STATE. */
+ * the ctx stream).  Sec. 3.1 ("Paged Weight Representation"): the page table row holds the
+ * committed bitwidth q_i the kernels read, and q_i may only name pages the GPU holds;
+ * Sec. 3.3: a bitwidth changes only at a safe boundary, here between launches on the ctx
+ * stream.  Every page below q must be GPU-resident (else PW_ERR_STATE, as for an unpacked
+ * block); PW_ERR_BUSY while a transfer of the block is in flight; PW_ERR_INVALID if q is not
+ * a supported bitwidth or block is out of range. */
 pw_status pw_set_bits(pw_ctx *ctx, int block, int q);
 
 /* Offload (Sec. 3.1, Sec. 3.3): lower the committed bitwidth of `block` to q_new first
@@ -241,14 +258,20 @@ pw_status pw_offload(pw_ctx *ctx, int block, int q_new);
 pw_status pw_reload(pw_ctx *ctx, int block, int q_new);
 
 /* Apply every transfer that has landed: retire offloaded device pages and commit the
- * raises of landed reloads on the ctx stream.  *n_applied (may be NULL) receives the
+ * raises of landed reloads on the ctx stream (Sec. 3.1: q_i rises only once the pages are
+ * GPU-resident; Sec. 3.3 and Fig. 4: a reload becomes visible to the kernels at a later safe
+ * commit point, and retired pages become free device memory).  *n_applied (may be NULL) receives the
  * number of raises committed.  Never blocks.  A failed copy rolls its block back
  * (pages stay or become CPU-resident, q is not raised) and returns PW_ERR_CUDA. */
 pw_status pw_commit(pw_ctx *ctx, int *n_applied);
 
-/* Wait for every transfer in flight (then pw_commit applies them). */
+/* Wait for every transfer in flight (then pw_commit applies them).  Sec. 3.3's page movement
+ * is asynchronous; this is the blocking point a caller uses before teardown or a test. */
 pw_status pw_sync_io(pw_ctx *ctx);
 
+/* One row of the weight page table and its host-side state (Sec. 3.1: the committed bitwidth
+ * q_i, the desired bitwidth d_i, where each page lives, and M_i^b of Eq. 3 for every b).
+ * info: caller storage.  PW_ERR_INVALID if block is out of range.  Does not wait. */
 pw_status pw_query(pw_ctx *ctx, int block, pw_block_info *info);
 
 typedef struct {
@@ -260,9 +283,12 @@ typedef struct {
     int64_t held_bytes;       /* device bytes of the weight pages the GPU holds: resident, in
                                  transfer, or lowered but not yet retired by pw_commit */
 } pw_mem_info;
+/* Memory accounting of the context (Sec. 3.1 and Eq. 3: the GPU holds M_i^{q_i} bytes of
+ * block i; Sec. 3.3: retired pages return to the device budget).  Does not wait. */
 pw_status pw_memory(pw_ctx *ctx, pw_mem_info *info);
 
-/* Host-side fault injection for testing the page I/O paths (no GPU fault is ever made):
+/* Host-side fault injection for testing the page I/O paths (no GPU fault is ever made; no
+ * counterpart in the paper):
  * kind 1 = the n-th next page copy is reported failed instead of issued;
  * kind 2 = the n-th next device page allocation fails;
  * kind 3 = while n != 0, no transfer is observed as landed (the copies still run), so a
@@ -419,11 +445,17 @@ pw_status pw_kv_get_stats(pw_kv *kv, pw_kv_stats *out);
 /* ---------------------------------------------------------------- inspection */
 
 /* b-bit codes of a block as the GPU kernels read them (the same device extraction code
- * as the forward): host uint8 [N][K].  Pages 0..b-1 must be GPU-resident.  Waits. */
+ * as the forward): host uint8 [N][K].  Sec. 2.2 (Any-Precision LLM's overlaid bit-planes):
+ * the b-bit code of an element is its top b bit-planes, plane 0 the most significant.
+ * Pages 0..b-1 must be GPU-resident, else PW_ERR_STATE; PW_ERR_INVALID for a bad block or
+ * b outside 1..bmax.  Waits for the ctx stream. */
 pw_status pw_unpack_indices(pw_ctx *ctx, int block, int b, uint8_t *host_out);
 
 /* Dequantised weights W^(b)[n][k] = LUT_b[n][code] as the GPU kernels produce them:
- * host fp16 bits [N][K].  Pages 0..b-1 and LUT_b must be GPU-resident.  Waits. */
+ * host fp16 bits [N][K].  Sec. 2.2: each output row has its own table of 2^b centroids per
+ * supported bitwidth b, indexed by the b-bit code.  Pages 0..b-1 and LUT_b must be
+ * GPU-resident, else PW_ERR_STATE; PW_ERR_INVALID for a bad block or unsupported b.
+ * Waits for the ctx stream. */
 pw_status pw_dequant(pw_ctx *ctx, int block, int b, uint16_t *host_out);
 
 /* Self-check of the 5th-generation tensor-core path (tcgen05) on one CTA: D[128][N] =
@@ -436,7 +468,8 @@ pw_status pw_dequant(pw_ctx *ctx, int block, int b, uint16_t *host_out);
 pw_status pw_tc_selftest(const uint16_t *A, const uint16_t *B, int N, int K, int flags, float *D, int *err,
                          pw_stream stream);
 
-/* Pure host helpers (no context, no GPU) for checking the packer.
+/* Pure host helpers (no context, no GPU) for checking the packer (Sec. 2.2 bit-planes,
+ * Sec. 3.1 one page per plane).
  * pw_pack_planes_host: the plain plane layout -- planes [bmax][N][W] uint32,
  *   W = ceil(K/128)*4 words per row, bit j of word w is column 32w+j, plane 0 = MSB.
  * pw_tile_planes_host / pw_untile_planes_host: the kernel-private device tiling of
