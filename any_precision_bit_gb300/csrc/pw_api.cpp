@@ -177,6 +177,8 @@ struct pw_ctx {
   int fault_copy = 0, fault_alloc = 0;
   int hold = 0;  // testing: transfers are not observed as landed while set
   int gemv_max = kGemvDefaultTokens;  // routed items of at most this many tokens run on the CUDA cores
+  int fault_withhold = 0;              // testing: the next forward withholds one device barrier arrival
+  long long wait_cycles = kWaitCyclesDefault;  // bounded device waits of the expert kernels
 };
 
 namespace {
@@ -689,6 +691,7 @@ static pw_status forward_args(pw_ctx *c, int layer, const void *x, int T, void *
   if (c->packed_count[layer] != 2 * c->d.E) return fail(c, PW_ERR_STATE, "layer %d has unpacked blocks", layer);
   *a = FwdArgs{};
   a->layer = layer;
+  a->stat_layer = layer;
   a->T = T;
   a->E = c->d.E;
   a->H = c->d.H;
@@ -706,6 +709,9 @@ static pw_status forward_args(pw_ctx *c, int layer, const void *x, int T, void *
   a->w_out = w;
   a->sm_count = c->sm_count;
   a->gemv_max = c->gemv_max;
+  a->wait_cycles = c->wait_cycles;
+  a->withhold = c->fault_withhold;
+  c->fault_withhold = 0;  // one launch
   a->bmaps = c->has_bmaps ? &c->bmaps : nullptr;
   return PW_OK;
 }
@@ -1115,8 +1121,14 @@ pw_status pw_set_fault(pw_ctx *c, int kind, int n) {
     c->fault_alloc = n;
   else if (kind == 3)
     c->hold = n ? 1 : 0;
-  else
+  else if (kind == 4)
+    c->fault_withhold = n ? 1 : 0;
+  else if (kind == 5) {
+    if (n < 0) return fail(c, PW_ERR_INVALID, "wait limit must be >= 0 microseconds");
+    c->wait_cycles = n ? (long long)n * 2000 : kWaitCyclesDefault;  // about 2 SM cycles per ns
+  } else
     return fail(c, PW_ERR_INVALID, "unknown fault kind %d", kind);
+  if (kind >= 4) drop_graphs(c);  // captured launches hold the old arguments
   return PW_OK;
 }
 

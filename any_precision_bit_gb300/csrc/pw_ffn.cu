@@ -102,8 +102,10 @@ struct Tiling {
   static_assert(kAStages % 4 == 0, "each A buffer belongs to one chunk stream");
   static_assert(kBStages <= kBStagesMax, "activation stages");
 };
-constexpr uint32_t kWaitSleepNs = 20000;          // suspend-time hint of a barrier wait
-constexpr long long kWaitLimitCycles = 1LL << 32;  // a wait gives up after this many SM cycles (about 2 s)
+constexpr uint32_t kWaitSleepNs = 20000;  // suspend-time hint of a barrier wait
+// The launch's wait limit in SM cycles (FwdArgs::wait_cycles), set by thread 0 before the
+// roles start.
+__shared__ long long s_wait_cycles;
 constexpr int kSmemLimit = 227 * 1024 - 1024;
 
 // Shared-memory map.  The host fills npad_max, b_bytes and smem (the dynamic size);
@@ -250,7 +252,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) break;
+    if (clock64() - t0 > s_wait_cycles) break;
   }
   *abort_flag = 1;
   atomicExch(err, 1);
@@ -259,7 +261,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Wait that ignores the abort flag (used to drain what this thread issued); bounded.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
-  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs) && clock64() - t0 <= kWaitLimitCycles) {
+  while (!mbar_try_wait_sleep(bar, parity, kWaitSleepNs) && clock64() - t0 <= s_wait_cycles) {
   }
 }
 // Two waits taken by a whole warp; when both phases are already complete (the common case
@@ -745,7 +747,10 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bars + 8 * (kTAF + ts));
+      // (testing: a.withhold keeps back one arrival of the launch's first routed chunk, so that
+      // the MMA warp's bounded wait on it expires; nothing asynchronous is held back)
+      const bool keep_back = PHASE == 1 && a.withhold && as == 0 && quarter == 0;
+      if (lane == 0 && !keep_back) mbar_arrive(bars + 8 * (kTAF + ts));
     } else {
       if (!wait_bar_all(bars + 8 * (kGXF + stream), gx_seq & 1, abort_flag, a.s.err)) return false;
 #pragma unroll 1
@@ -987,6 +992,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
       mbar_init(bars + 8 * (kAFG + i), kDq);
     }
     abort_flag = 0;
+    s_wait_cycles = a.wait_cycles > 0 ? a.wait_cycles : kWaitCyclesDefault;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {

@@ -298,6 +298,7 @@ struct LayerDev {
 
 struct FwdArgs {
   int layer, T, E, H, I, K, Is, renorm, flags;
+  int stat_layer;         // row of the routing statistics the router adds to (the layer, or 0 for discarded slots)
   const BlockDev *table;  // device page table
   LayerDev lay;
   Scratch s;
@@ -307,9 +308,12 @@ struct FwdArgs {
   float *w_out;           // optional
   int sm_count;
   int gemv_max;           // routed work items of at most this many tokens run on the CUDA cores (decode tiling)
+  long long wait_cycles;  // a bounded device wait of the expert kernels gives up after this many SM cycles
+  int withhold;           // testing: 1 = the gate_up kernel withholds one A-buffer arrival (its wait expires)
   const BMaps *bmaps;     // host copy of the activation tensor maps
 };
 constexpr int kGemvMaxTokens = 8;      // largest GEMV item
+constexpr long long kWaitCyclesDefault = 1LL << 32;  // bounded device waits: about 2 s of SM clock
 constexpr int kGemvDefaultTokens = 0;  // default threshold of a context (the tensor cores measured faster)
 
 // ev: null, or five timing events recorded before, between and after the four kernels

@@ -350,7 +350,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   // and the running statistics of this thread's expert (E <= kRtThreads).
   const BlockDev *tab = a.table + (size_t)a.layer * E * 2;
   const int q1 = tid < E ? tab[2 * tid].q : 0, q2 = tid < E ? tab[2 * tid + 1].q : 0;
-  const size_t si = (size_t)a.layer * E + tid;
+  const size_t si = (size_t)a.stat_layer * E + tid;
   double st_c = 0., st_w = 0., st_p[4] = {0., 0., 0., 0.};
   if (tid < E) {
     st_c = a.s.stat_count[si];

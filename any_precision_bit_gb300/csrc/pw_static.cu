@@ -114,8 +114,12 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   s.sgate = reinterpret_cast<float *>(take(sizes[17]));
   s.max_items1 = 0;
   s.max_items2 = 0;
+  // a router whose bounded wait for its copies expires records it in the context's own error
+  // word (allocated by pw_create), which the next pw_check on the context reports
+  s.err = a.s.err;
   a.s = s;
-  a.layer = 0;  // the kernel indexes its statistics by layer; these go to the discarded slots
+  a.stat_layer = 0;  // the statistics go to the discarded slots; a.layer still selects the
+                     // layer's router, bias and page-table bitwidths
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the last-CTA tickets must start at zero; the array keeps whatever the last call left

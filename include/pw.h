@@ -216,7 +216,10 @@ pw_status pw_profile_read(pw_ctx *ctx, int layer, float *ms);
  * does not fit returns PW_ERR_INVALID.  The first call on a device looks up the array's
  * device address, so make it before any stream capture.  Calls share the array: calls
  * that overlap on the GPU (e.g. on two streams) race.  Online routing statistics are not
- * updated.  No cudaMalloc, cudaFree or other allocation happens in the call. */
+ * updated.  The call returns before the router runs: if the router's bounded wait for its
+ * input copies gives up, a pw_check on the context made after the call's stream has run it
+ * reports PW_ERR_TIMEOUT (and the ids and w of that call are invalid).  No cudaMalloc, cudaFree or other allocation happens
+ * in the call. */
 pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int T, int32_t *ids, float *w,
                            int flags, pw_stream stream);
 
@@ -292,7 +295,14 @@ pw_status pw_memory(pw_ctx *ctx, pw_mem_info *info);
  * kind 1 = the n-th next page copy is reported failed instead of issued;
  * kind 2 = the n-th next device page allocation fails;
  * kind 3 = while n != 0, no transfer is observed as landed (the copies still run), so a
- * test can act while pages are in transfer.  n = 0 clears. */
+ * test can act while pages are in transfer;
+ * kind 4 = with n != 0, the next forward's gate_up kernel withholds one barrier arrival of
+ *   its first routed chunk (nothing asynchronous is held back), so that the bounded device
+ *   wait on it expires: the launch's outputs are invalid and pw_check reports
+ *   PW_ERR_TIMEOUT, after which the context is usable as before;
+ * kind 5 = bounded device waits of the expert kernels give up after about n microseconds
+ *   (n = 0: the default, about 2 s).
+ * n = 0 clears kinds 1-4. */
 pw_status pw_set_fault(pw_ctx *ctx, int kind, int n);
 
 /* ---------------------------------------------------------------- planner */
