@@ -159,7 +159,20 @@ def test_split_k_parts(name, T):
 
 
 # ---------------------------------------------------------------- model-shaped layers
-CASES = [("qwen", 1), ("qwen", 16), ("qwen", 64), ("g128", 1), ("g128", 32), ("mixtral", 1), ("mixtral", 8)]
+# every decode batch the benchmarks time: Qwen-shaped T = 1, 16, 64, 256; 128-expert T = 1, 32,
+# 256; Mixtral-shaped T = 1, 8, 64, 256
+CASES = [("qwen", 1), ("qwen", 16), ("qwen", 64), ("qwen", 256), ("g128", 1), ("g128", 32), ("g128", 256),
+         ("mixtral", 1), ("mixtral", 8), ("mixtral", 64), ("mixtral", 256)]
+
+
+def expert_cover(ids, E):
+    """The first and the last token routed to each expert (every expert's work items)."""
+    tok = set()
+    for e in range(E):
+        rows = np.nonzero((ids == e).any(axis=1))[0]
+        if len(rows):
+            tok.update((int(rows[0]), int(rows[-1])))
+    return np.array(sorted(tok))
 
 
 @pytest.mark.parametrize("name,T", CASES)
@@ -170,10 +183,14 @@ def test_model_shaped_layer(name, T):
     try:
         data.load(pw, ctx)
         y, ids, w = run_layer(ctx, data, T)
-        y_ref, ids_ref, w_ref = data.oracle()
-        assert np.array_equal(ids, ids_ref)
-        assert np.allclose(w, w_ref, rtol=1e-5, atol=1e-7)
-        assert_close(y, y_ref, f"{name} T={T}")
+        # the Mixtral shape's dense float64 experts are large: check its bigger batches on the
+        # first and last token of every expert (rows are independent); routing on every token
+        tok = expert_cover(ids, shape.E) if (name == "mixtral" and T > 8) else None
+        ids_all, w_all, _ = omoe.route(data.x, data.Wr, data.bias, shape.K)
+        assert np.array_equal(ids, ids_all)
+        assert np.allclose(w, w_all, rtol=1e-5, atol=1e-7)
+        y_ref, _, _ = data.oracle(tokens=tok)
+        assert_close(y if tok is None else y[tok], y_ref, f"{name} T={T}")
     finally:
         pw.pw_destroy(ctx)
 
