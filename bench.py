@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-also", action="store_true",
+                    help="skip the largest single-GPU configurations timed after the main workload")
     ap.add_argument("--gemv-tokens", type=int, default=None,
                     help="routed work items of at most this many tokens run on the CUDA cores (default: the library's)")
     ap.add_argument("--paging", action="store_true",
@@ -54,11 +56,12 @@ def parse():
 
 PREFILL_MIN_T = 512  # batches of at least this many tokens run the prefill tiling (tensor-bound)
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of one launch) per
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture of each launch) per
 # algorithmic byte of that launch, for the expert kernels: (phase, prefill tiling) -> ratio.
-# Taken on the two-layer Qwen-shaped decode run and the one-layer Mixtral-shaped prefill run
-# of this kernel version; to be measured again whenever the kernel changes.
-TRAFFIC_PER_ALGORITHMIC_BYTE = {(1, False): 1.040, (2, False): 1.056, (1, True): 1.320, (2, True): 2.904}
+# Taken on the two-layer Qwen-shaped decode run (T = 64) and the one-layer Mixtral-shaped
+# prefill run (T = 4096) of the current kernels (profiles/ names the commands); to be measured
+# again whenever the expert kernels change.
+TRAFFIC_PER_ALGORITHMIC_BYTE = {(1, False): 1.031, (2, False): 1.029, (1, True): 1.320, (2, True): 2.720}
 
 
 def peaks():
@@ -99,8 +102,9 @@ class Clocks:
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
+    def __init__(self, index, period_ms=5):
         self.index = index
+        self.period_ms = period_ms
         self.proc = None
         self.path = None
 
@@ -110,7 +114,7 @@ class Clocks:
             os.close(fd)
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -329,6 +333,99 @@ def run_paging(args, pw, torch, ctx, shape, L, T, stream, x0, xw, clocks_cls):
     }
 
 
+def stack_roofline(pw, ctx, shape, qs, L, T, kern):
+    """Algorithmic bytes of the stack's layers (from the routing statistics of the timed
+    steps), the per-kernel shares from the profiled pass, and the roofline of the dominant
+    kernel: HBM GB/s at decode sizes, tensor TFLOP/s for prefill-sized batches."""
+    bytes_l = []
+    for l in range(L):
+        cnt, _ = pw.pw_routing_stats(ctx, l, shape.E)
+        bytes_l.append(layer_bytes(shape, qs[l], cnt, T))
+    tot = {k: sum(b[k] for b in bytes_l) for k in bytes_l[0]}
+    peak, peak_kind = peaks()
+    # dominant kernel: the one with the largest share of the step
+    share = kern.sum(axis=0) / kern.sum()
+    names = ["route_kernel + gather_kernel", "tc_ffn_kernel<1> (gate_up + SiLU*up)", "tc_ffn_kernel<2> (down)",
+             "combine_kernel"]
+    dom = int(np.argmax(share))
+    dom_bytes = {1: tot["gu"] + tot["sh_gu"] + T * shape.H * 2 * L,
+                 2: tot["dn"] + tot["sh_dn"],
+                 0: tot["router"] + T * shape.H * 2 * L,
+                 3: T * shape.H * 2 * L}[dom]
+    dom_ms = kern[:, dom].sum()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    ratio = TRAFFIC_PER_ALGORITHMIC_BYTE.get((dom, T >= PREFILL_MIN_T)) if dom in (1, 2) else None
+    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": ratio * dom_bytes / L if ratio else None,
+                "algorithmic_bytes_per_launch": dom_bytes / L, "avg_launch_ms": dom_ms / L,
+                "kernel_share": {n: float(s) for n, s in zip(names, share)}}
+    flops = None
+    if T >= PREFILL_MIN_T and dom in (1, 2):
+        # prefill: the expert kernels are tensor-bound; algorithmic FLOPs of the dominant one
+        # = 2 x (routed pairs x its block's N x K + tokens x the shared block's N x K)
+        pairs = T * shape.K
+        fl = {1: 2.0 * (pairs * 2 * shape.I * shape.H + T * 2 * shape.Is * shape.H),
+              2: 2.0 * (pairs * shape.H * shape.I + T * shape.H * shape.Is)}
+        flops = fl
+        tp, tp_kind = tensor_peak()
+        t_ach = fl[dom] * L / (dom_ms * 1e-3) / 1e12
+        roofline.update({"bound": "tensor", "achieved": t_ach, "peak": tp, "peak_kind": tp_kind,
+                         "unit": "TFLOP/s", "frac": t_ach / tp, "algorithmic_flops_per_launch": fl[dom],
+                         "hbm_achieved_gbs": achieved})
+    return {"bytes_l": bytes_l, "tot": tot, "roofline": roofline, "flops": flops}
+
+
+def time_stack(pw, torch, ctx, shape, qs, L, T, steps, warmup, seed, local):
+    """One more workload on an already loaded stack: warm-up, K timed steps (CUDA events on
+    the launching stream, clocks sampled during them), a profiled pass for the kernel
+    shares, and the dominant kernel's roofline."""
+    stream = torch.cuda.Stream()
+    pw.pw_set_stream(ctx, stream)
+    x0 = torch.from_numpy(syn.gen_tokens_np(shape, seed, 0, T).view(np.int16)).cuda()
+    xw = torch.empty_like(x0)
+    torch.cuda.synchronize()
+
+    def step():
+        xw.copy_(x0)
+        pw.pw_stack_forward(ctx, xw, T, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            step()
+    stream.synchronize()
+    for l in range(L):
+        pw.pw_routing_stats(ctx, l, shape.E, reset=True)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+    stream.synchronize()
+    ms = ev0.elapsed_time(ev1) / steps
+    clk = clocks.stop()
+    pw.pw_set_profiling(ctx, 1)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    kern = np.array([pw.pw_profile_read(ctx, l) for l in range(L)], dtype=np.float64)
+    pw.pw_set_profiling(ctx, 0)
+    rf = stack_roofline(pw, ctx, shape, qs, L, T, kern)
+    out = {"config": workload_config(shape, T, L), "value": T * L / (ms * 1e-3), "unit": "tokens/s",
+           "steps": steps, "warmup": max(warmup, 3), "ms_per_step": ms,
+           "gbs": rf["tot"]["total"] / (ms * 1e-3) / 1e9, "roofline": rf["roofline"], "clocks": clk,
+           "gpu_launches": 5 * L * steps}
+    if rf["flops"] is not None:
+        out["tflops"] = (rf["flops"][1] + rf["flops"][2]) * L / (ms * 1e-3) / 1e12
+    return out
+
+
 def run_ours(args, shape, L, T):
     import torch
     import any_precision_bit_gb300 as pw
@@ -416,43 +513,10 @@ def run_ours(args, shape, L, T):
     stream.synchronize()
     kern = np.array([pw.pw_profile_read(ctx, l) for l in range(L)], dtype=np.float64)  # [L][4] ms
     pw.pw_set_profiling(ctx, 0)
-    bytes_l = []
-    for l in range(L):
-        cnt, _ = pw.pw_routing_stats(ctx, l, shape.E)
-        bytes_l.append(layer_bytes(shape, qs[l], cnt, T))
-    tot = {k: sum(b[k] for b in bytes_l) for k in bytes_l[0]}
+    rf = stack_roofline(pw, ctx, shape, qs, L, T, kern)
+    bytes_l, tot, roofline, flops = rf["bytes_l"], rf["tot"], rf["roofline"], rf["flops"]
     value = world * T * L / (ms * 1e-3)
-    peak, peak_kind = peaks()
-    # dominant kernel: the one with the largest share of the step
-    share = kern.sum(axis=0) / kern.sum()
-    names = ["route_kernel + gather_kernel", "tc_ffn_kernel<1> (gate_up + SiLU*up)", "tc_ffn_kernel<2> (down)",
-             "combine_kernel"]
-    dom = int(np.argmax(share))
-    dom_bytes = {1: tot["gu"] + tot["sh_gu"] + T * shape.H * 2 * L,
-                 2: tot["dn"] + tot["sh_dn"],
-                 0: tot["router"] + T * shape.H * 2 * L,
-                 3: T * shape.H * 2 * L}[dom]
-    dom_ms = kern[:, dom].sum()
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    ratio = TRAFFIC_PER_ALGORITHMIC_BYTE.get((dom, T >= PREFILL_MIN_T)) if dom in (1, 2) else None
-    roofline = {"bound": "hbm", "kernel": names[dom], "achieved": achieved, "peak": peak,
-                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": ratio * dom_bytes / L if ratio else None,
-                "algorithmic_bytes_per_launch": dom_bytes / L, "avg_launch_ms": dom_ms / L,
-                "kernel_share": {n: float(s) for n, s in zip(names, share)}}
-    flops = None
-    if T >= PREFILL_MIN_T and dom in (1, 2):
-        # prefill: the expert kernels are tensor-bound; algorithmic FLOPs of the dominant one
-        # = 2 x (routed pairs x its block's N x K + tokens x the shared block's N x K)
-        pairs = T * shape.K
-        fl = {1: 2.0 * (pairs * 2 * shape.I * shape.H + T * 2 * shape.Is * shape.H),
-              2: 2.0 * (pairs * shape.H * shape.I + T * shape.H * shape.Is)}
-        flops = fl
-        tp, tp_kind = tensor_peak()
-        t_ach = fl[dom] * L / (dom_ms * 1e-3) / 1e12
-        roofline.update({"bound": "tensor", "achieved": t_ach, "peak": tp, "peak_kind": tp_kind,
-                         "unit": "TFLOP/s", "frac": t_ach / tp, "algorithmic_flops_per_launch": fl[dom],
-                         "hbm_achieved_gbs": achieved})
+    peak, _ = peaks()
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -491,13 +555,28 @@ def run_ours(args, shape, L, T):
         line["e2e"] = {"value": world * T * L / te, "unit": "tokens/s", "ms_per_step": te * 1e3,
                        "h2d_bytes_per_step": T * shape.H * 2, "d2h_bytes_per_step": T * shape.H * 2}
     if rank == 0 and not args.no_cpu_baseline:
+        line["_cpu_pending"] = True
+    pw.pw_destroy(ctx)
+    # The largest single-GPU configurations, on one loaded stack: the Mixtral-shaped stack with
+    # all 32 layers, decoding a 256-token batch and running a 4096-token prefill.
+    if world == 1 and not args.no_also and args.config == "qwen":
+        mix = syn.SHAPES["mixtral"]
+        t0 = time.time()
+        mctx, mqs = load_stack(pw, torch, mix, mix.L, mix.prefill_T, args.seed, local)
+        setup = round(time.time() - t0, 1)
+        also = [time_stack(pw, torch, mctx, mix, mqs, mix.L, 256, max(args.steps, 10), args.warmup, args.seed, local),
+                time_stack(pw, torch, mctx, mix, mqs, mix.L, mix.prefill_T, 5, 3, args.seed, local)]
+        for a in also:
+            a["setup_s"] = setup
+        line["also"] = also
+        pw.pw_destroy(mctx)
+    if line.pop("_cpu_pending", False):
         Ts = min(T, 64)
         sample = oracle_sample(shape, args.seed, Ts)
         t = time_oracle(shape, sample)
         line["cpu_baseline"] = {"value": Ts / t, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"layer 0 of {L}, the first {Ts} of {T} tokens, one pass of the float64 "
                                           f"numpy oracle ({t:.1f} s); BLAS may use every core, the rest runs on one"}
-    pw.pw_destroy(ctx)
     if dist:
         dist.barrier()
         dist.destroy_process_group()
