@@ -467,7 +467,7 @@ __device__ void lut_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, u
 // The activation producer: per chunk, slot b_seq % kBSlots is refilled once the MMAs of its
 // previous chunk are done; lane i loads box i (stage i / boxes, rows kBoxRows (i % boxes)
 // onward) of the item's consecutive rows, all completing on the slot's barrier.
-template <int PHASE, int TOK>
+template <int PHASE, int TOK, bool GV>
 __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L, uint8_t *sm, uint32_t bars,
                             const ItemQueue &qu, volatile int *abort_flag) {
   using T_ = Tiling<TOK>;
@@ -479,7 +479,7 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
     WorkItem w;
     ItemView v;
     if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
-    if (v.gemv) {  // one 8-row box of 128 columns per chunk into its stream's GEMV slot
+    if (GV && v.gemv) {  // one 8-row box of 128 columns per chunk into its stream's GEMV slot
       const TmaDesc *map = PHASE == 1 ? &bm.gemv.xs : &bm.gemv.h_routed;
       for (int kc = w.kc0; kc < w.kc1; ++kc) {
         const uint32_t gs = a_seq++ % kDqStreams;
@@ -538,7 +538,7 @@ __device__ __forceinline__ uint64_t b_desc(uint32_t stage) { return smem_desc_sw
 // as its operands stay in the uniform datapath.  For a GEMV item the warp only grants the
 // accumulator buffer to the dequantising warps and returns each chunk's slabs to the weight
 // producer once those warps have read them.
-template <int PHASE, int TOK>
+template <int PHASE, int TOK, bool GV>
 __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                            const ItemQueue &qu, volatile int *abort_flag) {
   using T_ = Tiling<TOK>;
@@ -561,7 +561,7 @@ __device__ void mma_issuer(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uin
     ok = wait_bar_all(bars + 8 * (kAE + acs), ((item_seq / 2) & 1) ^ 1, abort_flag, a.s.err);
     if (!ok) break;
     ++item_seq;
-    if (v.gemv) {  // computed by the dequantising warps: grant them the accumulator buffer
+    if (GV && v.gemv) {  // computed by the dequantising warps: grant them the accumulator buffer
       if (elect_one()) mbar_arrive(bars + 8 * (kGAG + gi_seq % 2));
       __syncwarp();
       ++gi_seq;
@@ -689,7 +689,7 @@ __device__ __forceinline__ void dq_words(const uint32_t (&W)[8], const LutRegs &
 // dot products; at the end of the item the stream's sums go to tensor memory (columns
 // 8 stream + t of the item's accumulator buffer), where the epilogue adds the streams in
 // order.  Either way the warp then signals the chunk's A-buffer barrier.
-template <int PHASE, int TOK, int Q>
+template <int PHASE, int TOK, bool GV, int Q>
 __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, uint8_t *sm, const TcLayout &L,
                         uint32_t bars, uint32_t tmem, uint32_t lut_slot, int quarter, int stream, RingPos &pos,
                         uint32_t &a_seq, uint32_t &gx_seq, uint32_t &gi_seq, uint32_t acs, volatile int *abort_flag) {
@@ -708,7 +708,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   const uint32_t cg_off = (uint32_t)v.nr * 4;  // column-group stride inside a slab
   const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off + (uint32_t)r * 4;
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-  const bool gemv = TOK == kTokChunk && v.gemv;
+  const bool gemv = GV && TOK == kTokChunk && v.gemv;
   const uint32_t gx = smem_u32(sm) + (uint32_t)L.gx_off + (uint32_t)stream * kGxBytes;
   float acc[kGemvMaxTok];
 #pragma unroll
@@ -803,7 +803,7 @@ __device__ bool dq_item(const FwdArgs &a, const WorkItem &w, const ItemView &v, 
   return true;
 }
 
-template <int PHASE, int TOK>
+template <int PHASE, int TOK, bool GV>
 __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, uint32_t bars, uint32_t tmem,
                             const ItemQueue &qu, volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -833,7 +833,7 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
     switch (v.q) {
 #define PW_DQ_CASE(QQ)                                                                                          \
   case QQ:                                                                                                      \
-    ok = dq_item<PHASE, TOK, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, stream, pos, a_seq, gx_seq, gi_seq, acs, \
+    ok = dq_item<PHASE, TOK, GV, QQ>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, stream, pos, a_seq, gx_seq, gi_seq, acs, \
                                  abort_flag);                                                                  \
     break;
       PW_DQ_CASE(1)
@@ -844,7 +844,7 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
       PW_DQ_CASE(6)
       PW_DQ_CASE(7)
       default:
-        ok = dq_item<PHASE, TOK, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, stream, pos, a_seq, gx_seq, gi_seq, acs,
+        ok = dq_item<PHASE, TOK, GV, 8>(a, w, v, sm, L, bars, tmem, lut_slot, quarter, stream, pos, a_seq, gx_seq, gi_seq, acs,
                                     abort_flag);
         break;
 #undef PW_DQ_CASE
@@ -859,7 +859,7 @@ __device__ void dequantiser(const FwdArgs &a, const TcLayout &L, uint8_t *sm, ui
   }
 }
 
-template <int PHASE, int TOK>
+template <int PHASE, int TOK, bool GV>
 __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const ItemQueue &qu,
                          volatile int *abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -870,7 +870,7 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
     ItemView v;
     if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
     const int acs = item_seq % 2;
-    const bool gemv = TOK == kTokChunk && v.gemv;
+    const bool gemv = GV && TOK == kTokChunk && v.gemv;
     bool ok;
     if (gemv) {
       ok = wait_bar_all(bars + 8 * (kAFG + gi_seq % 2), (gi_seq / 2) & 1, abort_flag, a.s.err);
@@ -931,7 +931,7 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
   }
 }
 
-template <int PHASE, int TOK>
+template <int PHASE, int TOK, bool GV>
 __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayout L, const __grid_constant__ BMaps bm) {
   using T_ = Tiling<TOK>;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -1009,15 +1009,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   const uint32_t tmem = tmem_slot;
   const ItemQueue qu{queue_slot, bars};
   if (warp < kDq)
-    dequantiser<PHASE, TOK>(a, L, sm, bars, tmem, qu, &abort_flag);
+    dequantiser<PHASE, TOK, GV>(a, L, sm, bars, tmem, qu, &abort_flag);
   else if (warp < kWarpP)
-    epilogue<PHASE, TOK>(a, bars, tmem, qu, &abort_flag);
+    epilogue<PHASE, TOK, GV>(a, bars, tmem, qu, &abort_flag);
   else if (warp == kWarpP)
     weight_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
   else if (warp == kWarpAB)
-    ab_producer<PHASE, TOK>(a, bm, L, sm, bars, qu, &abort_flag);
+    ab_producer<PHASE, TOK, GV>(a, bm, L, sm, bars, qu, &abort_flag);
   else if (warp == kWarpMma)
-    mma_issuer<PHASE, TOK>(a, L, sm, bars, tmem, qu, &abort_flag);
+    mma_issuer<PHASE, TOK, GV>(a, L, sm, bars, tmem, qu, &abort_flag);
   else
     lut_producer<PHASE>(a, L, sm, bars, qu, &abort_flag);
   tc_fence_before();
@@ -1028,7 +1028,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   }
 }
 
-template <int TOK>
+template <int TOK, bool GV>
 static int launch_tiled(const FwdArgs &a, int phase, cudaStream_t st) {
   using T_ = Tiling<TOK>;
   TcLayout L{};
@@ -1042,17 +1042,19 @@ static int launch_tiled(const FwdArgs &a, int phase, cudaStream_t st) {
   const int max_items = phase == 1 ? a.s.max_items1 : a.s.max_items2;
   const int grid = min(max_items, a.sm_count);
   if (phase == 1) {
-    cudaFuncSetAttribute(tc_ffn_kernel<1, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-    return (int)launch_pdl(tc_ffn_kernel<1, TOK>, dim3(grid), dim3(kTcThreads), (size_t)L.smem, st, a, L, bm);
+    cudaFuncSetAttribute(tc_ffn_kernel<1, TOK, GV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    return (int)launch_pdl(tc_ffn_kernel<1, TOK, GV>, dim3(grid), dim3(kTcThreads), (size_t)L.smem, st, a, L, bm);
   }
-  cudaFuncSetAttribute(tc_ffn_kernel<2, TOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
-  return (int)launch_pdl(tc_ffn_kernel<2, TOK>, dim3(grid), dim3(kTcThreads), (size_t)L.smem, st, a, L, bm);
+  cudaFuncSetAttribute(tc_ffn_kernel<2, TOK, GV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+  return (int)launch_pdl(tc_ffn_kernel<2, TOK, GV>, dim3(grid), dim3(kTcThreads), (size_t)L.smem, st, a, L, bm);
 }
 
+// The kernel image with the GEMV items' code is launched only when some item may take that
+// path; the tensor-core-only image is smaller, which keeps instruction fetch out of the way.
 int launch_ffn(const FwdArgs &a, int phase, void *stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return tok_chunk_for(a.T) == kTokChunkPrefill ? launch_tiled<kTokChunkPrefill>(a, phase, st)
-                                                 : launch_tiled<kTokChunk>(a, phase, st);
+  if (tok_chunk_for(a.T) == kTokChunkPrefill) return launch_tiled<kTokChunkPrefill, false>(a, phase, st);
+  return a.gemv_max > 0 ? launch_tiled<kTokChunk, true>(a, phase, st) : launch_tiled<kTokChunk, false>(a, phase, st);
 }
 
 }  // namespace pw
