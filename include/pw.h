@@ -79,8 +79,8 @@ typedef struct {
  * model: the per-block weight pages and the device weight page table of Sec. 3.1 ("Paged
  * Weight Representation": committed bitwidth q_i, desired bitwidth d_i, per-page residency),
  * the compute and side streams of Sec. 3.3 ("Asynchronous Page Movement"), and the forward
- * scratch of the fused layer of Sec. 3.3.  The paper specifies no API; the call itself is this
- * library's (the benchmark spec (b): a small C-ABI library).  Requires H % 16 == 0, I % 8 == 0, Is % 8 == 0,
+ * scratch of the fused layer of Sec. 3.3.  The paper specifies no API; the call and its
+ * plain-C signature are this library's own.  Requires H % 16 == 0, I % 8 == 0, Is % 8 == 0,
  * K <= E <= 256, K <= 8.  Allocates the page table, scratch for max_tokens tokens and
  * the two streams (compute stream = a new non-blocking stream, side stream for page
  * copies).  Errors: PW_ERR_INVALID on bad shapes, PW_ERR_CUDA / PW_ERR_OOM otherwise. */
@@ -185,14 +185,15 @@ pw_status pw_routing_stats(pw_ctx *ctx, int layer, double *count, double *weight
  * phi.  Output host double [E][3].  Waits for the compute stream. */
 pw_status pw_routing_features(pw_ctx *ctx, int layer, double *phi, int reset);
 
-/* Decode kernel choice (the benchmark spec (d): CUDA-core bit-plane GEMV for the memory-bound decode
- * regime, tensor cores only where the path is a dense contraction; the paper's fused kernel,
- * Sec. 3.3, has one path).  At decode batch sizes (T < 512) a routed work item -- a 128-row
+/* Decode kernel choice (no counterpart in the paper: its fused kernel, Sec. 3.3, has one
+ * path; this switch offers a CUDA-core bit-plane GEMV for items too small to fill a tensor-core
+ * tile in the memory-bound decode regime).  At decode batch sizes (T < 512) a routed work item -- a 128-row
  * tile of one expert's block times the tokens routed to that expert -- with at most
  * `max_tokens` tokens is computed on the CUDA cores (packed fp16 products of the decoded
  * centroids and the activations, summed in fp32 per 32 columns); larger items go to the
  * tensor cores.  0 sends every item to the tensor cores.  Default 0 (on GB300 the
- * tensor-core items measured faster at every decode size); valid 0..8, else PW_ERR_INVALID.  Takes effect at the next forward launch (captured stack graphs are
+ * tensor-core items measured faster at every decode size); valid 0..8, else
+ * PW_ERR_INVALID.  Takes effect at the next forward launch (captured stack graphs are
  * dropped). */
 pw_status pw_set_gemv_tokens(pw_ctx *ctx, int max_tokens);
 
