@@ -15,13 +15,14 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libpw.so")
 
-PW_OK, PW_ERR_INVALID, PW_ERR_CUDA, PW_ERR_OOM, PW_ERR_STATE, PW_ERR_TIMEOUT, PW_ERR_BUSY = range(7)
+PW_OK, PW_ERR_INVALID, PW_ERR_CUDA, PW_ERR_OOM, PW_ERR_STATE, PW_ERR_TIMEOUT, PW_ERR_BUSY, PW_ERR_RANGE = range(8)
 PW_FLAG_POISON = 1
 PW_ACCUMULATE = 1
 PW_PRENORM = 2
 PW_PAGE_GPU, PW_PAGE_CPU, PW_PAGE_TO_CPU, PW_PAGE_TO_GPU = range(4)
 STATUS_NAMES = {0: "PW_OK", 1: "PW_ERR_INVALID", 2: "PW_ERR_CUDA", 3: "PW_ERR_OOM",
-                4: "PW_ERR_STATE", 5: "PW_ERR_TIMEOUT", 6: "PW_ERR_BUSY"}
+                4: "PW_ERR_STATE", 5: "PW_ERR_TIMEOUT", 6: "PW_ERR_BUSY",
+                7: "PW_ERR_RANGE"}
 
 
 class PwError(RuntimeError):

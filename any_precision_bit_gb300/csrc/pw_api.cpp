@@ -1289,7 +1289,11 @@ extern "C" pw_status pw_check(pw_ctx *c) {
   CU(c, cudaMemcpy(&err, c->s.err, sizeof(int), cudaMemcpyDeviceToHost));
   if (err) {
     CU(c, cudaMemset(c->s.err, 0, sizeof(int)));
-    return fail(c, PW_ERR_TIMEOUT, "a bounded wait in an expert kernel expired; that launch's outputs are invalid");
+    if (err & pw::kErrWaitMask)
+      return fail(c, PW_ERR_TIMEOUT, "a bounded device wait expired; that launch's outputs are invalid");
+    return fail(c, PW_ERR_RANGE,
+                "an activation left the fp16 range (|x| or |h| >= 65520, or NaN) or y is not finite; the outputs "
+                "since the last check are invalid");
   }
   return check_sticky(c);
 }

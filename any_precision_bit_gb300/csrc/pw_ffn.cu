@@ -255,7 +255,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     if (clock64() - t0 > s_wait_cycles) break;
   }
   *abort_flag = 1;
-  atomicExch(err, 1);
+  atomicOr(err, 1);
   return false;
 }
 // Wait that ignores the abort flag (used to drain what this thread issued); bounded.
@@ -885,6 +885,7 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
     const int R = w.tile * kCtaRows + row;
     const bool empty = w.kc1 <= w.kc0;     // nothing accumulated (an empty split part)
     const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + acs * Tiling<TOK>::kAccCols;
+    bool fin = true;  // every h written is a finite fp16
     for (int c = 0; c < (gemv ? 8 : v.npad); c += 8) {
       uint32_t r8[8];
       if (gemv) {  // the column-group sets' dot products, added in order
@@ -910,7 +911,9 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
           const float up = __shfl_down_sync(0xffffffffu, acc, 8);
           if ((row & 15) < 8 && R < v.N && j < v.ntok) {
             const int f = R / 16 * 8 + (R & 7);
-            const uint16_t hv = f2h(silu(acc) * up);
+            const float hf = silu(acc) * up;
+            fin = fin && fp16_finite(hf);
+            const uint16_t hv = f2h(hf);
             if (v.routed)
               a.s.h_routed[(size_t)(v.row0 + j) * a.I + f] = hv;
             else
@@ -924,6 +927,7 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
         }
       }
     }
+    if (PHASE == 1 && !fin) atomicOr(a.s.err, kErrRange);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kAE + acs));
@@ -952,7 +956,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
     // a dense chunk (16 slabs, one of padding at most) must fit the ring
     const bool misaligned = ((base + L.b_off) & 1023u) != 0u;  // swizzle atoms are 1 KB-aligned
     if (base >= kLutAddr || L.bar_off + kNumBars * 8 > L.lut_off || L.slabs < kDenseSlabs + 2 || misaligned) {
-      if (threadIdx.x == 0) atomicExch(a.s.err, 3);  // the map does not fit this launch
+      if (threadIdx.x == 0) atomicOr(a.s.err, 3);  // the map does not fit this launch
       return;
     }
   }

@@ -12,6 +12,7 @@
 //   bit transpose across the planes of a row then yields 4-bit codes of 8 consecutive
 //   columns per word, and an 8x8 transpose yields 8-bit codes of 4 columns per word.
 #pragma once
+#include <math.h>
 #include <stdint.h>
 
 #ifdef __CUDACC__
@@ -283,7 +284,8 @@ struct Scratch {
   double *stat_count;  // [L][E]
   double *stat_wsum;   // [L][E]
   double *stat_phi;    // [L][E][4] routed-input sums for Eq. 5: sum r, sum r n, sum r n^2, max n
-  int *err;            // [1] bounded-wait timeouts in the expert kernels (0 = none)
+  int *err;            // [1] error bits: kErrWaitMask = a bounded wait gave up (1 expert kernel,
+                       // 2 router, 3 tensor map), kErrRange = an fp16 activation or y not finite
   int *work;           // [2] next unclaimed work item of the two expert kernels (reset by the router)
   int max_items1, max_items2;
 };
@@ -314,6 +316,10 @@ struct FwdArgs {
 };
 constexpr int kGemvMaxTokens = 8;      // largest GEMV item
 constexpr long long kWaitCyclesDefault = 1LL << 32;  // bounded device waits: about 2 s of SM clock
+constexpr int kErrWaitMask = 0xFF;  // error-word bits of the bounded waits
+constexpr int kErrRange = 0x100;    // an fp16 activation (x or h) overflowed, or y is not finite
+// |v| < 65520 rounds to a finite fp16 (65504 at most); NaN fails the test too.
+PW_HD bool fp16_finite(float v) { return fabsf(v) < 65520.f; }
 constexpr int kGemvDefaultTokens = 0;  // default threshold of a context (the tensor cores measured faster)
 
 // ev: null, or five timing events recorded before, between and after the four kernels

@@ -91,7 +91,11 @@ __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
       acc.z += bf16f(old.y & 0xFFFF);
       acc.w += bf16f(old.y >> 16);
     }
-    *yp = make_uint2(pack2(f2bf(acc.x), f2bf(acc.y)), pack2(f2bf(acc.z), f2bf(acc.w)));
+    const uint2 yv = make_uint2(pack2(f2bf(acc.x), f2bf(acc.y)), pack2(f2bf(acc.z), f2bf(acc.w)));
+    *yp = yv;
+    // a bf16 whose exponent bits are all ones is an infinity or a NaN
+    const bool fin = (~yv.x & 0x7F80u) && (~yv.x & 0x7F800000u) && (~yv.y & 0x7F80u) && (~yv.y & 0x7F800000u);
+    if (!fin) atomicOr(a.s.err, kErrRange);
   }
 }
 

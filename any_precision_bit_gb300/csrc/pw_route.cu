@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
     bool landed = false;
     for (int round = 0; round < 2 && !landed; ++round) {
       for (long i = 0; i < kRtSpin && !landed; ++i) landed = mbar_try_wait(b, (uint32_t)(ch & 1));
-      if (!landed && round == 0 && tid == 0 && a.s.err) atomicExch(a.s.err, 2);
+      if (!landed && round == 0 && tid == 0 && a.s.err) atomicOr(a.s.err, 2);
     }
     if (ch == 0) {
       // unit-gain RMSNorm of the layer input (PW_PRENORM): one warp per staged token
@@ -286,8 +286,14 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
           const float inv = s_inv[t];
           const uint32_t r[4] = {raw.x, raw.y, raw.z, raw.w};
           uint32_t o[4];
+          bool fin = true;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) o[i] = pack2(f2h(bf16f(r[i]) * inv), f2h(bf16f(r[i] >> 16) * inv));
+          for (int i = 0; i < 4; ++i) {
+            const float lo = bf16f(r[i]) * inv, hi = bf16f(r[i] >> 16) * inv;
+            fin = fin && fp16_finite(lo) && fp16_finite(hi);
+            o[i] = pack2(f2h(lo), f2h(hi));
+          }
+          if (!fin && a.s.err) atomicOr(a.s.err, kErrRange);
           *reinterpret_cast<uint4 *>(a.s.xh + (size_t)(t0 + t) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }

@@ -50,7 +50,8 @@ def parse():
     ap.add_argument("--gemv-tokens", type=int, default=None,
                     help="routed work items of at most this many tokens run on the CUDA cores (default: the library's)")
     ap.add_argument("--paging", action="store_true",
-                    help="dynamic paging run: a free-KV-block trace drives the planner, offload and reload every step")
+                    help="dynamic paging run: a request schedule served by the KV-block allocator drives the planner, "
+                         "offload and reload every step")
     return ap.parse_args()
 
 
@@ -275,55 +276,106 @@ def run_reference(args, shape, L, T):
     print(json.dumps(line), flush=True)
 
 
+def serve_requests(pw, kv, events, dropped):
+    """Apply one step of the request schedule to the KV-block allocator; a request whose
+    arrival or growth does not fit is dropped (its blocks released, its later events
+    skipped)."""
+    for ev in events:
+        kind, r = ev[0], ev[1]
+        if r in dropped:
+            continue
+        if kind == "finish":
+            pw.pw_kv_release(kv, r)
+        elif kind == "announce":
+            pw.pw_kv_announce(kv, r, ev[2])
+        else:
+            try:
+                pw.pw_kv_grow(kv, r, ev[2])
+            except pw.PwError as e:
+                if e.status != pw.PW_ERR_OOM:
+                    raise
+                dropped.add(r)
+                pw.pw_kv_release(kv, r)
+
+
 def run_paging(args, pw, torch, ctx, shape, L, T, stream, x0, xw, clocks_cls):
-    """PagedWeight Sec. 3.2-3.3 in the loop: per decode step the planner (Eqs. 3-8) reads the
-    trace's free KV blocks, its plan is applied with offload / reload on the side stream,
-    landed reloads are committed, then the stack runs.  Timed end to end on the host (the
-    planner and the page I/O calls are part of the step) and on the device."""
+    """PagedWeight Sec. 3.2-3.3 in the loop: per decode step a seeded request schedule
+    (arrivals, growth announced a step ahead, completions) is served by the KV-block
+    allocator attached to the context, which shares one device budget with the weight
+    pages; the planner (Eqs. 3-8) reads the allocator's free KV blocks, its plan is applied
+    with offload / reload on the side stream, landed transfers are committed (retired pages
+    become KV headroom), then the stack runs.  Timed end to end on the host (the serving
+    loop, the planner and the page I/O calls are part of the step) and on the device."""
     steps = 200
-    trace = syn.kv_free_block_trace(steps)
+    schedule = syn.gen_kv_requests(steps, args.seed)
     n_blocks = L * shape.E * 2
     off = syn.gen_planner_offline_np(n_blocks, list(shape.bits), 4, args.seed)
     off["n_stages"] = 3
-    B_KV = 2.0 * 1024 * 1024
+    T_blk, R = 16, 8
     start = pw.pw_memory(ctx).resident_bytes
+    held0 = pw.pw_memory(ctx).held_bytes
+    live, peak = {}, 0  # the schedule's demand peak in blocks
+    for events in schedule:
+        for ev in events:
+            if ev[0] == "finish":
+                live.pop(ev[1])
+            elif ev[0] in ("arrive", "grow"):
+                live[ev[1]] = live.get(ev[1], 0) + ev[2]
+        peak = max(peak, sum(live.values()))
+    B_KV = int(0.3 * held0 / peak)            # the peak asks for 30% of the weight bytes
+    S = held0 + (T_blk + R) * B_KV            # and the budget starts with T_blk + R free blocks
+    kv = pw.pw_kv_create(S, B_KV)
+    pw.pw_kv_attach(kv, ctx)
+    dropped = set()
     moved = {"offload": 0.0, "reload": 0.0}
     applied = 0
     kinds = {0: 0, 1: 0, 2: 0}
-    resident = []
+    resident, free_blk, used = [], [], []
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     clocks = clocks_cls(int(os.environ.get("LOCAL_RANK", "0")))
     clocks.start()
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for step in range(steps):
-            obs = dict(T_blk=16, F_blk=int(trace[step]), B_KV=B_KV, R=8, mass=None,
-                       phi=syn.gen_phi_np(n_blocks, args.seed, step))
-            plan = pw.pw_plan_step(ctx, n_blocks, obs, off)
-            kinds[plan["kind"]] += 1
-            applied += len(plan["entries"])
-            for block, fb, tb, delta in plan["entries"]:
-                if tb < fb:
-                    pw.pw_offload(ctx, block, tb)
-                    moved["offload"] += delta
-                else:
-                    pw.pw_reload(ctx, block, tb)
-                    moved["reload"] += delta
-            pw.pw_commit(ctx)
-            xw.copy_(x0)
-            pw.pw_stack_forward(ctx, xw, T, stream)
-            resident.append(pw.pw_memory(ctx).resident_bytes)
-        ev1.record(stream)
-    stream.synchronize()
-    wall = time.perf_counter() - t0
-    clk = clocks.stop()
-    dev_ms = ev0.elapsed_time(ev1)
-    pw.pw_sync_io(ctx)
+    try:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for step in range(steps):
+                serve_requests(pw, kv, schedule[step], dropped)
+                st = pw.pw_kv_get_stats(kv)
+                obs = dict(T_blk=T_blk, F_blk=int(st["free_blocks"]), B_KV=float(B_KV), R=R, mass=None,
+                           phi=syn.gen_phi_np(n_blocks, args.seed, step))
+                plan = pw.pw_plan_step(ctx, n_blocks, obs, off)
+                kinds[plan["kind"]] += 1
+                applied += len(plan["entries"])
+                for block, fb, tb, delta in plan["entries"]:
+                    if tb < fb:
+                        pw.pw_offload(ctx, block, tb)
+                        moved["offload"] += delta
+                    else:
+                        pw.pw_reload(ctx, block, tb)
+                        moved["reload"] += delta
+                pw.pw_commit(ctx)
+                xw.copy_(x0)
+                pw.pw_stack_forward(ctx, xw, T, stream)
+                resident.append(pw.pw_memory(ctx).resident_bytes)
+                free_blk.append(int(st["free_blocks"]))
+                used.append(int(st["used_blocks"]))
+            ev1.record(stream)
+        stream.synchronize()
+        wall = time.perf_counter() - t0
+        clk = clocks.stop()
+        dev_ms = ev0.elapsed_time(ev1)
+        pw.pw_sync_io(ctx)
+    finally:
+        pw.pw_kv_destroy(kv)
+    n_req = len({ev[1] for events in schedule for ev in events})
     return {
-        "steps": steps, "trace": "F_blk(t) = round(32 + 32 cos(2 pi t / 200)), T_blk = 16, R = 8, B_KV = 2 MiB",
+        "steps": steps,
+        "kv": {"source": "pw_kv allocator attached to the context (F_blk read every step)",
+               "schedule": f"gen_kv_requests(200, seed={args.seed}): {n_req} requests, demand peak {peak} blocks",
+               "budget_bytes": S, "block_bytes": B_KV, "T_blk": T_blk, "R": R, "dropped_requests": len(dropped),
+               "F_blk": {"min": min(free_blk), "max": max(free_blk)}, "used_blocks_max": max(used)},
         "host_ms_per_step": wall * 1e3 / steps, "device_ms_per_step": dev_ms / steps,
         "tokens_per_s": T * L * steps / wall, "plans": {"none": kinds[0], "offload": kinds[1], "reload": kinds[2]},
         "offloaded_bytes": moved["offload"], "reloaded_bytes": moved["reload"],
@@ -474,7 +526,7 @@ def run_ours(args, shape, L, T):
                 "steps": res["steps"], "warmup": max(args.warmup, 3), "ms_per_step": res["host_ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
                 "config": dict(workload_config(shape, T, L), workload=f"{shape.name}-shaped MoE stack decode with "
-                               f"dynamic paging: {L} layers, T={T}, 200 steps"),
+                               f"dynamic paging driven by the KV-block allocator: {L} layers, T={T}, 200 steps"),
                 "static_ms_per_step": static_ms, "paging": res, "clocks": res["clocks"],
                 "gpu_launches": res["gpu_launches"]}
         pw.pw_destroy(ctx)

@@ -46,7 +46,8 @@ typedef enum {
     PW_ERR_OOM = 3,     /* device or pinned-host memory exhausted: nothing was changed */
     PW_ERR_STATE = 4,   /* the page state forbids the request (e.g. a page in transfer) */
     PW_ERR_TIMEOUT = 5, /* a bounded device wait gave up */
-    PW_ERR_BUSY = 6     /* an earlier transfer of the same block has not landed yet */
+    PW_ERR_BUSY = 6,    /* an earlier transfer of the same block has not landed yet */
+    PW_ERR_RANGE = 7    /* an fp16 activation overflowed or an output is not finite */
 } pw_status;
 
 typedef struct pw_ctx pw_ctx;
@@ -148,14 +149,17 @@ pw_status pw_set_shared_gate(pw_ctx *ctx, int layer, const float *wsg);
  *   y may equal x).  ids (int32 [T][K]) and w (fp32 [T][K]) are optional device
  *   outputs (NULL to skip).  1 <= T <= max_tokens.  Asynchronous on `stream`; no host
  *   synchronisation and no allocation, so it can be captured in a CUDA graph.
- * Activations are handled in fp16 inside the expert kernels: |x| and |h| must stay
- * below 65504. */
+ * Activations are handled in fp16 inside the expert kernels: |x| (after the RMS norm under
+ * PW_PRENORM) and |h| must stay below 65504.  A value that rounds past it (or a NaN), and a
+ * y that is not finite, set a flag in the context that pw_check reports as PW_ERR_RANGE. */
 pw_status pw_moe_forward(pw_ctx *ctx, int layer, const void *x, int T, void *y,
                          int32_t *ids, float *w, int flags, pw_stream stream);
 
 /* Wait for the compute stream and report whether a bounded wait inside an expert kernel
- * expired since the last check (PW_ERR_TIMEOUT; the outputs of that launch are invalid).
- * Also reports sticky CUDA errors.  No counterpart in the paper: the fused kernel of
+ * expired since the last check (PW_ERR_TIMEOUT; the outputs of that launch are invalid),
+ * else whether an fp16 activation (x as the experts read it, or h) overflowed or a y came out
+ * infinite or NaN (PW_ERR_RANGE; the outputs since the last check are invalid).  Both
+ * flags are cleared by the call.  Also reports sticky CUDA errors.  No counterpart in the paper: the fused kernel of
  * Sec. 3.3 synchronises its warps on device barriers, and this library bounds every such
  * wait and reports the ones that gave up here. */
 pw_status pw_check(pw_ctx *ctx);

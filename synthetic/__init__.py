@@ -19,7 +19,7 @@ from .gen import (  # noqa: F401
     gen_phi_np,
     gen_q_assignment,
     gen_planner_offline_np,
-    kv_free_block_trace,
+    gen_kv_requests,
     zipf_log_prior,
     GATE_UP,
     DOWN,

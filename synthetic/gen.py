@@ -96,7 +96,7 @@ def f32_from_bf16_bits(b: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- blocks
-TAG_IDX, TAG_LUT, TAG_ROUTER, TAG_TOK, TAG_SHARED, TAG_Q, TAG_PLAN = 1, 2, 3, 4, 5, 6, 7
+TAG_IDX, TAG_LUT, TAG_ROUTER, TAG_TOK, TAG_SHARED, TAG_Q, TAG_PLAN, TAG_KV = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def gen_block_np(shape: LayerShape, seed: int, layer: int, expert: int, u: int):
@@ -209,7 +209,32 @@ def gen_phi_np(n_blocks: int, seed: int, step: int) -> np.ndarray:
     return np.abs(r.normal(1.0, 0.5, size=(n_blocks, 3)))
 
 
-def kv_free_block_trace(steps: int = 200):
-    """Free KV blocks per decode step: 32 + 32 cos(2 pi t / steps), rounded (64 -> 0 -> 64)."""
-    t = np.arange(steps)
-    return np.rint(32.0 + 32.0 * np.cos(2.0 * np.pi * t / steps)).astype(np.int64)
+def gen_kv_requests(steps: int, seed: int, scale: int = 1, arrive_until: float = 0.7):
+    """A decode-serving request schedule, per step a list of events in the order they are
+    applied: ("finish", r), ("arrive", r, n) with n blocks of prompt KV, ("grow", r, n) and
+    ("announce", r, n) -- n blocks the request expects to need at its next growth.
+
+    Arrivals: one request with probability 0.9 sin^2(pi t / (arrive_until * steps)) at step
+    t < arrive_until * steps, none later, so that the live KV demand rises, peaks and drains.
+    A request (id = its arrival step) lives 20..50 steps, brings 2..6 prompt blocks and
+    grows by one block every 2..4 steps, announcing each growth one step ahead; block
+    counts are multiplied by `scale`.  The schedule does not depend on whether an event
+    succeeds: a serving loop that cannot grant a request drops that request's later events."""
+    r = _rng(seed, TAG_KV, 0)
+    events = [[] for _ in range(steps)]
+    last = int(arrive_until * steps)
+    for t in range(last):
+        u, life, prompt, every = r.random(), int(r.integers(20, 51)), int(r.integers(2, 7)), int(r.integers(2, 5))
+        if u >= 0.9 * math.sin(math.pi * t / last) ** 2:
+            continue
+        prompt *= scale
+        events[t].append(("arrive", t, prompt))
+        end = min(steps - 1, t + life)
+        for s in range(t + 1, end):
+            if (s - t) % every == 0:
+                events[s].append(("grow", t, scale))
+            if (s + 1 - t) % every == 0 and s + 1 < end:
+                events[s].append(("announce", t, scale))
+        if t + life < steps:
+            events[end].insert(0, ("finish", t))
+    return events

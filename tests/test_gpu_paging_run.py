@@ -1,21 +1,26 @@
-"""The dynamic paging run (PagedWeight Sec. 3.2 and Sec. 3.3, Fig. 4) on the device: a
-synthetic free-KV-block trace F_blk(t) = round(32 + 32 cos(2 pi t / 200)) drives the greedy
-planner (Eqs. 3-8, Algorithm 1) for 200 decode steps of 64 tokens; every plan is applied with
-pw_offload / pw_reload on the side stream and pw_commit between steps, retired device pages
-are poisoned with 0xFF, and at EVERY step every layer's output is compared with the float64
-oracle run at that step's committed bitwidths.
+"""The dynamic paging run (PagedWeight Sec. 3.2 and Sec. 3.3, Fig. 4) on the device, its KV
+pressure coming from a running KV-block allocator: a seeded request schedule (arrivals with
+prompt blocks, growth one block at a time, each growth announced a step ahead, completions)
+is served by ``pw_kv`` attached to the context, so the weight pages the GPU holds and the KV
+blocks share one budget.  Every step the greedy planner (Eqs. 3-8, Algorithm 1) reads F_blk
+from the allocator, the plan is applied with pw_offload / pw_reload on the side stream and
+pw_commit between steps (retired pages become KV headroom), retired device pages are
+poisoned with 0xFF, and at EVERY step every layer's output is compared with the float64
+oracle at that step's committed bitwidths; the allocator's accounting is checked against the
+oracle's (oracle/kv.py) at every step too.
 
 The layers have the structure of the Qwen1.5-MoE-shaped stack (60 routed experts, top-4,
 hot/cold bitwidths under a Zipf(1.1) router prior, a dense shared expert, bits 3..8) at
-reduced widths, so that the oracle can check all 200 steps; the KV block size is scaled
-with the weight bytes so that the pressure phase of the trace pushes blocks to their floors
-and the recovery phase restores them.  A second test runs the trace on full-size
-Qwen-shaped layers and checks the oracle at a handful of steps."""
+reduced widths, so that the oracle can check all 200 steps; the KV block size is scaled with
+the weight bytes so that the demand peak pushes blocks toward their floors and the drain
+restores them.  A second test serves the schedule on full-size Qwen-shaped layers and checks
+the oracle at a handful of steps."""
 import numpy as np
 import pytest
 
 import synthetic as syn
 from oracle import ap
+from oracle import kv as okv
 from oracle import moe as omoe
 from oracle import planner as opl
 
@@ -174,35 +179,97 @@ def oracle_plan(st, off, obs):
     return (2 if total > 0 else 0), -1, D, [(idle[i], a, b, d) for i, (a, b, d) in plan.items()]
 
 
-def run_trace(st, off, B_KV, check_steps, check_layers, check_tokens=None, check_plans=False):
-    trace = syn.kv_free_block_trace(STEPS)
+class Serving:
+    """The request side of a serving loop on two allocators in step: the library's (attached
+    to the context, so its weight bytes are the pages the context holds) and the oracle's
+    accounting, given the same held bytes.  A request whose arrival or growth does not fit
+    is dropped (its blocks are released and its later events skipped)."""
+
+    def __init__(self, st, S, B):
+        self.ctx = st.ctx
+        self.kv = pw.pw_kv_create(S, B)
+        pw.pw_kv_attach(self.kv, st.ctx)
+        self.ref = okv.KVAllocator(S, B)
+        self.dropped = set()
+
+    def close(self):
+        pw.pw_kv_destroy(self.kv)
+
+    def sync_weights(self):
+        self.ref.set_weight_bytes(pw.pw_memory(self.ctx).held_bytes)
+
+    def apply(self, events):
+        self.sync_weights()
+        for ev in events:
+            kind, r = ev[0], ev[1]
+            if r in self.dropped:
+                continue
+            if kind == "finish":
+                assert pw.pw_kv_release(self.kv, r) == self.ref.release(r)
+            elif kind == "announce":
+                pw.pw_kv_announce(self.kv, r, ev[2])
+                self.ref.announce(r, ev[2])
+            else:  # arrive / grow
+                try:
+                    want = self.ref.grow(r, ev[2])
+                except okv.KVError:
+                    want = None
+                try:
+                    got = [int(i) for i in pw.pw_kv_grow(self.kv, r, ev[2])]
+                except pw.PwError as e:
+                    assert e.status == pw.PW_ERR_OOM
+                    got = None
+                assert got == want, (kind, r)
+                if got is None:
+                    self.dropped.add(r)
+                    pw.pw_kv_release(self.kv, r)
+                    self.ref.release(r)
+        return self.stats()
+
+    def stats(self):
+        self.sync_weights()
+        got = pw.pw_kv_get_stats(self.kv)
+        assert got == self.ref.stats()
+        return got
+
+
+def run_requests(st, off, S, B, check_steps, check_layers, check_tokens=None, check_plans=False):
+    schedule = syn.gen_kv_requests(STEPS, st.seed)
+    srv = Serving(st, S, B)
     log = []
-    for step in range(STEPS):
-        obs = dict(T_blk=T_BLK, F_blk=int(trace[step]), B_KV=B_KV, R=R, mass=None,
-                   phi=syn.gen_phi_np(st.n_blocks, st.seed, step))
-        if check_plans:
-            pw.pw_set_fault(st.ctx, 3, 1)  # hold: no transfer is observed landing until the plan is compared
-            want = oracle_plan(st, off, obs)
-        plan = pw.pw_plan_step(st.ctx, st.n_blocks, obs, off)
-        if check_plans:
-            pw.pw_set_fault(st.ctx, 3, 0)
-            assert (plan["kind"], plan["stage"], plan["D"]) == want[:3], f"step {step}"
-            assert plan["entries"] == want[3], f"step {step}"
-        for block, fb, tb, _ in plan["entries"]:
-            if tb < fb:
-                pw.pw_offload(st.ctx, block, tb)
-            else:
-                pw.pw_reload(st.ctx, block, tb)
-        pw.pw_commit(st.ctx)  # reloads that have landed raise q now, between launches
-        for l in range(st.L):
-            x = st.tokens(step, l)
-            y = st.forward(l, x)
-            if step in check_steps and l in check_layers:
-                q = st.committed_q(l)
-                rows = np.arange(T) if check_tokens is None else (np.arange(check_tokens) + 5 * step) % T
-                assert_close(y[rows], st.oracle(l, x[rows], q), f"step {step} layer {l}")
-        log.append((step, plan["kind"], len(plan["entries"]), pw.pw_memory(st.ctx).resident_bytes))
-    return log
+    try:
+        for step in range(STEPS):
+            F = srv.apply(schedule[step])["free_blocks"]
+            obs = dict(T_blk=T_BLK, F_blk=int(F), B_KV=float(B), R=R, mass=None,
+                       phi=syn.gen_phi_np(st.n_blocks, st.seed, step))
+            if check_plans:
+                pw.pw_set_fault(st.ctx, 3, 1)  # hold: no transfer is observed landing until the plan is compared
+                want = oracle_plan(st, off, obs)
+            plan = pw.pw_plan_step(st.ctx, st.n_blocks, obs, off)
+            if check_plans:
+                pw.pw_set_fault(st.ctx, 3, 0)
+                assert (plan["kind"], plan["stage"], plan["D"]) == want[:3], f"step {step}"
+                assert plan["entries"] == want[3], f"step {step}"
+            for block, fb, tb, _ in plan["entries"]:
+                if tb < fb:
+                    pw.pw_offload(st.ctx, block, tb)
+                else:
+                    pw.pw_reload(st.ctx, block, tb)
+            pw.pw_commit(st.ctx)  # landed offloads retire their pages (KV headroom), landed reloads raise q
+            for l in range(st.L):
+                x = st.tokens(step, l)
+                y = st.forward(l, x)
+                if step in check_steps and l in check_layers:
+                    q = st.committed_q(l)
+                    rows = np.arange(T) if check_tokens is None else (np.arange(check_tokens) + 5 * step) % T
+                    assert_close(y[rows], st.oracle(l, x[rows], q), f"step {step} layer {l}")
+            kv = srv.stats()
+            log.append(dict(step=step, kind=plan["kind"], n=len(plan["entries"]), F_blk=int(F),
+                            resident=pw.pw_memory(st.ctx).resident_bytes, used=kv["used_blocks"],
+                            free_after=kv["free_blocks"]))
+    finally:
+        srv.close()
+    return log, srv.dropped
 
 
 def offline_inputs(st):
@@ -211,24 +278,39 @@ def offline_inputs(st):
     return off
 
 
+def budget(st, peak_frac):
+    """Block size and budget: the schedule's demand peak asks for peak_frac of the resident
+    weight bytes, and the budget leaves T_blk + R free blocks over the packed weights."""
+    start = pw.pw_memory(st.ctx).held_bytes
+    live, peak = {}, 0
+    for events in syn.gen_kv_requests(STEPS, st.seed):
+        for ev in events:
+            if ev[0] == "finish":
+                live.pop(ev[1])
+            elif ev[0] in ("arrive", "grow"):
+                live[ev[1]] = live.get(ev[1], 0) + ev[2]
+        peak = max(peak, sum(live.values()))
+    B = int(peak_frac * start / peak)
+    return start + (T_BLK + R) * B, B
+
+
 def test_paging_run_every_step_matches_oracle():
     st = Stack(MINI, L=MINI.L)
     try:
         start = st.resident_bytes_eq3()
         assert pw.pw_memory(st.ctx).resident_bytes == start
-        # KV block size: the whole pressure phase asks for about half the resident bytes
-        trace = syn.kv_free_block_trace(STEPS)
-        demand = sum(max(0, T_BLK - int(f) + 1) for f in trace)
-        B_KV = 0.5 * start / demand
-        log = run_trace(st, offline_inputs(st), B_KV, check_steps=set(range(STEPS)), check_layers=range(st.L),
-                        check_plans=True)
+        S, B = budget(st, 0.3)
+        log, dropped = run_requests(st, offline_inputs(st), S, B, check_steps=set(range(STEPS)),
+                                    check_layers=range(st.L), check_plans=True)
         pw.pw_sync_io(st.ctx)
         pw.pw_commit(st.ctx)
-        kinds = [k for _, k, _, _ in log]
-        resident = [r for _, _, _, r in log]
+        kinds = [r["kind"] for r in log]
+        resident = [r["resident"] for r in log]
         assert 1 in kinds and 2 in kinds          # both offload and reload plans were applied
-        assert min(resident) < 0.75 * start       # the pressure phase freed weight pages
-        assert resident[-1] > min(resident)       # and the recovery phase brought some back
+        assert min(resident) < 0.8 * start        # the demand peak freed weight pages
+        assert resident[-1] > min(resident)       # and the drain brought some back
+        assert max(r["used"] for r in log) > 2 * (T_BLK + R)  # the KV blocks took the freed bytes
+        assert len(dropped) < 0.25 * len({ev[1] for evs in syn.gen_kv_requests(STEPS, st.seed) for ev in evs})
         assert pw.pw_memory(st.ctx).resident_bytes == st.resident_bytes_eq3()
         for l in range(st.L):                     # never above the packed bitwidths
             assert np.all(st.committed_q(l) <= st.layers[l]["q0"])
@@ -240,9 +322,10 @@ def test_paging_run_full_size_spot_checks():
     shape = syn.SHAPES["qwen"]
     st = Stack(shape, L=2)
     try:
-        B_KV = 2.0 * 1024 * 1024 * 2 / shape.L  # 2 MiB per KV block, scaled to 2 of the 24 layers
-        log = run_trace(st, offline_inputs(st), B_KV, check_steps={0, 100, 199}, check_layers={0}, check_tokens=3)
-        assert any(k == 1 for _, k, _, _ in log)
+        S, B = budget(st, 0.3)
+        log, _ = run_requests(st, offline_inputs(st), S, B, check_steps={0, 100, 199}, check_layers={0},
+                              check_tokens=3)
+        assert any(r["kind"] == 1 for r in log)
         pw.pw_sync_io(st.ctx)
         pw.pw_commit(st.ctx)
         assert pw.pw_memory(st.ctx).resident_bytes == st.resident_bytes_eq3()

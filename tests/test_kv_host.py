@@ -258,3 +258,35 @@ def test_batch_merge_weighted_by_the_allocator():
             assert np.array_equal(np.asarray(got[key]), np.asarray(want[key])), key
     finally:
         lib.close()
+
+
+def test_request_schedule_is_well_formed():
+    """The seeded serving schedule that drives the paging run: each request arrives once (at
+    the step that is its id), every growth was announced the step before, nothing follows a
+    finish, and the live demand rises from zero, peaks and drains."""
+    from synthetic import gen_kv_requests
+    steps = 200
+    sched = gen_kv_requests(steps, 0)
+    seen, done, announced, live, demand = set(), set(), {}, {}, []
+    for t, events in enumerate(sched):
+        for ev in events:
+            kind, r = ev[0], ev[1]
+            assert r not in done
+            if kind == "arrive":
+                assert r == t and r not in seen
+                seen.add(r)
+                live[r] = ev[2]
+            elif kind == "finish":
+                assert r in seen
+                done.add(r)
+                live.pop(r)
+            elif kind == "announce":
+                assert r in seen
+                announced[r] = (t, ev[2])
+            else:
+                assert kind == "grow" and announced.get(r) == (t - 1, ev[2])
+                live[r] += ev[2]
+        demand.append(sum(live.values()))
+    assert len(seen) > 30 and demand[0] == 0
+    peak = int(np.argmax(demand))
+    assert 0.3 * steps < peak < 0.7 * steps and demand[-1] < 0.2 * demand[peak]
