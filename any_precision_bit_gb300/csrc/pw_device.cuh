@@ -112,6 +112,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // completed and their memory is visible (returns at once for a launch without a
 // programmatic dependency).  pdl_trigger: let the next grid of the stream be scheduled now;
 // it still waits in its own pdl_wait for this one to complete.
+// Order this thread's generic-proxy global writes (or what it has observed of other threads')
+// before later tensor-copy (async-proxy) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;\n" ::: "memory");
+}
+// Load with acquire semantics at GPU scope.
+__device__ __forceinline__ int ld_acquire_gpu(const int *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 

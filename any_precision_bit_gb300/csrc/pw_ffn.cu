@@ -258,6 +258,26 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   atomicOr(err, 1);
   return false;
 }
+// Bounded wait for the router to have written this layer's fp16 input rows (every router CTA
+// counted in `ready`); false on expiry or when another warp gave up.  The gate_up kernel's
+// shared-expert items read only those rows, so they start on this instead of on the end of
+// the routing.
+__device__ __forceinline__ bool wait_ready(const FwdArgs &a, volatile int *abort_flag) {
+  if (!a.s.ready) return true;
+  const int *p = a.s.ready + a.layer;
+  const int target = route_ctas(a.T, a.E);
+  if (ld_acquire_gpu(p) >= target) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    __nanosleep(200);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > s_wait_cycles) break;
+  }
+  *abort_flag = 1;
+  atomicOr(a.s.err, 1);
+  return false;
+}
 // Wait that ignores the abort flag (used to drain what this thread issued); bounded.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
@@ -332,7 +352,11 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
   const int S = L.slabs;
-  const int n_items = a.s.n_items[PHASE - 1];
+  // gate_up: the shared expert's items (the first n_shared) need only the layer's input rows
+  // and are built here; the routed ones, the item count and the list wait for the routing
+  const int n_shared = PHASE == 1 ? shared_item_count(0, a.T, a.H, a.I, a.Is) : 0;
+  int n_items = PHASE == 1 ? 0 : a.s.n_items[PHASE - 1];
+  bool routed_ready = PHASE != 1;
   RingPos pos;
   // room accounting (the same in every lane); the chunks in flight are kept across the
   // lanes: lane i holds chunk c with c % kRing == i (its slab count, landed barrier and the
@@ -348,14 +372,24 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
     QEntry &e = qu.slot[k % kQueue];
     if (lane == 0) {
       ok = wait_bar(qu.bars + 8 * (kIQE + k % kQueue), ((k / kQueue) & 1) ^ 1, abort_flag, a.s.err);
+      if (ok && PHASE == 1 && k == 0) ok = wait_ready(a, abort_flag);
       if (ok) {
         it = atomicAdd(a.s.work + (PHASE - 1), 1);
-        if (it >= n_items) it = -1;
-        e.it = it;
-        if (it >= 0) {
-          e.w = items[it];
-          e.v = view_item<PHASE>(a, e.w);
+        if (it < n_shared) {
+          e.w = work_item(0, it, &n_shared, nullptr, nullptr, a.E, a.T, a.H, a.I, a.Is);
+        } else {
+          if (!routed_ready) {  // the router and the gather kernel have completed
+            pdl_wait();
+            n_items = a.s.n_items[0];
+            routed_ready = true;
+          }
+          if (it >= n_items)
+            it = -1;
+          else
+            e.w = items[it];
         }
+        e.it = it;
+        if (it >= 0) e.v = view_item<PHASE>(a, e.w);
         mbar_arrive(qu.bars + 8 * (kIQF + k % kQueue));
       }
     }
@@ -475,10 +509,26 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
   const uint32_t gx = smem_u32(sm) + (uint32_t)L.gx_off;
   uint32_t b_seq = 0, a_seq = 0, gx_seq[kGxSlots] = {0u, 0u, 0u, 0u};
   bool ok = true;
+  // gate_up: the input rows are the router's (counted ready), the routed rows the gather
+  // kernel's (complete at the end of the grid dependency); the tensor copies of every lane
+  // are ordered after what lane 0 observed
+  bool xh_ready = PHASE != 1, xs_ready = PHASE != 1;
   for (uint32_t k = 0; ok; ++k) {
     WorkItem w;
     ItemView v;
     if (!queue_read(qu, k, 0xffffffffu, abort_flag, a.s.err, w, v)) break;
+    if (!(v.routed ? xs_ready : xh_ready)) {
+      if (v.routed) {
+        pdl_wait();
+        xs_ready = true;
+      } else {
+        if (lane == 0) ok = wait_ready(a, abort_flag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        xh_ready = true;
+      }
+      fence_proxy_async_global();
+    }
     if (GV && v.gemv) {  // one 8-row box of 128 columns per chunk into its stream's GEMV slot
       const TmaDesc *map = PHASE == 1 ? &bm.gemv.xs : &bm.gemv.h_routed;
       for (int kc = w.kc0; kc < w.kc1; ++kc) {
@@ -1007,9 +1057,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   __syncthreads();
   tc_fence_after();
   // set up before the previous kernel of the stream has finished; its outputs (work items,
-  // activations) are read only after this
+  // activations) are read only after this.  gate_up waits per role: the shared expert's items
+  // on the router's input rows, the routed items on the completed grid dependency.
   pdl_trigger();
-  pdl_wait();
+  if (PHASE == 2) {
+    pdl_wait();
+    // the layer's gate_up kernel has completed: its item counter and ready count start over
+    // for the next layer (whose router runs after this kernel has completed)
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      a.s.work[0] = 0;
+      if (a.s.ready) a.s.ready[a.layer] = 0;
+    }
+  }
   const uint32_t tmem = tmem_slot;
   const ItemQueue qu{queue_slot, bars};
   if (warp < kDq)

@@ -34,6 +34,11 @@ constexpr int kPrefillMinT = 512;      // batches of at least this many tokens u
 // weight tile is dequantised when experts see hundreds of tokens.
 PW_HD int tok_chunk_for(int T) { return T >= kPrefillMinT ? kTokChunkPrefill : kTokChunk; }
 
+constexpr int kRtTok = 8;  // tokens per router CTA (one warp each in top-K)
+constexpr int kRtExp = 8;  // experts per router CTA (one warp each for the logits)
+// CTAs of a router launch: (token groups) x (expert groups).
+PW_HD int route_ctas(int T, int E) { return ((T + kRtTok - 1) / kRtTok) * ((E + kRtExp - 1) / kRtExp); }
+
 // One row of the device weight page table (PagedWeight Sec. 3.1).  The kernels read q and
 // the pointers of the block they run; commits rewrite the whole row between launches.
 struct BlockDev {
@@ -98,6 +103,14 @@ constexpr int kRankStride = 257;
 // chunks of a row tile consecutive, so that CTAs claiming them together share the tile's
 // planes in L2; for the down projection each (row tile, K part) has its slot chunks
 // consecutive, the parts of a tile one after the other.
+// Number of the shared expert's work items of projection u (they lead both lists).
+PW_HD int shared_item_count(int u, int T, int H, int I, int Is) {
+  if (Is <= 0) return 0;
+  const int tc = tok_chunk_for(T), tchunks = (T + tc - 1) / tc;
+  return u == 0 ? ((2 * Is + kCtaRows - 1) / kCtaRows) * tchunks
+                : ((H + kCtaRows - 1) / kCtaRows) * tchunks * shared_down_splits(I, Is);
+}
+
 PW_HD WorkItem work_item(int u, int i, const int *first, const int *rk, const int *off, int E, int T, int H,
                          int I, int Is) {
   const int tc = tok_chunk_for(T), tchunks = (T + tc - 1) / tc;
@@ -272,6 +285,9 @@ struct Scratch {
   WorkItem *items2;    // down work
   int *n_items;        // [2]
   unsigned *ticket;    // [1 + ceil(Tm/8)] router last-CTA counters: all token groups, then per group
+  int *ready;          // [L] router CTAs that have written layer l's fp16 input rows; the layer's
+                       // gate_up kernel starts the shared expert's items once all have (the
+                       // layer's down kernel resets it); NULL: not counted
   uint16_t *xh;        // fp16 [Tm][H]: the layer input as the experts read it (normalised under PW_PRENORM)
   uint16_t *xs;        // fp16 [Tm*K][H]: xh rows in expert-sorted slot order
   uint16_t *h_routed;  // fp16 [Tm*K][I]

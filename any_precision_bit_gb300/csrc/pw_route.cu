@@ -25,8 +25,6 @@
 
 namespace pw {
 
-constexpr int kRtTok = 8;   // tokens per router CTA (one warp each in top-K)
-constexpr int kRtExp = 8;   // experts per router CTA (one warp each for the logits)
 constexpr int kRtThreads = 256;
 constexpr int kRtWarps = kRtThreads / 32;
 constexpr int kRtStageBytes = 96 * 1024;  // token rows + one column chunk of the router rows
@@ -296,6 +294,12 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
           if (!fin && a.s.err) atomicOr(a.s.err, kErrRange);
           *reinterpret_cast<uint4 *>(a.s.xh + (size_t)(t0 + t) * H + c) = make_uint4(o[0], o[1], o[2], o[3]);
         }
+        if (a.s.ready) {  // publish the slice: the gate_up kernel reads it with tensor copies
+          fence_proxy_async_global();
+          __threadfence();
+          __syncthreads();
+          if (tid == 0) atomicAdd(a.s.ready + a.layer, 1);
+        }
       }
     }
     if (warp < ne) {
@@ -430,8 +434,8 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   const int tc = tok_chunk_for(T);
   const int tchunks = (T + tc - 1) / tc;
   const int nsplit = shared_down_splits(a.I, a.Is);
-  const int sh1 = a.Is > 0 ? ((2 * a.Is + kCtaRows - 1) / kCtaRows) * tchunks : 0;
-  const int sh2 = a.Is > 0 ? tiles2 * tchunks * nsplit : 0;
+  const int sh1 = shared_item_count(0, T, a.H, a.I, a.Is);
+  const int sh2 = shared_item_count(1, T, a.H, a.I, a.Is);
   {
     int cnt = 0;
     if (tid < E)
@@ -564,10 +568,8 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   }
   if (tid == 0) {
     *a.s.ticket = 0u;
-    if (a.s.work) {  // the expert kernels that follow claim their work items from zero
-      a.s.work[0] = 0;
-      a.s.work[1] = 0;
-    }
+    if (a.s.work) a.s.work[1] = 0;  // the down kernel claims its work items from zero (the
+                                    // gate_up counter is reset by the previous down kernel)
   }
 }
 
