@@ -413,7 +413,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
             salloc((void **)&c->s.stat_phi, sizeof(double) * 4 * d.L * d.E) &&
             salloc((void **)&c->s.xh, sizeof(uint16_t) * Tm * d.H) &&
             salloc((void **)&c->s.err, sizeof(int)) && salloc((void **)&c->s.work, sizeof(int) * 2) &&
-            salloc((void **)&c->s.ready, sizeof(int) * d.L) &&
+            salloc((void **)&c->s.ready, sizeof(int) * 2 * d.L) &&
             salloc((void **)&c->s.stat_count, sizeof(double) * d.L * d.E) &&
             salloc((void **)&c->s.stat_wsum, sizeof(double) * d.L * d.E) &&
             salloc(&c->xdev, sizeof(uint16_t) * Tm * d.H);
@@ -442,7 +442,7 @@ pw_status pw_create(const pw_desc *desc, pw_ctx **out) {
   cudaMemset(c->s.ticket, 0, sizeof(unsigned) * (1 + (Tm + 7) / 8));
   cudaMemset(c->s.err, 0, sizeof(int));
   cudaMemset(c->s.work, 0, sizeof(int) * 2);
-  cudaMemset(c->s.ready, 0, sizeof(int) * d.L);
+  cudaMemset(c->s.ready, 0, sizeof(int) * 2 * d.L);
   cudaMemset(c->s.stat_count, 0, sizeof(double) * d.L * d.E);
   cudaMemset(c->s.stat_wsum, 0, sizeof(double) * d.L * d.E);
   cudaMemset(c->s.stat_phi, 0, sizeof(double) * 4 * d.L * d.E);

@@ -258,14 +258,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   atomicOr(err, 1);
   return false;
 }
-// Bounded wait for the router to have written this layer's fp16 input rows (every router CTA
-// counted in `ready`); false on expiry or when another warp gave up.  The gate_up kernel's
-// shared-expert items read only those rows, so they start on this instead of on the end of
-// the routing.
+// Bounded wait for the inputs of the shared expert's items of this kernel: for gate_up the
+// layer's fp16 input rows (every router CTA counted), for down the shared h (every epilogue
+// warp of every shared gate_up item counted).  False on expiry or when another warp gave up.
+// The shared items start on this instead of on the end of the previous kernels.
+template <int PHASE>
 __device__ __forceinline__ bool wait_ready(const FwdArgs &a, volatile int *abort_flag) {
   if (!a.s.ready) return true;
-  const int *p = a.s.ready + a.layer;
-  const int target = route_ctas(a.T, a.E);
+  const int *p = a.s.ready + 2 * a.layer + (PHASE - 1);
+  const int target = PHASE == 1 ? route_ctas(a.T, a.E) : shared_item_count(0, a.T, a.H, a.I, a.Is) * kEpi;
   if (ld_acquire_gpu(p) >= target) return true;
   const long long t0 = clock64();
   for (;;) {
@@ -352,11 +353,12 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
   const WorkItem *items = (PHASE == 1) ? a.s.items1 : a.s.items2;
   const uint32_t ring = smem_u32(sm) + (uint32_t)L.ring_off;
   const int S = L.slabs;
-  // gate_up: the shared expert's items (the first n_shared) need only the layer's input rows
-  // and are built here; the routed ones, the item count and the list wait for the routing
-  const int n_shared = PHASE == 1 ? shared_item_count(0, a.T, a.H, a.I, a.Is) : 0;
-  int n_items = PHASE == 1 ? 0 : a.s.n_items[PHASE - 1];
-  bool routed_ready = PHASE != 1;
+  // The shared expert's items (the first n_shared of the list) need only their activations
+  // (gate_up: the router's input rows; down: the shared h) and are built here; the routed
+  // ones, the item count and the list wait for the previous kernels to complete.
+  const int n_shared = shared_item_count(PHASE - 1, a.T, a.H, a.I, a.Is);
+  int n_items = 0;
+  bool routed_ready = false;
   RingPos pos;
   // room accounting (the same in every lane); the chunks in flight are kept across the
   // lanes: lane i holds chunk c with c % kRing == i (its slab count, landed barrier and the
@@ -372,15 +374,15 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
     QEntry &e = qu.slot[k % kQueue];
     if (lane == 0) {
       ok = wait_bar(qu.bars + 8 * (kIQE + k % kQueue), ((k / kQueue) & 1) ^ 1, abort_flag, a.s.err);
-      if (ok && PHASE == 1 && k == 0) ok = wait_ready(a, abort_flag);
+      if (ok && k == 0 && n_shared > 0) ok = wait_ready<PHASE>(a, abort_flag);
       if (ok) {
         it = atomicAdd(a.s.work + (PHASE - 1), 1);
         if (it < n_shared) {
-          e.w = work_item(0, it, &n_shared, nullptr, nullptr, a.E, a.T, a.H, a.I, a.Is);
+          e.w = work_item(PHASE - 1, it, &n_shared, nullptr, nullptr, a.E, a.T, a.H, a.I, a.Is);
         } else {
-          if (!routed_ready) {  // the router and the gather kernel have completed
+          if (!routed_ready) {  // the previous kernels (router, gather; gate_up) have completed
             pdl_wait();
-            n_items = a.s.n_items[0];
+            n_items = a.s.n_items[PHASE - 1];
             routed_ready = true;
           }
           if (it >= n_items)
@@ -509,10 +511,10 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
   const uint32_t gx = smem_u32(sm) + (uint32_t)L.gx_off;
   uint32_t b_seq = 0, a_seq = 0, gx_seq[kGxSlots] = {0u, 0u, 0u, 0u};
   bool ok = true;
-  // gate_up: the input rows are the router's (counted ready), the routed rows the gather
-  // kernel's (complete at the end of the grid dependency); the tensor copies of every lane
-  // are ordered after what lane 0 observed
-  bool xh_ready = PHASE != 1, xs_ready = PHASE != 1;
+  // the shared expert's activations are counted ready (router rows, shared h), the routed ones
+  // complete with the grid dependency; the tensor copies of every lane are ordered after what
+  // lane 0 observed
+  bool xh_ready = false, xs_ready = false;
   for (uint32_t k = 0; ok; ++k) {
     WorkItem w;
     ItemView v;
@@ -522,7 +524,7 @@ __device__ void ab_producer(const FwdArgs &a, const BMaps &bm, const TcLayout &L
         pdl_wait();
         xs_ready = true;
       } else {
-        if (lane == 0) ok = wait_ready(a, abort_flag);
+        if (lane == 0) ok = wait_ready<PHASE>(a, abort_flag);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         xh_ready = true;
@@ -978,6 +980,12 @@ __device__ void epilogue(const FwdArgs &a, uint32_t bars, uint32_t tmem, const I
       }
     }
     if (PHASE == 1 && !fin) atomicOr(a.s.err, kErrRange);
+    if (PHASE == 1 && !v.routed && a.s.ready) {  // this warp's rows of the shared h are written
+      fence_proxy_async_global();
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(a.s.ready + 2 * a.layer + 1, 1);
+    }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (kAE + acs));
@@ -1056,19 +1064,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_ffn_kernel(FwdArgs a, TcLayo
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // set up before the previous kernel of the stream has finished; its outputs (work items,
-  // activations) are read only after this.  gate_up waits per role: the shared expert's items
-  // on the router's input rows, the routed items on the completed grid dependency.
+  // set up before the previous kernel of the stream has finished.  Its outputs are read per
+  // role: the shared expert's items start on their counted activations, the routed items on
+  // the completed grid dependency.
   pdl_trigger();
-  if (PHASE == 2) {
-    pdl_wait();
-    // the layer's gate_up kernel has completed: its item counter and ready count start over
-    // for the next layer (whose router runs after this kernel has completed)
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      a.s.work[0] = 0;
-      if (a.s.ready) a.s.ready[a.layer] = 0;
-    }
-  }
   const uint32_t tmem = tmem_slot;
   const ItemQueue qu{queue_slot, bars};
   if (warp < kDq)

@@ -285,9 +285,11 @@ struct Scratch {
   WorkItem *items2;    // down work
   int *n_items;        // [2]
   unsigned *ticket;    // [1 + ceil(Tm/8)] router last-CTA counters: all token groups, then per group
-  int *ready;          // [L] router CTAs that have written layer l's fp16 input rows; the layer's
-                       // gate_up kernel starts the shared expert's items once all have (the
-                       // layer's down kernel resets it); NULL: not counted
+  int *ready;          // [L][2] per layer: [0] router CTAs that have written its fp16 input rows
+                       // (the gate_up kernel starts the shared expert's items once all have),
+                       // [1] gate_up epilogue warps done with a shared item (the down kernel
+                       // starts the shared expert's items once all are); reset with the claim
+                       // counters by the layer's combine kernel.  NULL: not counted
   uint16_t *xh;        // fp16 [Tm][H]: the layer input as the experts read it (normalised under PW_PRENORM)
   uint16_t *xs;        // fp16 [Tm*K][H]: xh rows in expert-sorted slot order
   uint16_t *h_routed;  // fp16 [Tm*K][I]

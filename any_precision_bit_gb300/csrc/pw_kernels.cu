@@ -26,6 +26,17 @@ namespace pw {
 __global__ void __launch_bounds__(256) combine_kernel(FwdArgs a) {
   pdl_trigger();
   pdl_wait();
+  // both expert kernels of the layer have completed: their claim counters and the layer's
+  // ready counts start over (the next expert kernel claims only after the next router has
+  // counted its rows, and that router waits for this kernel)
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    a.s.work[0] = 0;
+    a.s.work[1] = 0;
+    if (a.s.ready) {
+      a.s.ready[2 * a.layer] = 0;
+      a.s.ready[2 * a.layer + 1] = 0;
+    }
+  }
   const int t = blockIdx.x;
   const int h_begin = blockIdx.y * 1024, h_end = min(a.H, h_begin + 1024);
   const int H = a.H, K = a.K;

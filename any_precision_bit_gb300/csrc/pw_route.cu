@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
           fence_proxy_async_global();
           __threadfence();
           __syncthreads();
-          if (tid == 0) atomicAdd(a.s.ready + a.layer, 1);
+          if (tid == 0) atomicAdd(a.s.ready + 2 * a.layer, 1);
         }
       }
     }
@@ -432,8 +432,6 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   const int tiles1 = (2 * a.I + kCtaRows - 1) / kCtaRows;
   const int tiles2 = (a.H + kCtaRows - 1) / kCtaRows;
   const int tc = tok_chunk_for(T);
-  const int tchunks = (T + tc - 1) / tc;
-  const int nsplit = shared_down_splits(a.I, a.Is);
   const int sh1 = shared_item_count(0, T, a.H, a.I, a.Is);
   const int sh2 = shared_item_count(1, T, a.H, a.I, a.Is);
   {
@@ -568,8 +566,6 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   }
   if (tid == 0) {
     *a.s.ticket = 0u;
-    if (a.s.work) a.s.work[1] = 0;  // the down kernel claims its work items from zero (the
-                                    // gate_up counter is reset by the previous down kernel)
   }
 }
 
