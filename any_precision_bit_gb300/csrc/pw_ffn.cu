@@ -359,6 +359,12 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
   const int n_shared = shared_item_count(PHASE - 1, a.T, a.H, a.I, a.Is);
   int n_items = 0;
   bool routed_ready = false;
+  // The weights are read once per launch at decode sizes, the activations by every row tile:
+  // there the weights' lines go first.  A prefill gate_up tile is read by the several token
+  // chunks of its expert, claimed together, and keeps the default policy (evict-first made
+  // its DRAM reads 1.18x the algorithmic bytes instead of 1.05x).
+  const uint64_t stream_policy = l2_evict_first_policy();
+  const bool evict_first = PHASE == 2 || a.T < kPrefillMinT;
   RingPos pos;
   // room accounting (the same in every lane); the chunks in flight are kept across the
   // lanes: lane i holds chunk c with c % kRing == i (its slab count, landed barrier and the
@@ -459,7 +465,12 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
       head += n;
       // the copies first: a barrier's transaction count may run below zero until the expected
       // bytes are announced, and the phase cannot complete before that arrival
-      if (copies) bulk_g2s(ring + ring_add(base, lane_slab, S) * kSlab, src, cbytes, full);
+      if (copies) {
+        if (evict_first)
+          bulk_g2s_hint(ring + ring_add(base, lane_slab, S) * kSlab, src, cbytes, full, stream_policy);
+        else
+          bulk_g2s(ring + ring_add(base, lane_slab, S) * kSlab, src, cbytes, full);
+      }
       if (lane == 0) mbar_arrive_expect_tx(full, tx);
       src += src_step;
     }

@@ -116,12 +116,72 @@ __device__ __forceinline__ void store_item(WorkItem *dst, const WorkItem &w) {
   p[1] = make_int4(w.ntok, w.kc0, w.kc1, w.part);
 }
 
-// Two jobs between the router and the expert kernels, grid-stride over every CTA:
+// The layer's routing statistics, added to the running sums of row a.stat_layer: per expert
+// the number of its (token, k) selections and the sum of their routing weights r (Eq. 1's
+// inputs), and the sums behind Eq. 5's routed-input features (sum r n, sum r n^2, max n; n =
+// the slot token's input norm as the experts read it).  G lanes per expert stride over its
+// slots [offsets[e], offsets[e + 1]) and a shuffle tree adds their sums, so the order is
+// fixed.  An expert holds at most T slots: decode batches take G = 4, larger ones a warp.
+template <int G>
+__device__ void routing_statistics(const FwdArgs &a) {
+  const int E = a.E, lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int sub = lane / G, gl = lane % G;
+  for (int eb = warp * (32 / G); eb < E; eb += nw * (32 / G)) {
+    const int e = eb + sub;
+    const size_t si = (size_t)a.stat_layer * E + (e < E ? e : 0);
+    // the running sums and the slot range load together
+    double st_c = 0., st_w = 0., st_p[4] = {0., 0., 0., 0.};
+    int o0 = 0, o1 = 0;
+    if (e < E && gl == 0) {
+      st_c = a.s.stat_count[si];
+      st_w = a.s.stat_wsum[si];
+      if (a.s.stat_phi)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) st_p[i] = a.s.stat_phi[si * 4 + i];
+    }
+    if (e < E) {
+      o0 = a.s.offsets[e];
+      o1 = a.s.offsets[e + 1];
+    }
+    float wsum = 0.f, s1 = 0.f, s2 = 0.f, mx = 0.f;
+#pragma unroll 4
+    for (int sl = o0 + gl; sl < o1; sl += G) {
+      const float r = a.s.slot_w[sl];
+      const float n = a.s.xnorm[a.s.slot_tok[sl]];
+      wsum += r;
+      s1 = fmaf(r, n, s1);
+      s2 = fmaf(r * n, n, s2);
+      mx = fmaxf(mx, n);
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+      wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    if (e < E && gl == 0) {
+      const int cnt = o1 - o0;
+      a.s.stat_count[si] = st_c + (double)cnt;
+      a.s.stat_wsum[si] = st_w + (double)wsum;
+      if (a.s.stat_phi && cnt > 0) {
+        double *ph = a.s.stat_phi + si * 4;
+        ph[0] = st_p[0] + (double)wsum;
+        ph[1] = st_p[1] + (double)s1;
+        ph[2] = st_p[2] + (double)s2;
+        ph[3] = fmax(st_p[3], (double)mx);
+      }
+    }
+  }
+}
+
+// Three jobs between the router and the expert kernels, grid-stride over every CTA:
 //  * the layer input's rows in expert-sorted slot order (xs[slot] = xh[token of slot]), so
 //    that every routed gate_up work item reads consecutive rows with TMA boxes (16-byte
 //    vectors);
 //  * the work items of both projections, expanded from the router's work-list tables (one
-//    thread per item).
+//    thread per item);
+//  * in the last CTA, the layer's routing statistics.
 // The tables' loads are issued first and land while the rows are copied.
 __global__ void __launch_bounds__(256) gather_kernel(FwdArgs a) {
   pdl_trigger();
@@ -172,6 +232,12 @@ __global__ void __launch_bounds__(256) gather_kernel(FwdArgs a) {
     const int u = i >= n1 ? 1 : 0, iu = u ? i - n1 : i;
     store_item((u ? a.s.items2 : a.s.items1) + iu,
                work_item(u, iu, s_first[u], s_rk[u], s_off, E, a.T, a.H, a.I, a.Is));
+  }
+  if (blockIdx.x == gridDim.x - 1) {
+    if (a.T <= 256)
+      routing_statistics<4>(a);
+    else
+      routing_statistics<32>(a);
   }
 }
 

@@ -9,14 +9,14 @@
 //   last CTA of a    (elected by a per-group atomic ticket once every expert group wrote its
 //   token group      logits) takes softmax and top-K of the group's tokens, one warp each;
 //   last CTA of all  (elected by a second ticket once every token group is ranked) buckets
-//                    the (token, k) pairs by expert in the stable (expert, token, k) order,
-//                    writes the tables of the expert kernels' work lists and adds the
-//                    layer's routing statistics (the inputs of Eq. 1 and Eq. 5).
+//                    the (token, k) pairs by expert in the stable (expert, token, k) order
+//                    and writes the tables of the expert kernels' work lists.
 // The single-CTA tail is short by construction: top-K runs in as many CTAs as there are
 // token groups, the bucket ranks come from warp-private match_any counts and block scans,
-// the work items are expanded from the tables by the many CTAs of the gather kernel, and
-// the global loads of the tail (pairs, bitwidths, running statistics, input norms) are
-// issued in batches so that their latencies overlap instead of adding up.
+// the work items are expanded from the tables by the many CTAs of the gather kernel, which
+// also adds the layer's routing statistics (the inputs of Eq. 1 and Eq. 5) off this path,
+// and the tail's global loads (pairs, bitwidths) are issued in batches so that their
+// latencies overlap instead of adding up.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,23 +40,19 @@ __host__ __device__ inline int route_hchunk(int H) {
   return hc < H ? hc : H;
 }
 
-// Dynamic shared memory of a router launch.  The last CTA reuses it for the pair arrays
-// [ids][weights][slot weights] when they fit, and for [slot input norms][token input norms]
-// after them when those fit too.
+// Dynamic shared memory of a router launch: the staged rows, or the pair arrays [ids][weights]
+// that the last CTA keeps there when they fit in kRtStageBytes (or in the stage, if larger).
 struct RouteSmem {
   int bytes;
   bool pairs;
-  bool norms;
 };
 __host__ __device__ inline RouteSmem route_smem(int T, int K, int H) {
   RouteSmem r;
   const int stage = kRtTok * H * 2 + kRtExp * route_hchunk(H) * 4;
   const int cap = stage > kRtStageBytes ? stage : kRtStageBytes;
-  const int pair_bytes = T * K * 12, norm_bytes = T * K * 16 + T * 4;
+  const int pair_bytes = T * K * 8;
   r.pairs = pair_bytes <= cap;
-  r.norms = norm_bytes <= cap;
-  const int need = r.norms ? norm_bytes : (r.pairs ? pair_bytes : 0);
-  r.bytes = need > stage ? need : stage;
+  r.bytes = r.pairs && pair_bytes > stage ? pair_bytes : stage;
   return r;
 }
 
@@ -156,46 +152,6 @@ __device__ void softmax_topk_warp(const FwdArgs &a, int t, int lane) {
     a.s.w[j] = wv;
     if (a.ids_out) a.ids_out[j] = ik;
     if (a.w_out) a.w_out[j] = wv;
-  }
-}
-
-// Per expert: the sum of its slot weights r and the sums behind Eq. 5's routed-input
-// features (sum r n, sum r n^2, max n; n = the slot token's input norm), G lanes per expert
-// over its slots [offsets[e], offsets[e] + count[e]) in a fixed order.  An expert holds at
-// most T slots: decode batches take G = 4, larger ones a warp.
-template <int G>
-__device__ __forceinline__ void slot_sums(const FwdArgs &a, const RouteSmem &rs, const float *psw,
-                                          const float *s_n, const int *s_cnt, const int *s_off,
-                                          int warp, int lane, float *s_fsum, float (*s_phi)[256]) {
-  const int E = a.E, sub = lane / G, gl = lane % G;
-  for (int eb = warp * (32 / G); eb < E; eb += kRtWarps * (32 / G)) {
-    const int ee = eb + sub;
-    float wsum = 0.f, s1 = 0.f, s2 = 0.f, mx = 0.f;
-    if (ee < E) {
-      const int o1 = s_off[ee] + s_cnt[ee];
-#pragma unroll 4
-      for (int sl = s_off[ee] + gl; sl < o1; sl += G) {
-        const float r = rs.pairs ? psw[sl] : __ldcg(psw + sl);
-        const float n = rs.norms ? s_n[sl] : __ldcg(a.s.xnorm + a.s.slot_tok[sl]);
-        wsum += r;
-        s1 = fmaf(r, n, s1);
-        s2 = fmaf(r * n, n, s2);
-        mx = fmaxf(mx, n);
-      }
-    }
-#pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-      wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
-      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (gl == 0 && ee < E) {
-      s_fsum[ee] = wsum;
-      s_phi[0][ee] = s1;
-      s_phi[1][ee] = s2;
-      s_phi[2][ee] = mx;
-    }
   }
 }
 
@@ -353,22 +309,9 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   const RouteSmem rs = route_smem(T, K, H);
   int *s_ids = reinterpret_cast<int *>(smem_raw);
   float *s_w = reinterpret_cast<float *>(smem_raw) + TK;
-  float *s_sw = reinterpret_cast<float *>(smem_raw) + 2 * TK;
-  float *s_n = reinterpret_cast<float *>(smem_raw) + 3 * TK;   // slot input norms (rs.norms)
-  float *s_xn = reinterpret_cast<float *>(smem_raw) + 4 * TK;  // token input norms (rs.norms)
-  // Loads whose latency overlaps the bucketing: the committed bitwidths of the layer's blocks
-  // and the running statistics of this thread's expert (E <= kRtThreads).
+  // a load whose latency overlaps the bucketing: the committed bitwidths of the layer's blocks
   const BlockDev *tab = a.table + (size_t)a.layer * E * 2;
   const int q1 = tid < E ? tab[2 * tid].q : 0, q2 = tid < E ? tab[2 * tid + 1].q : 0;
-  const size_t si = (size_t)a.stat_layer * E + tid;
-  double st_c = 0., st_w = 0., st_p[4] = {0., 0., 0., 0.};
-  if (tid < E) {
-    st_c = a.s.stat_count[si];
-    st_w = a.s.stat_wsum[si];
-    if (a.s.stat_phi)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) st_p[i] = a.s.stat_phi[si * 4 + i];
-  }
   if (rs.pairs) {  // the pairs were written by other CTAs: read them through L2
     for (int j0 = 0; j0 < TK; j0 += 4 * kRtThreads) {
       int iv[4];
@@ -388,24 +331,18 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
         }
       }
     }
-    if (rs.norms)
-      for (int t = tid; t < T; t += kRtThreads) s_xn[t] = __ldcg(a.s.xnorm + t);
   }
   const int *pid = rs.pairs ? s_ids : a.s.ids;
   const float *pwt = rs.pairs ? s_w : a.s.w;
-  float *psw = rs.pairs ? s_sw : a.s.slot_w;
 
   // bucketing: pair j = (t, k) goes to slot offsets[e] + (rank of j among expert e's pairs)
   __shared__ int s_wc[kRtWarps][256];  // per warp and expert: pairs counted, then first rank
-  __shared__ int s_cnt[256];
   __shared__ int s_off[257];
   __shared__ int s_itm1[257];
   __shared__ int s_itm2[257];
   __shared__ int s_q[2][256];  // bitwidths, then item counts by rank
   __shared__ int s_rk[2][256];  // expert of each rank
   __shared__ int s_wsum[3][kRtWarps];
-  __shared__ float s_fsum[256];
-  __shared__ float s_phi[3][256];  // per expert: sum r n, sum r n^2, max n
   for (int i = tid; i < kRtWarps * 256; i += kRtThreads) (&s_wc[0][0])[i] = 0;
   __syncthreads();
   const unsigned lt = (1u << lane) - 1u;
@@ -454,6 +391,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
     __syncthreads();
     int r1 = 0, r2 = 0;  // ranks in the two orders
     if (tid < E)
+#pragma unroll 8
       for (int e = 0; e < E; ++e) {
         r1 += s_q[0][e] > q1 || (s_q[0][e] == q1 && e < tid);
         r2 += s_q[1][e] > q2 || (s_q[1][e] == q2 && e < tid);
@@ -490,7 +428,6 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
       x2 += s_wsum[2][w];
     }
     if (tid < E) {  // exclusive scans in rank order, by rank
-      s_cnt[tid] = cnt;
       s_off[tid] = x0 - cnt;
       s_itm1[tid] = sh1 + x1 - s_q[0][tid];
       s_itm2[tid] = sh2 + x2 - s_q[1][tid];
@@ -509,14 +446,13 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
   }
   for (int jb = j0; jb < j1; jb += 4 * 32) {
     int ev[4];
-    float wv[4], nv[4];
+    float wv[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int j = jb + 32 * u + lane;
       const bool in = j < j1;
       ev[u] = in ? (rs.pairs ? pid[j] : __ldcg(pid + j)) : -1 - lane;
       wv[u] = in ? (rs.pairs ? pwt[j] : __ldcg(pwt + j)) : 0.f;
-      nv[u] = in && rs.norms ? s_xn[j / K] : 0.f;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -527,8 +463,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
         const int slot = s_off[ee] + s_wc[warp][ee] + __popc(peers & lt);
         a.s.slot_tok[slot] = j / K;
         a.s.pair_slot[j] = slot;
-        psw[slot] = wv[u];
-        if (rs.norms) s_n[slot] = nv[u];
+        a.s.slot_w[slot] = wv[u];
       }
       __syncwarp();
       if (ee >= 0 && (peers & lt) == 0u) s_wc[warp][ee] += __popc(peers);
@@ -545,28 +480,7 @@ __global__ void __launch_bounds__(kRtThreads, 2) route_kernel(FwdArgs a) {
         a.s.ranks[3 * kRankStride + i] = s_rk[1][i];
       }
     }
-  __syncthreads();  // every slot weight and slot norm is in place
-  // per expert: its routing statistics and the sums behind Eq. 5's routed-input features
-  if (T <= 256)
-    slot_sums<4>(a, rs, psw, s_n, s_cnt, s_off, warp, lane, s_fsum, s_phi);
-  else
-    slot_sums<32>(a, rs, psw, s_n, s_cnt, s_off, warp, lane, s_fsum, s_phi);
-  __syncthreads();
-  // the running statistics of this thread's expert (loaded at the start of the tail)
-  if (tid < E) {
-    a.s.stat_count[si] = st_c + (double)s_cnt[tid];
-    a.s.stat_wsum[si] = st_w + (double)s_fsum[tid];
-    if (a.s.stat_phi && s_cnt[tid] > 0) {
-      double *ph = a.s.stat_phi + si * 4;
-      ph[0] = st_p[0] + (double)s_fsum[tid];
-      ph[1] = st_p[1] + (double)s_phi[0][tid];
-      ph[2] = st_p[2] + (double)s_phi[1][tid];
-      ph[3] = fmax(st_p[3], (double)s_phi[2][tid]);
-    }
-  }
-  if (tid == 0) {
-    *a.s.ticket = 0u;
-  }
+  if (tid == 0) *a.s.ticket = 0u;
 }
 
 int launch_route(const FwdArgs &a, void *stream_) {

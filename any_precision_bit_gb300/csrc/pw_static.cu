@@ -57,8 +57,8 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
       sizeof(int) * 2,              // n_items
       sizeof(unsigned) * (1 + (T + 7) / 8),  // tickets: all token groups, then one per group
       sizeof(float) * T,            // inv_rms
-      sizeof(double) * a.E,         // stat_count (discarded)
-      sizeof(double) * a.E,         // stat_wsum (discarded)
+      0,                            // stat_count (the router does not add statistics)
+      0,                            // stat_wsum
       sizeof(uint16_t) * T * a.H,   // xh: the fp16 expert input the router also writes
       sizeof(float) * T,            // xnorm: per-token input norms
       sizeof(float) * T,            // sgate: per-token shared-expert gates (gated layers)
@@ -107,8 +107,8 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   s.n_items = reinterpret_cast<int *>(take(sizes[10]));
   s.ticket = reinterpret_cast<unsigned *>(take(sizes[11]));
   s.inv_rms = reinterpret_cast<float *>(take(sizes[12]));
-  s.stat_count = reinterpret_cast<double *>(take(sizes[13]));
-  s.stat_wsum = reinterpret_cast<double *>(take(sizes[14]));
+  s.stat_count = nullptr;  // the routing statistics are added by the forward's gather kernel
+  s.stat_wsum = nullptr;
   s.xh = reinterpret_cast<uint16_t *>(take(sizes[15]));
   s.xnorm = reinterpret_cast<float *>(take(sizes[16]));
   s.sgate = reinterpret_cast<float *>(take(sizes[17]));
@@ -117,9 +117,7 @@ extern "C" pw_status pw_route_noalloc(pw_ctx *ctx, int layer, const void *x, int
   // a router whose bounded wait for its copies expires records it in the context's own error
   // word (allocated by pw_create), which the next pw_check on the context reports
   s.err = a.s.err;
-  a.s = s;
-  a.stat_layer = 0;  // the statistics go to the discarded slots; a.layer still selects the
-                     // layer's router, bias and page-table bitwidths
+  a.s = s;  // a.layer still selects the layer's router, bias and page-table bitwidths
 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the last-CTA tickets must start at zero; the array keeps whatever the last call left
