@@ -21,28 +21,39 @@
 //     per 128-column chunk the weights into a ring of 2 KB slabs:
 //     the q bit-plane slabs of a routed chunk (lane p copies plane p) or the eight 4 KB K-step
 //     pieces of a dense shared-expert tile (lane t copies piece t).  A chunk takes exactly the
-//     bytes it needs, so low bitwidths keep more chunks in flight;
+//     bytes it needs, so low bitwidths keep more chunks in flight.  A routed chunk's slabs
+//     return to the ring once its dequantising warps have read them; the copies stream with
+//     an L2 evict-first policy (except a prefill gate_up, whose tiles several token chunks
+//     read), so that the activations stay in L2;
 //   * activation producer (1 warp): the B operand tiles, three per-chunk slots of two stages
 //     (64 columns each, 128-byte swizzle), loaded by TMA from row-contiguous buffers (the
 //     layer input gathered into slot order beforehand, h, the shared expert's input and h):
 //     decode, one 16-row box per lane, as many as the item has tokens padded to 16; prefill,
 //     one 128-row box per stage.  TMA keeps every slot's copies in flight at once (16-byte
 //     cp.async gathers stall on one round trip per tile);
-//   * dequantising warps (16, four per tensor-memory lane quarter): each thread owns one row
-//     and 32 columns of the chunk, turns its plane words into fp16 centroids (pw_dq.cuh) and
-//     writes them straight into tensor memory (tcgen05.st), a 4-deep ring of A buffers;
-//   * MMA thread (1 warp): per chunk eight tcgen05.mma (M = 128, N, K = 16) with A read from
-//     tensor memory (routed blocks) or from the slab ring (shared expert), B from shared
-//     memory, the accumulator in one of two tensor-memory buffers; tcgen05.commit releases
-//     the chunk's slabs, A buffer and B tile when the MMAs are done;
+//   * dequantising warps (16: four chunk streams, each with one warp per tensor-memory lane
+//     quarter): stream s takes the routed chunks c with c mod 4 = s; each thread owns one row
+//     and the chunk's 128 columns, turns its plane words into fp16 centroids (pw_dq.cuh) and
+//     writes them straight into tensor memory (tcgen05.st), a 4-deep ring of A buffers, so
+//     that one stream's store wait overlaps the others' arithmetic.  In the GEMV kernel image
+//     they also compute small routed items on the CUDA cores (below the GEMV threshold);
+//   * MMA warp (1 warp): per chunk eight tcgen05.mma (M = 128, N, K = 16), issued by one
+//     elected lane of the converged warp, with A read from tensor memory (routed blocks) or
+//     from the slab ring (shared expert), B from shared memory, the accumulator in one of two
+//     tensor-memory buffers; tcgen05.commit releases the A buffer, the B tile and a dense
+//     chunk's slabs when the MMAs are done;
 //   * epilogue (4 warps, one per lane quarter): tcgen05.ld of the accumulator, then
 //     h = silu(g) * u (gate_up) or the down output, while the next item is being computed.
 //     A down item that covers one K part (the shared expert's down, and at decode sizes a
 //     long routed down) writes that part's partial-sum buffer; the combine kernel adds the
 //     parts in order.
-// Every mbarrier wait is bounded: on expiry the kernel records an error (PW_ERR_TIMEOUT on
-// the host), every role stops, the producers and the MMA thread wait (bounded) for what they
-// issued, and tensor memory is freed before the kernel returns.
+// The shared expert's items lead the work list and depend only on their activations: they
+// start once the router has counted the layer's input rows ready (gate_up) or every shared
+// gate_up item has counted its h written (down), while the routed items wait for the
+// previous kernels to complete (griddepcontrol.wait).
+// Every wait is bounded: on expiry the kernel records an error (PW_ERR_TIMEOUT on the host),
+// every role stops, the producers and the MMA warp wait (bounded) for what they issued, and
+// tensor memory is freed before the kernel returns.
 #include <cuda_runtime.h>
 #include <stdint.h>
 

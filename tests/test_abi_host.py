@@ -39,6 +39,16 @@ def test_every_declared_symbol_is_exported():
     assert "sm_103a" in pw.pw_version()
 
 
+def test_status_codes_match_the_header():
+    """The binding's status constants and names are the header's enum, value for value."""
+    src = open(os.path.join(ROOT, "include", "pw.h")).read()
+    enum = dict((n, int(v)) for n, v in re.findall(r"\b(PW_(?:OK|ERR_[A-Z]+))\s*=\s*(\d+)", src))
+    assert enum["PW_OK"] == 0 and "PW_ERR_RANGE" in enum and "PW_ERR_TIMEOUT" in enum
+    for name, value in enum.items():
+        assert getattr(pw, name) == value, name
+        assert value == 0 or pw.STATUS_NAMES[value] == name
+
+
 def test_create_rejects_bad_shapes_without_gpu():
     d = pw.pw_desc(L=1, E=8, H=100, I=256, K=2, Is=0, bmax=6, bits_mask=0b1111000, renorm=0, device=0,
                    max_tokens=8, flags=0)
