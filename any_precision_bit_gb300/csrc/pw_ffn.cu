@@ -391,7 +391,18 @@ __device__ void weight_producer(const FwdArgs &a, const TcLayout &L, uint8_t *sm
     QEntry &e = qu.slot[k % kQueue];
     if (lane == 0) {
       ok = wait_bar(qu.bars + 8 * (kIQE + k % kQueue), ((k / kQueue) & 1) ^ 1, abort_flag, a.s.err);
-      if (ok && k == 0 && n_shared > 0) ok = wait_ready<PHASE>(a, abort_flag);
+      // The claim counter is reset by the previous layer's combine kernel: the first claim
+      // waits until that is visible, through the ready count (which the router raises only
+      // after that kernel has completed) or, without shared items, the grid dependency.
+      if (ok && k == 0) {
+        if (n_shared > 0) {
+          ok = wait_ready<PHASE>(a, abort_flag);
+        } else {
+          pdl_wait();
+          n_items = a.s.n_items[PHASE - 1];
+          routed_ready = true;
+        }
+      }
       if (ok) {
         it = atomicAdd(a.s.work + (PHASE - 1), 1);
         if (it < n_shared) {
