@@ -62,7 +62,7 @@ PREFILL_MIN_T = 512  # batches of at least this many tokens run the prefill tili
 # Taken on the two-layer Qwen-shaped decode run (T = 64) and the one-layer Mixtral-shaped
 # prefill run (T = 4096) of the current kernels (profiles/ names the commands); to be measured
 # again whenever the expert kernels change.
-TRAFFIC_PER_ALGORITHMIC_BYTE = {(1, False): 1.031, (2, False): 1.029, (1, True): 1.320, (2, True): 2.720}
+TRAFFIC_PER_ALGORITHMIC_BYTE = {(1, False): 1.025, (2, False): 1.027, (1, True): 1.321, (2, True): 2.469}
 
 
 def peaks():
