@@ -258,9 +258,9 @@ def test_gated_shared_expert(name, T, prenorm):
         pw.pw_destroy(ctx)
 
 
-# decode batches (one thread per expert), a prefill batch whose slot norms sit in shared
-# memory, and one whose pairs are too many for it (the sums read the slots from memory)
-@pytest.mark.parametrize("name,T,prenorm", [("qwen", 16, False), ("qwen", 16, True),
+# decode batches, one token to sixteen (four lanes per expert), and prefill batches (a warp
+# per expert)
+@pytest.mark.parametrize("name,T,prenorm", [("qwen", 1, True), ("qwen", 16, False), ("qwen", 16, True),
                                             ("qwen", 600, True), ("g128", 1100, False)])
 def test_routed_input_features_match_eq5(name, T, prenorm):
     """Eq. 5's phi per expert from the device sums, against the oracle's definition on the
