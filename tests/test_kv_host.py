@@ -290,3 +290,77 @@ def test_request_schedule_is_well_formed():
     assert len(seen) > 30 and demand[0] == 0
     peak = int(np.argmax(demand))
     assert 0.3 * steps < peak < 0.7 * steps and demand[-1] < 0.2 * demand[peak]
+
+
+def test_request_schedule_served_through_the_allocator():
+    """The paging run's serving loop on the CPU: the seeded request schedule served by the C
+    allocator and by the oracle's accounting in step (a request whose arrival or growth does
+    not fit is dropped), the planner reading F_blk from the allocator every step and its
+    plan setting the weight bytes (offloads retire one step later, as pages do once their
+    copy has landed).  Both planners (pw_plan_host and the oracle's) agree at every step; the
+    demand peak drives offloads and the drain reloads."""
+    from synthetic import gen_kv_requests, gen_planner_offline_np
+    rng = np.random.default_rng(5)
+    bits, q, q_init, utype, layer, expert, M, L, E = _problem(rng)
+    n = len(q)
+    off = gen_planner_offline_np(n, list(range(len(bits))), 4, 5)
+    off["n_stages"] = 3
+    mass = rng.dirichlet(np.ones(E), size=L)
+    phi = np.abs(rng.normal(1.0, 0.5, size=(n, 3)))
+    T_blk, R, steps = 4, 2, 200
+    schedule = gen_kv_requests(steps, 0)
+    live, peak = {}, 0
+    for events in schedule:
+        for ev in events:
+            if ev[0] == "finish":
+                live.pop(ev[1])
+            elif ev[0] in ("arrive", "grow"):
+                live[ev[1]] = live.get(ev[1], 0) + ev[2]
+        peak = max(peak, sum(live.values()))
+    full = _weight_bytes(bits, q, M)
+    B_KV = int(0.3 * full / peak)
+    S = full + (T_blk + R) * B_KV
+    lib, ref = Lib(S, B_KV), okv.KVAllocator(S, B_KV)
+    q_c, pending, dropped, kinds, weights = q.copy(), [], set(), [], []
+    try:
+        for step in range(steps):
+            for i, b in pending:  # offloads retire at the next step's commit
+                q_c[i] = b
+            pending = []
+            w = _weight_bytes(bits, q_c, M)
+            lib.set_weight_bytes(w)
+            ref.set_weight_bytes(w)
+            for ev in schedule[step]:
+                kind, r = ev[0], ev[1]
+                if r in dropped:
+                    continue
+                if kind == "finish":
+                    assert apply(lib, "release", r, 0) == apply(ref, "release", r, 0)
+                elif kind == "announce":
+                    apply(lib, "announce", r, ev[2])
+                    apply(ref, "announce", r, ev[2])
+                else:
+                    out = apply(lib, "grow", r, ev[2])
+                    assert out == apply(ref, "grow", r, ev[2])
+                    if out == "error":
+                        dropped.add(r)
+                        apply(lib, "release", r, 0)
+                        apply(ref, "release", r, 0)
+            assert lib.stats() == ref.stats()
+            F = lib.stats()["free_blocks"]
+            obs = dict(T_blk=T_blk, F_blk=F, B_KV=float(B_KV), R=R, mass=mass, phi=phi)
+            got = pw.pw_plan_host(bits, q_c, q_init, utype, layer, expert, M, L, E, obs, off)
+            D, want = _oracle_plan(bits, q_c, q_init, utype, layer, expert, M, mass, phi, off, T_blk, F, B_KV, R)
+            assert got["D"] == D and got["entries"] == want, step
+            kinds.append(got["kind"])
+            for i, a, b, _ in got["entries"]:
+                if b < a:
+                    pending.append((i, b))
+                else:
+                    q_c[i] = b
+            weights.append(_weight_bytes(bits, q_c, M))
+        assert 1 in kinds and 2 in kinds
+        assert min(weights) < 0.85 * full and weights[-1] > min(weights)
+        assert len(dropped) <= 0.25 * len({ev[1] for evs in schedule for ev in evs})
+    finally:
+        lib.close()
