@@ -13,7 +13,9 @@
 //     contiguous, and the experts come by decreasing bitwidth, ties by expert id; experts
 //     without tokens have no items;
 //   * token ranges are within the batch (shared) or the expert's slots (routed), and each
-//     chunk except an expert's or the batch's last holds tok_chunk_for(T) tokens.
+//     chunk except an expert's or the batch's last holds tok_chunk_for(T) tokens;
+//   * the shared items the expert kernels build by themselves, from their count alone (they
+//     start before the tables exist), are the list's.
 // Exit status 0 when every check passes; the first failure is printed.
 #include <algorithm>
 #include <cstdio>
@@ -83,6 +85,8 @@ int main() {
         rk[r] = e;
       }
       const int n_sh = Is > 0 ? sh_tiles[u] * tchunks * (u ? nsplit : 1) : 0;
+      // the expert kernels count the shared items, and build them, without the tables
+      if (shared_item_count(u, T, H, I, Is) != n_sh) return fail("shared item count", trial, u, -1);
       first[0] = n_sh;
       const int np = u ? dsplit : 1;
       for (int r = 0; r < E; ++r) first[r + 1] = first[r] + tiles[u] * np * ((cnt[rk[r]] + tc - 1) / tc);
@@ -98,6 +102,10 @@ int main() {
         if (w.ntok < 1 || w.ntok > tc) return fail("token count", trial, u, i);
         if (i < n_sh) {
           if (w.kind != 1) return fail("shared items first", trial, u, i);
+          const WorkItem wl = work_item(u, i, &n_sh, nullptr, nullptr, E, T, H, I, Is);
+          if (wl.kind != w.kind || wl.tile != w.tile || wl.tok0 != w.tok0 || wl.ntok != w.ntok || wl.kc0 != w.kc0 ||
+              wl.kc1 != w.kc1 || wl.part != w.part)
+            return fail("shared item built without the tables differs", trial, u, i);
           if (w.tile < 0 || w.tile >= sh_tiles[u] || w.tok0 % tc || w.tok0 / tc >= tchunks)
             return fail("shared tile or chunk", trial, u, i);
           if (w.tok0 + w.ntok > T || (w.tok0 + w.ntok < T && w.ntok != tc)) return fail("shared tokens", trial, u, i);
